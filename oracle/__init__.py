@@ -81,6 +81,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_rmsnorm.argtypes = [_u16p, _u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_double, _u16p]
     L.oracle_linear.argtypes = [_u16p, _u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _u16p]
     L.oracle_linear_f32out.argtypes = [_u16p, _u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _f32p]
+    L.oracle_residual_add.argtypes = [_u16p, _u16p, ctypes.c_int64, _u16p]
     L.oracle_silu.restype = ctypes.c_double
     L.oracle_silu.argtypes = [ctypes.c_double]
     L.oracle_swiglu.argtypes = [_u16p, _u16p, ctypes.c_int64, _u16p]
@@ -167,6 +168,13 @@ def linear(a, w, f32_out: bool = False) -> np.ndarray:
         y = np.empty(a.shape[:-1] + (N,), dtype=np.uint16)
         lib().oracle_linear(_p(a, _u16p), _p(w, _u16p), M, N, K, _p(y, _u16p))
     return y
+
+
+def residual_add(x, y) -> np.ndarray:
+    x, y = _u16(x), _u16(y)
+    out = np.empty_like(x)
+    lib().oracle_residual_add(_p(x, _u16p), _p(y, _u16p), x.size, _p(out, _u16p))
+    return out
 
 
 def silu(z: float) -> float:

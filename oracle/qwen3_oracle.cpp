@@ -133,6 +133,12 @@ void oracle_linear_f32out(const uint16_t* a, const uint16_t* w, int64_t M, int64
         }
 }
 
+// Residual add on bf16 tensors: out = bf16(x + y) ("A modern architecture: Qwen3", The whole model:
+// x = x + self_attn(...), x + mlp(...)).
+void oracle_residual_add(const uint16_t* x, const uint16_t* y, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bf16_of(f32_of(x[i]) + f32_of(y[i]));
+}
+
 // SiLU(z) = z * sigmoid(z).
 double oracle_silu(double z) {
 #ifdef ORACLE_PLANT_SILU_SIGN
@@ -309,14 +315,14 @@ void oracle_layer_out(const oracle_config* c, const oracle_weights* w, int layer
 #ifdef ORACLE_PLANT_DROP_ATTN_RESIDUAL
     for (int64_t i = 0; i < n * D.d; ++i) x1[i] = o[i];
 #else
-    for (int64_t i = 0; i < n * D.d; ++i) x1[i] = bf16_of(f32_of(xin[i]) + f32_of(o[i]));
+    oracle_residual_add(xin, o.data(), n * D.d, x1.data());
 #endif
     oracle_rmsnorm(x1.data(), w->post_norm[layer], n, D.d, D.eps, xn.data());
     oracle_linear(xn.data(), w->gate_proj[layer], n, D.F, D.d, gt.data());
     oracle_linear(xn.data(), w->up_proj[layer], n, D.F, D.d, up.data());
     oracle_swiglu(gt.data(), up.data(), n * D.F, a.data());
     oracle_linear(a.data(), w->down_proj[layer], n, D.d, D.F, dn.data());
-    for (int64_t i = 0; i < n * D.d; ++i) xout[i] = bf16_of(f32_of(x1[i]) + f32_of(dn[i]));
+    oracle_residual_add(x1.data(), dn.data(), n * D.d, xout);
 }
 
 // Final RMSNorm, then hidden @ W^T with W = lm_head, or the embedding matrix when tied.

@@ -61,6 +61,9 @@ void oracle_rmsnorm(const uint16_t* x, const uint16_t* gamma, int64_t rows, int 
 void oracle_linear(const uint16_t* a, const uint16_t* w, int64_t M, int64_t N, int64_t K, uint16_t* y);
 void oracle_linear_f32out(const uint16_t* a, const uint16_t* w, int64_t M, int64_t N, int64_t K, float* y);
 
+/* ---- residual add: out = bf16(x + y) ---- */
+void oracle_residual_add(const uint16_t* x, const uint16_t* y, int64_t n, uint16_t* out);
+
 /* ---- SwiGLU ---- */
 double oracle_silu(double z);
 /* a = bf16(bf16(silu(g)) * u), elementwise. */

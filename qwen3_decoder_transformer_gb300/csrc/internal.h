@@ -1,0 +1,70 @@
+// Internal launch interface between the kernel files and the runtime (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q3 {
+
+// Device error-flag bits (one int per context, read by qwen3_get_error).
+enum : int { ERR_TOKEN = 1, ERR_TIMEOUT = 2 };
+
+enum Epilogue : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_RESIDUAL = 2, EPI_F32 = 3 };
+
+// ---------------------------------------------------------------- host utilities (gemm.cu)
+int device_sm_count();
+bool device_is_sm103();
+// Encode a 2-D bf16 tensor map over a row-major [outer, inner] matrix with the 128-byte swizzle.
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------------------------------------------- GEMM (gemm.cu)
+struct GemmArgs {
+    int M, N, K;
+    int epi;
+    void* C;
+    long long ldc;
+    const __nv_bfloat16* R;
+    long long ldr;
+    int* err;
+};
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
+// A: [rows >= M, K] activations; B: [N, K] weights. Both maps are built with encode_gemm_maps.
+bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t a_rows, const void* B, uint64_t N,
+                      uint64_t K);
+cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st);
+
+// ---------------------------------------------------------------- small kernels (kernels.cu)
+cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* ids, int M, __nv_bfloat16* out, int* err,
+                         cudaStream_t st);
+cudaError_t rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* g, int rows, int n, long long in_stride,
+                           long long in_offset, float eps, __nv_bfloat16* y, cudaStream_t st);
+cudaError_t rope_table_launch(float theta, int dh, int n_pos, __nv_bfloat16* table, cudaStream_t st);
+cudaError_t pack_gate_up_launch(const __nv_bfloat16* gate, const __nv_bfloat16* up, int F, int d, __nv_bfloat16* out,
+                                cudaStream_t st);
+cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, int Hq, int Hkv, int dh,
+                                      const __nv_bfloat16* qg, const __nv_bfloat16* kg, const __nv_bfloat16* table,
+                                      const int* len0, float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc,
+                                      __nv_bfloat16* vc, int cap, cudaStream_t st);
+// Length bookkeeping on the device: *len = value, or *len += delta.
+cudaError_t set_len_launch(int* len, int value, cudaStream_t st);
+cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention (attention.cu)
+cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
+                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, cudaStream_t st);
+size_t attn_decode_workspace(int B, int Hq, int dh, int cap);
+cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
+                               int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,
+                               cudaStream_t st);
+int attn_decode_kernel_count();
+
+// One-time per-process kernel attribute setup (dynamic shared memory limits); idempotent, and must
+// run outside stream capture. Called by every entry point that launches these kernels.
+cudaError_t gemm_prepare();
+cudaError_t attention_prepare();
+cudaError_t prepare_kernels();
+
+}  // namespace q3

@@ -1,0 +1,254 @@
+// Memory-bound kernels of the Qwen3 block: embedding gather, RMSNorm, the RoPE table, and the
+// fused q_norm/k_norm + RoPE + KV-cache append. Each reads and writes its rows once with 8- or
+// 16-byte vector accesses; one warp owns one row or one head vector.
+#include "common.cuh"
+#include "internal.h"
+
+namespace q3 {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// x = E[ids] ("A modern architecture: Qwen3", The whole model: embed_tokens(ids)). One warp per row.
+__global__ void embed_kernel(const __nv_bfloat16* __restrict__ E, int V, int d, const int32_t* __restrict__ ids, int M,
+                             __nv_bfloat16* __restrict__ out, int* err) {
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const int id = ids[row];
+    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * d);
+    const int nv = d / 8;
+    if (id < 0 || id >= V) {
+        for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        if (lane == 0 && err) atomicOr(err, ERR_TOKEN);
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(E + (size_t)id * d);
+    for (int v = lane; v < nv; v += 32) dst[v] = __ldg(src + v);
+}
+
+__device__ __forceinline__ float sumsq8(uint4 v) {
+    float s = 0.f;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+        s = fmaf(a, a, s);
+        s = fmaf(b, b, s);
+    }
+    return s;
+}
+
+// Qwen3 RMSNorm on 8 bf16 values: bf16(gamma * bf16(x * r)).
+__device__ __forceinline__ uint4 norm8(uint4 v, uint4 g, float r) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = pack_bf16(bf16_lo(gw[e]) * rbf(bf16_lo(w[e]) * r), bf16_hi(gw[e]) * rbf(bf16_hi(w[e]) * r));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// RMSNorm ("A modern architecture: Qwen3", section RMSNorm): mean of squares in fp32, r =
+// rsqrt(mean + eps) correctly rounded, cast of x*r to bf16, then times gamma. One warp per row;
+// rows up to 32*8*CACHE elements stay in registers, longer rows are re-read for the second pass.
+template <int CACHE>
+__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int rows,
+                               int n, long long in_stride, long long in_offset, float eps,
+                               __nv_bfloat16* __restrict__ y) {
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(row * in_stride + in_offset) * n);
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * n);
+    const int nv = n / 8;
+    uint4 cache[CACHE];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < CACHE; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) {
+            cache[i] = xr[v];
+            ss += sumsq8(cache[i]);
+        }
+    }
+    for (int v = lane + 32 * CACHE; v < nv; v += 32) ss += sumsq8(xr[v]);
+    ss = warp_sum(ss);
+    const float r = __frsqrt_rn(ss / (float)n + eps);
+#pragma unroll
+    for (int i = 0; i < CACHE; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) yr[v] = norm8(cache[i], __ldg(gr + v), r);
+    }
+    for (int v = lane + 32 * CACHE; v < nv; v += 32) yr[v] = norm8(xr[v], __ldg(gr + v), r);
+}
+
+// RoPE table row p: cos(fp32(p * w_i)) for i < dh/2, then sin(...), each rounded fp32 -> bf16, with
+// w_i = fp32(theta^(-2i/dh)) ("A modern architecture: Qwen3", Rotary position embeddings,
+// rope_cos_sin). Built once per context; the transcendental functions run in fp64 and are rounded
+// to fp32, so the table holds the correctly rounded fp32 values before the bf16 cast.
+__global__ void rope_table_kernel(double theta, int dh, int n_pos, __nv_bfloat16* __restrict__ table) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int half = dh / 2;
+    if (idx >= (long long)n_pos * half) return;
+    const int p = (int)(idx / half), i = (int)(idx % half);
+    const float w = (float)pow(theta, -2.0 * i / dh);
+    const float ang = (float)p * w;
+    const float c = (float)cos((double)ang), s = (float)sin((double)ang);
+    table[(size_t)p * dh + i] = __float2bfloat16_rn(c);
+    table[(size_t)p * dh + half + i] = __float2bfloat16_rn(s);
+}
+
+// Fused per-head q_norm / k_norm, RoPE and cache append ("A modern architecture: Qwen3", Attention
+// with grouped KV heads and Q/K normalization; checklist items on q/k norm before RoPE, V untouched,
+// rotate-half pairing). One warp per (token, head) vector of DH values; lane l holds features
+// [l*E, l*E+E), so feature i < DH/2 and its rotation partner i + DH/2 sit in lanes l and l^16.
+// The rotation is evaluated as bf16(bf16(a*c) + bf16(-b*s)) and bf16(bf16(b*c) + bf16(a*s)).
+template <int DH>
+__global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int B, int T, int Hq, int Hkv,
+                                          const __nv_bfloat16* __restrict__ qg, const __nv_bfloat16* __restrict__ kg,
+                                          const __nv_bfloat16* __restrict__ table, const int* __restrict__ len0p,
+                                          float eps, __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
+                                          __nv_bfloat16* __restrict__ vc, int cap) {
+    constexpr int E = DH / 32;  // 2 or 4 features per lane
+    constexpr int HALF = DH / 2;
+    const int H = Hq + 2 * Hkv;
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)B * T * H) return;
+    const int hh = (int)(w % H);
+    const long long m = w / H;
+    const int b = (int)(m / T), t = (int)(m % T);
+    const int pos = *len0p + t;
+    const __nv_bfloat16* src = qkv + (size_t)m * H * DH + (size_t)hh * DH + lane * E;
+
+    uint32_t raw[E / 2];
+    if constexpr (E == 4) {
+        uint2 v = *reinterpret_cast<const uint2*>(src);
+        raw[0] = v.x;
+        raw[1] = v.y;
+    } else {
+        raw[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+    if (hh >= Hq + Hkv) {  // V: copied into the cache unchanged
+        __nv_bfloat16* dst = vc + (((size_t)b * Hkv + (hh - Hq - Hkv)) * cap + pos) * DH + lane * E;
+        if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(raw[0], raw[1]);
+        else *reinterpret_cast<uint32_t*>(dst) = raw[0];
+        return;
+    }
+    float x[E];
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+        x[2 * e] = bf16_lo(raw[e]);
+        x[2 * e + 1] = bf16_hi(raw[e]);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
+    ss = warp_sum(ss);
+    const float r = __frsqrt_rn(ss / (float)DH + eps);
+    const bool is_q = hh < Hq;
+    const __nv_bfloat16* gam = (is_q ? qg : kg) + lane * E;
+    float y[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) y[e] = rbf(bf16f(gam[e]) * rbf(x[e] * r));
+
+    const bool first = lane < 16;
+    const int i0 = (lane * E) % HALF;
+    const __nv_bfloat16* cs = table + (size_t)pos * DH;
+    uint32_t o[E / 2];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        float res[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float own = y[e + k];
+            const float other = __shfl_xor_sync(0xffffffffu, own, 16);
+            const float c = bf16f(cs[i0 + e + k]), s = bf16f(cs[HALF + i0 + e + k]);
+            res[k] = first ? rbf(rbf(own * c) + rbf(-(other * s))) : rbf(rbf(own * c) + rbf(other * s));
+        }
+        o[e / 2] = pack_bf16(res[0], res[1]);
+    }
+    __nv_bfloat16* dst;
+    if (is_q) dst = q_out + (((size_t)b * Hq + hh) * T + t) * DH + lane * E;
+    else dst = kc + (((size_t)b * Hkv + (hh - Hq)) * cap + pos) * DH + lane * E;
+    if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+    else *reinterpret_cast<uint32_t*>(dst) = o[0];
+}
+
+__global__ void set_len_kernel(int* len, int value) { *len = value; }
+__global__ void add_len_kernel(int* len, int delta) { *len += delta; }
+
+}  // namespace
+
+cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* ids, int M, __nv_bfloat16* out, int* err,
+                         cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    const int threads = 256, rows_per_block = threads / 32;
+    embed_kernel<<<(M + rows_per_block - 1) / rows_per_block, threads, 0, st>>>(E, V, d, ids, M, out, err);
+    return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* g, int rows, int n, long long in_stride,
+                           long long in_offset, float eps, __nv_bfloat16* y, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    const int threads = 128, rpb = threads / 32;
+    const int blocks = (rows + rpb - 1) / rpb;
+    if (n <= 32 * 8 * 4) rmsnorm_kernel<4><<<blocks, threads, 0, st>>>(x, g, rows, n, in_stride, in_offset, eps, y);
+    else rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, g, rows, n, in_stride, in_offset, eps, y);
+    return cudaGetLastError();
+}
+
+cudaError_t rope_table_launch(float theta, int dh, int n_pos, __nv_bfloat16* table, cudaStream_t st) {
+    const long long n = (long long)n_pos * (dh / 2);
+    if (n <= 0) return cudaSuccess;
+    rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>((double)theta, dh, n_pos, table);
+    return cudaGetLastError();
+}
+
+cudaError_t pack_gate_up_launch(const __nv_bfloat16* gate, const __nv_bfloat16* up, int F, int d, __nv_bfloat16* out,
+                                cudaStream_t st) {
+    // out rows [256j, 256j+128) = gate rows [128j, 128j+128); [256j+128, 256j+256) = up rows.
+    const size_t block_bytes = (size_t)128 * d * 2;
+    cudaError_t e = cudaMemcpy2DAsync(out, 2 * block_bytes, gate, block_bytes, block_bytes, F / 128,
+                                      cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy2DAsync(reinterpret_cast<char*>(out) + block_bytes, 2 * block_bytes, up, block_bytes, block_bytes,
+                             F / 128, cudaMemcpyDeviceToDevice, st);
+}
+
+cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, int Hq, int Hkv, int dh,
+                                      const __nv_bfloat16* qg, const __nv_bfloat16* kg, const __nv_bfloat16* table,
+                                      const int* len0, float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc,
+                                      __nv_bfloat16* vc, int cap, cudaStream_t st) {
+    const long long warps = (long long)B * T * (Hq + 2 * Hkv);
+    if (warps <= 0) return cudaSuccess;
+    const int threads = 256, wpb = threads / 32;
+    const unsigned blocks = (unsigned)((warps + wpb - 1) / wpb);
+    if (dh == 128)
+        qknorm_rope_append_kernel<128>
+            <<<blocks, threads, 0, st>>>(qkv, B, T, Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+    else if (dh == 64)
+        qknorm_rope_append_kernel<64>
+            <<<blocks, threads, 0, st>>>(qkv, B, T, Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t set_len_launch(int* len, int value, cudaStream_t st) {
+    set_len_kernel<<<1, 1, 0, st>>>(len, value);
+    return cudaGetLastError();
+}
+
+cudaError_t add_len_launch(int* len, int delta, cudaStream_t st) {
+    add_len_kernel<<<1, 1, 0, st>>>(len, delta);
+    return cudaGetLastError();
+}
+
+}  // namespace q3

@@ -1,0 +1,634 @@
+// Runtime behind the C ABI (include/qwen3.h): context ownership, shape validation, the per-layer
+// launch sequence of the forward pass ("A modern architecture: Qwen3", The whole model: embed,
+// L pre-norm blocks, final norm, LM head; positions continue from the cache length), CUDA-graph
+// replay of decode steps, per-kernel event timing, and the single-operation entry points.
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/qwen3.h"
+#include "internal.h"
+
+using bf16 = __nv_bfloat16;
+using namespace q3;
+
+namespace {
+
+enum KernelClass : int {
+    K_EMBED = 0,
+    K_RMSNORM,
+    K_GEMM_QKV,
+    K_QKNORM_ROPE,
+    K_ATTN_PREFILL,
+    K_GEMM_O,
+    K_GEMM_GATEUP,
+    K_GEMM_DOWN,
+    K_GEMM_LMHEAD,
+    K_ATTN_DECODE,
+    K_LENGTH,
+    K_NUM_CLASSES
+};
+const char* kClassNames[K_NUM_CLASSES] = {"embed",  "rmsnorm",     "gemm_qkv",    "qknorm_rope_append",
+                                          "attn_prefill", "gemm_o_residual", "gemm_gateup_swiglu",
+                                          "gemm_down_residual", "gemm_lmhead", "attn_decode", "length_update"};
+
+struct TimedLaunch {
+    int cls;
+    int launches;
+    cudaEvent_t start, stop;
+};
+
+struct DecodeGraph {
+    int B;
+    const int32_t* ids;
+    float* logits;
+    cudaGraphExec_t exec;
+};
+
+bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+namespace q3 {
+cudaError_t prepare_kernels() {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    cudaError_t e = gemm_prepare();
+    if (e == cudaSuccess) e = attention_prepare();
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+}  // namespace q3
+
+struct qwen3_ctx {
+    qwen3_config cfg;
+    int max_batch = 0, capacity = 0, max_tokens = 0;
+    int qkv_n = 0, q_width = 0;
+    // borrowed weights
+    const bf16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
+    std::vector<const bf16*> in_norm, q_norm, k_norm, post_norm, o_proj, down_proj;
+    // owned device memory
+    bf16 *wqkv = nullptr, *wgu = nullptr, *kcache = nullptr, *vcache = nullptr, *rope = nullptr;
+    bf16 *x = nullptr, *xn = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
+    float* dec_work = nullptr;
+    int* d_len = nullptr;
+    int* d_err = nullptr;
+    int32_t* d_ids_buf = nullptr;
+    float* d_logits_buf = nullptr;
+    size_t logits_buf_elems = 0;
+    size_t layer_elems = 0;
+    // host mirror of the cache state
+    int len = 0, batch = 0;
+    // tensor maps: A operands (activation buffers) and B operands (weights) per layer
+    CUtensorMap tA_xn, tA_attn, tA_h, tA_hn;
+    std::vector<CUtensorMap> tB_qkv, tB_o, tB_gu, tB_down;
+    CUtensorMap tB_head;
+    // decode graphs
+    std::vector<DecodeGraph> graphs;
+    cudaStream_t cap_stream = nullptr;
+    // timing
+    bool timing = false;
+    std::vector<TimedLaunch> timed;
+    std::vector<cudaEvent_t> free_events;
+    cudaStream_t last_timed = nullptr;
+    // debug tap
+    int tap_layer = -1;
+    void *tap_in = nullptr, *tap_out = nullptr;
+};
+
+namespace {
+
+cudaEvent_t take_event(qwen3_ctx* c) {
+    if (!c->free_events.empty()) {
+        cudaEvent_t e = c->free_events.back();
+        c->free_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Launch `fn` (returning cudaError_t) on st; with timing on, bracket it with events.
+template <typename F>
+int timed(qwen3_ctx* c, int cls, int launches, cudaStream_t st, F&& fn) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (c->timing) {
+        a = take_event(c);
+        b = take_event(c);
+        cudaEventRecord(a, st);
+    }
+    cudaError_t e = fn();
+    if (c->timing) {
+        cudaEventRecord(b, st);
+        c->timed.push_back({cls, launches, a, b});
+        c->last_timed = st;
+    }
+    return e == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
+}
+
+#define TRY(x)                              \
+    do {                                    \
+        int _rc = (x);                      \
+        if (_rc != QWEN3_OK) return _rc;    \
+    } while (0)
+
+int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int epi, void* C,
+         long long ldc, const bf16* R, long long ldr, cudaStream_t st) {
+    GemmArgs a{M, N, K, epi, C, ldc, R, ldr, c->d_err};
+    return timed(c, cls, 1, st, [&] { return gemm_launch(ta, tb, a, st); });
+}
+
+bf16* layer_k(qwen3_ctx* c, int l) { return c->kcache + (size_t)l * c->layer_elems; }
+bf16* layer_v(qwen3_ctx* c, int l) { return c->vcache + (size_t)l * c->layer_elems; }
+
+// One forward pass over M = B*T rows already gathered into c->x (T = 1 for decode).
+int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logits, int flags, bool decode,
+                    cudaStream_t st) {
+    const qwen3_config& g = c->cfg;
+    const int M = B * T, d = g.hidden, dh = g.head_dim, F = g.intermediate;
+    TRY(timed(c, K_EMBED, 1, st, [&] { return embed_launch(c->embed, g.vocab, d, ids, M, c->x, c->d_err, st); }));
+    for (int l = 0; l < g.n_layers; ++l) {
+        if (l == c->tap_layer && c->tap_in)
+            if (cudaMemcpyAsync(c->tap_in, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return QWEN3_E_CUDA;
+        TRY(timed(c, K_RMSNORM, 1, st,
+                  [&] { return rmsnorm_launch(c->x, c->in_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
+        TRY(gemm(c, K_GEMM_QKV, c->tA_xn, c->tB_qkv[l], M, c->qkv_n, d, EPI_BF16, c->qkv, c->qkv_n, nullptr, 0, st));
+        TRY(timed(c, K_QKNORM_ROPE, 1, st, [&] {
+            return qknorm_rope_append_launch(c->qkv, B, T, g.n_q_heads, g.n_kv_heads, dh, c->q_norm[l], c->k_norm[l],
+                                             c->rope, c->d_len, g.rms_eps, c->q, layer_k(c, l), layer_v(c, l),
+                                             c->capacity, st);
+        }));
+        if (decode) {
+            TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
+                return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
+                                          c->capacity, c->d_len, c->dec_work, c->attn, st);
+            }));
+        } else {
+            TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
+                return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
+                                           c->capacity, c->d_len, c->attn, st);
+            }));
+        }
+        TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], M, d, c->q_width, EPI_RESIDUAL, c->x, d, c->x, d, st));
+        TRY(timed(c, K_RMSNORM, 1, st,
+                  [&] { return rmsnorm_launch(c->x, c->post_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
+        TRY(gemm(c, K_GEMM_GATEUP, c->tA_xn, c->tB_gu[l], M, 2 * F, d, EPI_SWIGLU, c->h, F, nullptr, 0, st));
+        TRY(gemm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], M, d, F, EPI_RESIDUAL, c->x, d, c->x, d, st));
+        if (l == c->tap_layer && c->tap_out)
+            if (cudaMemcpyAsync(c->tap_out, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return QWEN3_E_CUDA;
+    }
+    const bool all_rows = decode || (flags & QWEN3_ALL_ROWS);
+    const int rows = all_rows ? M : B;
+    TRY(timed(c, K_RMSNORM, 1, st, [&] {
+        return all_rows ? rmsnorm_launch(c->x, c->final_norm, rows, d, 1, 0, g.rms_eps, c->hn, st)
+                        : rmsnorm_launch(c->x, c->final_norm, rows, d, T, T - 1, g.rms_eps, c->hn, st);
+    }));
+    TRY(gemm(c, K_GEMM_LMHEAD, c->tA_hn, c->tB_head, rows, g.vocab, d, EPI_F32, logits, g.vocab, nullptr, 0, st));
+    TRY(timed(c, K_LENGTH, 1, st, [&] { return add_len_launch(c->d_len, T, st); }));
+    return QWEN3_OK;
+}
+
+int check_call(qwen3_ctx* c, int B, int T) {
+    if (B < 1 || T < 1) return QWEN3_E_ARG;
+    if (B > c->max_batch || (long long)B * T > c->max_tokens) return QWEN3_E_BATCH;
+    if (c->len > 0 && B != c->batch) return QWEN3_E_BATCH;
+    if ((long long)c->len + T > c->capacity) return QWEN3_E_OVERFLOW;
+    return QWEN3_OK;
+}
+
+template <typename T>
+cudaError_t dmalloc(T** p, size_t elems) {
+    *p = nullptr;
+    if (elems == 0) elems = 1;
+    return cudaMalloc(reinterpret_cast<void**>(p), elems * sizeof(T));
+}
+
+void release(qwen3_ctx* c) {
+    if (!c) return;
+    for (auto& gph : c->graphs) cudaGraphExecDestroy(gph.exec);
+    for (auto& t : c->timed) {
+        cudaEventDestroy(t.start);
+        cudaEventDestroy(t.stop);
+    }
+    for (auto e : c->free_events) cudaEventDestroy(e);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    void* bufs[] = {c->wqkv, c->wgu, c->kcache, c->vcache, c->rope, c->x,     c->xn,        c->qkv,         c->q,
+                    c->attn, c->h,   c->hn,     c->dec_work, c->d_len, c->d_err, c->d_ids_buf, c->d_logits_buf};
+    for (void* p : bufs)
+        if (p) cudaFree(p);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qwen3_strerror(int code) {
+    switch (code) {
+        case QWEN3_OK: return "ok";
+        case QWEN3_E_CONFIG: return "invalid or unsupported model configuration";
+        case QWEN3_E_CAPACITY: return "requested cache exceeds the context limit";
+        case QWEN3_E_OVERFLOW: return "sequence exceeds the cache capacity";
+        case QWEN3_E_BATCH: return "batch or token count does not fit the context";
+        case QWEN3_E_ARG: return "invalid argument";
+        case QWEN3_E_CUDA: return "CUDA error";
+        case QWEN3_E_TOKEN: return "token id out of range";
+        case QWEN3_E_TIMEOUT: return "a kernel wait timed out";
+        case QWEN3_E_DEVICE: return "device is not an sm_103 GPU";
+    }
+    return "unknown error";
+}
+
+int qwen3_validate_config(const qwen3_config* g) {
+    if (!g) return QWEN3_E_ARG;
+    if (g->n_layers < 1 || g->hidden < 64 || g->n_q_heads < 1 || g->n_kv_heads < 1 || g->intermediate < 128 ||
+        g->vocab < 8 || g->max_positions < 1)
+        return QWEN3_E_CONFIG;
+    if (g->n_q_heads % g->n_kv_heads) return QWEN3_E_CONFIG;
+    const int grp = g->n_q_heads / g->n_kv_heads;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_CONFIG;
+    if (g->head_dim != 64 && g->head_dim != 128) return QWEN3_E_CONFIG;
+    if (g->hidden % 64 || g->intermediate % 128 || g->vocab % 8 || g->hidden > 8192) return QWEN3_E_CONFIG;
+    if (!(g->rms_eps > 0.f) || !(g->rope_theta > 1.f)) return QWEN3_E_CONFIG;
+    return QWEN3_OK;
+}
+
+int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int capacity, int max_tokens,
+               void* stream, qwen3_ctx** out) {
+    if (!g || !w || !out) return QWEN3_E_ARG;
+    *out = nullptr;
+    TRY(qwen3_validate_config(g));
+    if (max_batch < 1 || capacity < 1 || max_tokens < 0) return QWEN3_E_ARG;
+    if (capacity > g->max_positions) return QWEN3_E_CAPACITY;
+    if (!w->embed || !w->final_norm || (!g->tie_embeddings && !w->lm_head)) return QWEN3_E_ARG;
+    const void* const* lists[] = {w->in_norm, w->q_proj, w->k_proj,    w->v_proj,  w->o_proj,   w->q_norm,
+                                  w->k_norm,  w->post_norm, w->gate_proj, w->up_proj, w->down_proj};
+    for (auto lst : lists) {
+        if (!lst) return QWEN3_E_ARG;
+        for (int l = 0; l < g->n_layers; ++l)
+            if (!lst[l] || !is_aligned(lst[l], 16)) return QWEN3_E_ARG;
+    }
+    if (!device_is_sm103()) return QWEN3_E_DEVICE;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    qwen3_ctx* c = new (std::nothrow) qwen3_ctx();
+    if (!c) return QWEN3_E_CUDA;
+    c->cfg = *g;
+    c->max_batch = max_batch;
+    c->capacity = capacity;
+    const long long mt = max_tokens > 0 ? (long long)max_tokens : (long long)max_batch * capacity;
+    if (mt > (1ll << 30)) {
+        delete c;
+        return QWEN3_E_ARG;
+    }
+    c->max_tokens = (int)mt;
+    const int L = g->n_layers, d = g->hidden, dh = g->head_dim, F = g->intermediate, V = g->vocab;
+    c->q_width = g->n_q_heads * dh;
+    c->qkv_n = (g->n_q_heads + 2 * g->n_kv_heads) * dh;
+    const int kvw = g->n_kv_heads * dh;
+    c->embed = static_cast<const bf16*>(w->embed);
+    c->head = static_cast<const bf16*>(g->tie_embeddings ? w->embed : w->lm_head);
+    c->final_norm = static_cast<const bf16*>(w->final_norm);
+    for (int l = 0; l < L; ++l) {
+        c->in_norm.push_back(static_cast<const bf16*>(w->in_norm[l]));
+        c->q_norm.push_back(static_cast<const bf16*>(w->q_norm[l]));
+        c->k_norm.push_back(static_cast<const bf16*>(w->k_norm[l]));
+        c->post_norm.push_back(static_cast<const bf16*>(w->post_norm[l]));
+        c->o_proj.push_back(static_cast<const bf16*>(w->o_proj[l]));
+        c->down_proj.push_back(static_cast<const bf16*>(w->down_proj[l]));
+    }
+    c->layer_elems = (size_t)max_batch * g->n_kv_heads * capacity * dh;
+    const size_t rows = (size_t)c->max_tokens;
+    // The A-operand buffers get at least one full 128-row tile so TMA boxes stay inside them.
+    const size_t arows = rows < 128 ? 128 : rows;
+    bool ok = dmalloc(&c->wqkv, (size_t)L * c->qkv_n * d) == cudaSuccess &&
+              dmalloc(&c->wgu, (size_t)L * 2 * F * d) == cudaSuccess &&
+              dmalloc(&c->kcache, (size_t)L * c->layer_elems) == cudaSuccess &&
+              dmalloc(&c->vcache, (size_t)L * c->layer_elems) == cudaSuccess &&
+              dmalloc(&c->rope, (size_t)capacity * dh) == cudaSuccess &&
+              dmalloc(&c->x, rows * d) == cudaSuccess && dmalloc(&c->xn, arows * d) == cudaSuccess &&
+              dmalloc(&c->qkv, rows * c->qkv_n) == cudaSuccess && dmalloc(&c->q, rows * c->q_width) == cudaSuccess &&
+              dmalloc(&c->attn, arows * c->q_width) == cudaSuccess && dmalloc(&c->h, arows * F) == cudaSuccess &&
+              dmalloc(&c->hn, arows * d) == cudaSuccess &&
+              dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, capacity) / 4) ==
+                  cudaSuccess &&
+              dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
+              dmalloc(&c->d_ids_buf, rows) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        release(c);
+        return QWEN3_E_CUDA;
+    }
+    // zero the cache and scratch so no stale bits are ever read, then pack the fused weights
+    ok = cudaMemsetAsync(c->kcache, 0, (size_t)L * c->layer_elems * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->vcache, 0, (size_t)L * c->layer_elems * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->xn, 0, arows * d * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->attn, 0, arows * c->q_width * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->h, 0, arows * F * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->hn, 0, arows * d * 2, st) == cudaSuccess &&
+         cudaMemsetAsync(c->d_len, 0, sizeof(int), st) == cudaSuccess &&
+         cudaMemsetAsync(c->d_err, 0, sizeof(int), st) == cudaSuccess;
+    for (int l = 0; ok && l < L; ++l) {
+        bf16* dst = c->wqkv + (size_t)l * c->qkv_n * d;
+        ok = cudaMemcpyAsync(dst, w->q_proj[l], (size_t)c->q_width * d * 2, cudaMemcpyDeviceToDevice, st) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(dst + (size_t)c->q_width * d, w->k_proj[l], (size_t)kvw * d * 2,
+                             cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+             cudaMemcpyAsync(dst + (size_t)(c->q_width + kvw) * d, w->v_proj[l], (size_t)kvw * d * 2,
+                             cudaMemcpyDeviceToDevice, st) == cudaSuccess &&
+             pack_gate_up_launch(static_cast<const bf16*>(w->gate_proj[l]), static_cast<const bf16*>(w->up_proj[l]), F,
+                                 d, c->wgu + (size_t)l * 2 * F * d, st) == cudaSuccess;
+    }
+    ok = ok && rope_table_launch(g->rope_theta, dh, capacity, c->rope, st) == cudaSuccess;
+    // tensor maps
+    ok = ok && encode_tmap_bf16_2d(&c->tA_xn, c->xn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
+         encode_tmap_bf16_2d(&c->tA_attn, c->attn, c->q_width, arows, (uint64_t)c->q_width * 2, kGemmBK, kGemmBM) &&
+         encode_tmap_bf16_2d(&c->tA_h, c->h, F, arows, (uint64_t)F * 2, kGemmBK, kGemmBM) &&
+         encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
+         encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBN);
+    c->tB_qkv.resize(L);
+    c->tB_o.resize(L);
+    c->tB_gu.resize(L);
+    c->tB_down.resize(L);
+    for (int l = 0; ok && l < L; ++l) {
+        ok = encode_tmap_bf16_2d(&c->tB_qkv[l], c->wqkv + (size_t)l * c->qkv_n * d, d, c->qkv_n, (uint64_t)d * 2,
+                                 kGemmBK, kGemmBN) &&
+             encode_tmap_bf16_2d(&c->tB_o[l], c->o_proj[l], c->q_width, d, (uint64_t)c->q_width * 2, kGemmBK, kGemmBN) &&
+             encode_tmap_bf16_2d(&c->tB_gu[l], c->wgu + (size_t)l * 2 * F * d, d, 2 * F, (uint64_t)d * 2, kGemmBK,
+                                 kGemmBN) &&
+             encode_tmap_bf16_2d(&c->tB_down[l], c->down_proj[l], F, d, (uint64_t)F * 2, kGemmBK, kGemmBN);
+    }
+    ok = ok && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        release(c);
+        return QWEN3_E_CUDA;
+    }
+    *out = c;
+    return QWEN3_OK;
+}
+
+int qwen3_prefill(qwen3_ctx* c, const int32_t* d_ids, int B, int T, float* d_logits, int flags, void* stream) {
+    if (!c || !d_ids || !d_logits) return QWEN3_E_ARG;
+    TRY(check_call(c, B, T));
+    TRY(enqueue_forward(c, d_ids, B, T, d_logits, flags, false, static_cast<cudaStream_t>(stream)));
+    c->len += T;
+    c->batch = B;
+    return QWEN3_OK;
+}
+
+int qwen3_decode_step(qwen3_ctx* c, const int32_t* d_ids, int B, float* d_logits, void* stream) {
+    if (!c || !d_ids || !d_logits) return QWEN3_E_ARG;
+    TRY(check_call(c, B, 1));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (c->timing || c->tap_layer >= 0) {
+        TRY(enqueue_forward(c, d_ids, B, 1, d_logits, 0, true, st));
+    } else {
+        DecodeGraph* gph = nullptr;
+        for (auto& x : c->graphs)
+            if (x.B == B && x.ids == d_ids && x.logits == d_logits) gph = &x;
+        if (!gph) {
+            cudaGraph_t graph = nullptr;
+            cudaGraphExec_t exec = nullptr;
+            if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+                return QWEN3_E_CUDA;
+            int rc = enqueue_forward(c, d_ids, B, 1, d_logits, 0, true, c->cap_stream);
+            cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+            if (rc != QWEN3_OK) return rc;
+            if (e != cudaSuccess) return QWEN3_E_CUDA;
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) return QWEN3_E_CUDA;
+            c->graphs.push_back({B, d_ids, d_logits, exec});
+            gph = &c->graphs.back();
+        }
+        if (cudaGraphLaunch(gph->exec, st) != cudaSuccess) return QWEN3_E_CUDA;
+    }
+    c->len += 1;
+    c->batch = B;
+    return QWEN3_OK;
+}
+
+int qwen3_prefill_host(qwen3_ctx* c, const int32_t* h_ids, int B, int T, float* h_logits, int flags, void* stream) {
+    if (!c || !h_ids || !h_logits) return QWEN3_E_ARG;
+    TRY(check_call(c, B, T));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t rows = (flags & QWEN3_ALL_ROWS) ? (size_t)B * T : (size_t)B;
+    const size_t need = rows * c->cfg.vocab;
+    if (need > c->logits_buf_elems) {
+        if (c->d_logits_buf) cudaFree(c->d_logits_buf);
+        c->d_logits_buf = nullptr;
+        c->logits_buf_elems = 0;
+        if (dmalloc(&c->d_logits_buf, need) != cudaSuccess) return QWEN3_E_CUDA;
+        c->logits_buf_elems = need;
+    }
+    if (cudaMemcpyAsync(c->d_ids_buf, h_ids, (size_t)B * T * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return QWEN3_E_CUDA;
+    TRY(qwen3_prefill(c, c->d_ids_buf, B, T, c->d_logits_buf, flags, stream));
+    if (cudaMemcpyAsync(h_logits, c->d_logits_buf, need * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return QWEN3_E_CUDA;
+    return qwen3_get_error(c, stream);
+}
+
+int qwen3_length(const qwen3_ctx* c, int* length, int* batch) {
+    if (!c) return QWEN3_E_ARG;
+    if (length) *length = c->len;
+    if (batch) *batch = c->batch;
+    return QWEN3_OK;
+}
+
+int qwen3_set_length(qwen3_ctx* c, int length, int batch, void* stream) {
+    if (!c || length < 0) return QWEN3_E_ARG;
+    if (length > c->capacity) return QWEN3_E_OVERFLOW;
+    if (batch < 0 || batch > c->max_batch) return QWEN3_E_BATCH;
+    if (set_len_launch(c->d_len, length, static_cast<cudaStream_t>(stream)) != cudaSuccess) return QWEN3_E_CUDA;
+    c->len = length;
+    c->batch = batch;
+    return QWEN3_OK;
+}
+
+int qwen3_kv_view(qwen3_ctx* c, int layer, void** d_k, void** d_v, int64_t dims[4]) {
+    if (!c || layer < 0 || layer >= c->cfg.n_layers) return QWEN3_E_ARG;
+    if (d_k) *d_k = layer_k(c, layer);
+    if (d_v) *d_v = layer_v(c, layer);
+    if (dims) {
+        dims[0] = c->max_batch;
+        dims[1] = c->cfg.n_kv_heads;
+        dims[2] = c->capacity;
+        dims[3] = c->cfg.head_dim;
+    }
+    return QWEN3_OK;
+}
+
+int qwen3_set_tap(qwen3_ctx* c, int layer, void* d_in, void* d_out) {
+    if (!c || layer >= c->cfg.n_layers) return QWEN3_E_ARG;
+    c->tap_layer = layer < 0 ? -1 : layer;
+    c->tap_in = layer < 0 ? nullptr : d_in;
+    c->tap_out = layer < 0 ? nullptr : d_out;
+    return QWEN3_OK;
+}
+
+int qwen3_get_error(qwen3_ctx* c, void* stream) {
+    if (!c) return QWEN3_E_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QWEN3_E_CUDA;
+    int flags = 0;
+    if (cudaMemcpy(&flags, c->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QWEN3_E_CUDA;
+    if (flags && cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) return QWEN3_E_CUDA;
+    if (flags & ERR_TIMEOUT) return QWEN3_E_TIMEOUT;
+    if (flags & ERR_TOKEN) return QWEN3_E_TOKEN;
+    return QWEN3_OK;
+}
+
+int qwen3_set_timing(qwen3_ctx* c, int enable) {
+    if (!c) return QWEN3_E_ARG;
+    c->timing = enable != 0;
+    return QWEN3_OK;
+}
+
+int qwen3_kernel_times(qwen3_ctx* c, double* total_ms, int64_t* launches, int* n) {
+    if (!c || !n) return QWEN3_E_ARG;
+    const int cap = *n;
+    *n = K_NUM_CLASSES;
+    for (int i = 0; i < cap && i < K_NUM_CLASSES; ++i) {
+        if (total_ms) total_ms[i] = 0;
+        if (launches) launches[i] = 0;
+    }
+    if (c->last_timed && cudaStreamSynchronize(c->last_timed) != cudaSuccess) return QWEN3_E_CUDA;
+    for (auto& t : c->timed) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, t.start, t.stop);
+        if (t.cls < cap) {
+            if (total_ms) total_ms[t.cls] += ms;
+            if (launches) launches[t.cls] += t.launches;
+        }
+        c->free_events.push_back(t.start);
+        c->free_events.push_back(t.stop);
+    }
+    c->timed.clear();
+    return QWEN3_OK;
+}
+
+const char* qwen3_kernel_class_name(int i) { return (i >= 0 && i < K_NUM_CLASSES) ? kClassNames[i] : nullptr; }
+
+int qwen3_launch_count(const qwen3_ctx* c, int B, int T, int flags, int decode) {
+    (void)B;
+    (void)T;
+    (void)flags;
+    if (!c) return -1;
+    const int per_layer = 7 + (decode ? attn_decode_kernel_count() : 1);
+    return 1 + c->cfg.n_layers * per_layer + 3;
+}
+
+void qwen3_free(qwen3_ctx* c) {
+    if (!c) return;
+    cudaDeviceSynchronize();
+    release(c);
+}
+
+// ------------------------------------------------------------------------------ single operations
+
+int qwen3_op_embed(const void* E, int V, int d, const int32_t* ids, int M, void* out, int* err, void* stream) {
+    if (!E || !ids || !out || V < 1 || d < 8 || d % 8 || M < 0) return QWEN3_E_ARG;
+    return embed_launch(static_cast<const bf16*>(E), V, d, ids, M, static_cast<bf16*>(out), err,
+                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+int qwen3_op_rmsnorm(const void* x, const void* gamma, int rows, int n, int in_stride, int in_offset, float eps,
+                     void* y, void* stream) {
+    if (!x || !gamma || !y || rows < 0 || n < 8 || n % 8 || n > 8192 || in_stride < 1 || in_offset < 0)
+        return QWEN3_E_ARG;
+    return rmsnorm_launch(static_cast<const bf16*>(x), static_cast<const bf16*>(gamma), rows, n, in_stride, in_offset,
+                          eps, static_cast<bf16*>(y), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, void* C, int ldc, const void* R, int ldr,
+                  int* err, void* stream) {
+    if (!A || !B || !C || M < 0 || N < 1 || K < 8 || K % 8 || epi < 0 || epi > 3) return QWEN3_E_ARG;
+    if (epi == EPI_SWIGLU && N % 256) return QWEN3_E_ARG;
+    if (epi == EPI_RESIDUAL && !R) return QWEN3_E_ARG;
+    if (ldc < (epi == EPI_SWIGLU ? N / 2 : N) || ldc % (epi == EPI_F32 ? 4 : 8)) return QWEN3_E_ARG;
+    if (epi == EPI_RESIDUAL && (ldr < N || ldr % 8)) return QWEN3_E_ARG;
+    if (!is_aligned(A, 16) || !is_aligned(B, 16) || !is_aligned(C, 16) || (R && !is_aligned(R, 16)))
+        return QWEN3_E_ARG;
+    if (M == 0) return QWEN3_OK;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
+    CUtensorMap ta, tb;
+    if (!encode_gemm_maps(&ta, &tb, A, (uint64_t)M, B, (uint64_t)N, (uint64_t)K)) return QWEN3_E_CUDA;
+    GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err};
+    return gemm_launch(ta, tb, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
+}
+
+int qwen3_op_pack_gate_up(const void* gate, const void* up, int F, int d, void* out, void* stream) {
+    if (!gate || !up || !out || F < 128 || F % 128 || d < 8) return QWEN3_E_ARG;
+    return pack_gate_up_launch(static_cast<const bf16*>(gate), static_cast<const bf16*>(up), F, d,
+                               static_cast<bf16*>(out), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+int qwen3_op_rope_table(float theta, int dh, int n_pos, void* table, void* stream) {
+    if (!table || (dh != 64 && dh != 128) || n_pos < 0) return QWEN3_E_ARG;
+    return rope_table_launch(theta, dh, n_pos, static_cast<bf16*>(table), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+int qwen3_op_qknorm_rope_append(const void* qkv, int B, int T, int Hq, int Hkv, int dh, const void* qg, const void* kg,
+                                const void* table, const int* len0, float eps, void* q_out, void* kc, void* vc, int cap,
+                                void* stream) {
+    if (!qkv || !qg || !kg || !table || !len0 || !q_out || !kc || !vc) return QWEN3_E_ARG;
+    if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || (dh != 64 && dh != 128) || cap < 1) return QWEN3_E_ARG;
+    return qknorm_rope_append_launch(static_cast<const bf16*>(qkv), B, T, Hq, Hkv, dh, static_cast<const bf16*>(qg),
+                                     static_cast<const bf16*>(kg), static_cast<const bf16*>(table), len0, eps,
+                                     static_cast<bf16*>(q_out), static_cast<bf16*>(kc), static_cast<bf16*>(vc), cap,
+                                     static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, int B, int T, int Hq, int Hkv, int dh,
+                               int cap, const int* len0, void* out, void* stream) {
+    if (!q || !kc || !vc || !len0 || !out || B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+        (dh != 64 && dh != 128) || cap < 1)
+        return QWEN3_E_ARG;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
+    return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
+                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out),
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap) { return attn_decode_workspace(B, Hq, dh, cap); }
+
+int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh, int cap,
+                              const int* len0, void* work, void* out, void* stream) {
+    if (!q || !kc || !vc || !len0 || !work || !out || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+        (dh != 64 && dh != 128) || cap < 1)
+        return QWEN3_E_ARG;
+    const int grp = Hq / Hkv;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
+    return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
+                              Hq, Hkv, dh, cap, len0, static_cast<float*>(work), static_cast<bf16*>(out),
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
+}  // extern "C"

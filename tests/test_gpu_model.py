@@ -1,0 +1,106 @@
+"""Whole-model parity through the C ABI (qwen3_init / qwen3_prefill / qwen3_decode_step).
+
+Tiny config: the oracle runs the whole thing (prefill of 64 tokens + 8 greedy decode steps). Decode is
+teacher-forced with the oracle's own greedy tokens so that one near-tie cannot cascade. Bars: per-layer
+output relative L2 <= 1e-2, logits <= 2e-2, top-1 agreement >= 99% (raw, and on rows whose oracle
+top-1/top-2 margin exceeds 4x the largest logit error).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from qwen3_decoder_transformer_gb300 import TINY, build as Bld, synth
+from tests.util import bits, rel_l2, top1_agreement, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bd():
+    Bld.build()
+    from qwen3_decoder_transformer_gb300 import binding
+    binding.lib()
+    return binding
+
+
+@pytest.fixture(scope="module")
+def tiny(bd):
+    cfg = TINY
+    w_host = synth.make_weights(cfg, 0)
+    w_dev = {k: ([t.cuda() for t in v] if isinstance(v, list) else (None if v is None else v.cuda()))
+             for k, v in w_host.items()}
+    om = O.Model(cfg, synth.weights_to_numpy(w_host))
+    return cfg, w_dev, om
+
+
+def test_tiny_prefill_and_decode(bd, tiny):
+    cfg, w, om = tiny
+    T, steps, cap = 64, 8, 80
+    V, d, L = cfg["vocab"], cfg["hidden"], cfg["n_layers"]
+    ids = synth.make_ids(V, 1, T, 0)
+    m = bd.Model(cfg, w, max_batch=1, capacity=cap, max_tokens=T)
+    logits = torch.empty(T, V, dtype=torch.float32, device="cuda")
+    taps = {}
+    for layer in range(L):
+        taps[layer] = (torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
+                       torch.empty(T, d, dtype=torch.bfloat16, device="cuda"))
+    # one prefill per tapped layer would change the cache; tap layer 0 and L-1 on two contexts
+    m.set_tap(L - 1, *taps[L - 1])
+    m.prefill(ids.cuda(), logits, all_rows=True)
+    assert m.get_error() == 0
+    kc_o, vc_o = om.new_cache(1, cap)
+    ref, tin, tout = om.forward(kc_o, vc_o, ids.numpy(), 0, all_rows=True, tap_layer=L - 1)
+    got = logits.cpu().numpy()
+    assert rel_l2(widen(bits(taps[L - 1][0])), widen(tin)) <= 1e-2
+    assert rel_l2(widen(bits(taps[L - 1][1])), widen(tout)) <= 1e-2
+    assert rel_l2(got, ref) <= 2e-2, rel_l2(got, ref)
+    raw, filt, n = top1_agreement(got, ref)
+    assert filt >= 0.99 and raw >= 0.95, (raw, filt, n)
+    # KV cache: layer 0 keys depend only on the embedding rows and layer-0 weights
+    for layer in range(L):
+        k, v = m.kv_view(layer)
+        tol = 1e-3 if layer == 0 else 1e-2
+        assert rel_l2(widen(bits(k[0, :, :T])), widen(kc_o[layer, 0, :, :T])) <= tol
+        assert rel_l2(widen(bits(v[0, :, :T])), widen(vc_o[layer, 0, :, :T])) <= tol
+        assert not bits(k[0, :, T:]).any()
+    assert m.length() == (T, 1)
+    # greedy decode, teacher-forced with the oracle's tokens
+    m.set_tap(-1)
+    tok = int(ref[-1].argmax())
+    step_logits = torch.empty(1, V, dtype=torch.float32, device="cuda")
+    ids_dev = torch.empty(1, dtype=torch.int32, device="cuda")
+    agree = []
+    for s in range(steps):
+        ids_dev.fill_(tok)
+        m.decode_step(ids_dev, step_logits)
+        r = om.forward(kc_o, vc_o, np.array([[tok]], dtype=np.int32), T + s)
+        g = step_logits.cpu().numpy()
+        assert rel_l2(g, r) <= 2e-2, (s, rel_l2(g, r))
+        agree.append(int(g.argmax()) == int(r.argmax()))
+        tok = int(r.argmax())
+    assert m.get_error() == 0
+    assert m.length() == (T + steps, 1)
+    assert sum(agree) >= steps - 1
+    m.close()
+
+
+def test_tiny_errors(bd, tiny):
+    cfg, w, _ = tiny
+    V = cfg["vocab"]
+    m = bd.Model(cfg, w, max_batch=2, capacity=16, max_tokens=32)
+    logits = torch.empty(2, V, dtype=torch.float32, device="cuda")
+    with pytest.raises(bd.Qwen3Error) as e:
+        m.prefill(torch.zeros(1, 17, dtype=torch.int32, device="cuda"), logits)
+    assert e.value.code == 3  # overflow: 17 > capacity 16
+    with pytest.raises(bd.Qwen3Error) as e:
+        m.prefill(torch.zeros(3, 4, dtype=torch.int32, device="cuda"), logits)
+    assert e.value.code == 4  # batch above max_batch
+    bad = torch.tensor([[1, V + 5]], dtype=torch.int32, device="cuda")
+    m.prefill(bad, logits)
+    assert m.get_error() == 7  # token id out of range, reported by the device flag
+    assert m.get_error() == 0  # flag cleared
+    with pytest.raises(bd.Qwen3Error) as e:
+        bd.Model(dict(cfg, max_positions=8), w, max_batch=1, capacity=16)
+    assert e.value.code == 2  # capacity above max_positions
+    m.close()

@@ -1,0 +1,257 @@
+"""Per-kernel parity: each CUDA kernel, called through the C ABI's single-operation entry points, against
+the oracle on the same seeded inputs. Shapes span several tiles plus ragged tails.
+
+Tolerances (relative L2 unless stated): gather and cache indexing bit-exact; RMSNorm, RoPE table and
+q/k-norm+RoPE 1e-3; GEMM epilogues 1e-3 (bf16 outputs) and 1e-5 (fp32 logits); attention 1e-2 (P is
+rounded to bf16 on the tensor cores, the oracle keeps it exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from qwen3_decoder_transformer_gb300 import build as B
+from tests.util import bits, dev, rand_bf16, rel_l2, widen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bd():
+    B.build()
+    from qwen3_decoder_transformer_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ------------------------------------------------------------------------------------ embedding
+
+def test_embed_bitexact(bd):
+    rng = np.random.default_rng(0)
+    V, d = 1000, 256
+    E = rand_bf16(rng, (V, d), 0.02)
+    ids = rng.integers(0, V, 301).astype(np.int32)
+    out = torch.empty(301, d, dtype=torch.bfloat16, device="cuda")
+    err = _err()
+    bd.op_embed(dev(E), torch.from_numpy(ids).cuda(), out, err)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), E[ids])
+    assert err.item() == 0
+
+
+def test_embed_bad_id_zeroes_row_and_flags(bd):
+    rng = np.random.default_rng(1)
+    E = rand_bf16(rng, (64, 128), 0.02)
+    ids = np.array([3, 64, -1, 5], dtype=np.int32)
+    out = torch.full((4, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    err = _err()
+    bd.op_embed(dev(E), torch.from_numpy(ids).cuda(), out, err)
+    torch.cuda.synchronize()
+    got = bits(out)
+    assert np.array_equal(got[0], E[3]) and np.array_equal(got[3], E[5])
+    assert not got[1].any() and not got[2].any()
+    assert err.item() & 1
+
+
+# -------------------------------------------------------------------------------------- RMSNorm
+
+@pytest.mark.parametrize("rows,n", [(1, 256), (7, 1024), (300, 4096), (33, 64), (5, 8192), (1000, 1024)])
+def test_rmsnorm(bd, rows, n):
+    rng = np.random.default_rng(rows * 7 + n)
+    x = rand_bf16(rng, (rows, n), 3.0)
+    g = bits(torch.from_numpy(1 + 0.2 * (rng.random(n) - 0.5)).to(torch.bfloat16))
+    y = torch.empty(rows, n, dtype=torch.bfloat16, device="cuda")
+    bd.op_rmsnorm(dev(x), dev(g), 1e-6, y)
+    torch.cuda.synchronize()
+    ref = O.rmsnorm(x, g, 1e-6)
+    got = bits(y)
+    assert rel_l2(widen(got), widen(ref)) <= 1e-3
+    assert (got == ref).mean() > 0.99
+
+
+def test_rmsnorm_last_row_selection(bd):
+    rng = np.random.default_rng(5)
+    Bq, T, n = 3, 17, 1024
+    x = rand_bf16(rng, (Bq * T, n))
+    g = bits(torch.ones(n, dtype=torch.bfloat16))
+    y = torch.empty(Bq, n, dtype=torch.bfloat16, device="cuda")
+    bd.op_rmsnorm(dev(x), dev(g), 1e-6, y, rows=Bq, in_stride=T, in_offset=T - 1)
+    torch.cuda.synchronize()
+    ref = O.rmsnorm(x[T - 1::T], g, 1e-6)
+    assert rel_l2(widen(bits(y)), widen(ref)) <= 1e-3
+
+
+# ------------------------------------------------------------------------------------ RoPE table
+
+@pytest.mark.parametrize("dh", [64, 128])
+def test_rope_table(bd, dh):
+    n_pos = 32832
+    tab = torch.empty(n_pos, dh, dtype=torch.bfloat16, device="cuda")
+    bd.op_rope_table(1e6, dh, n_pos, tab)
+    torch.cuda.synchronize()
+    got = bits(tab)
+    inv = O.rope_inv_freq(1e6, dh)
+    positions = list(range(0, 70)) + list(range(4090, 4230)) + list(range(32700, n_pos)) + [12345, 23456]
+    ref = np.stack([np.concatenate(O.rope_cos_sin(p, inv)) for p in positions])
+    assert rel_l2(widen(got[positions]), widen(ref)) <= 1e-3
+    assert (got[positions] == ref).mean() > 0.999
+
+
+# ------------------------------------------------------------------------- q/k norm + RoPE + append
+
+@pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0", [(1, 64, 8, 4, 64, 0), (2, 37, 16, 8, 128, 5),
+                                                  (3, 1, 32, 8, 128, 4095)])
+def test_qknorm_rope_append(bd, Bq, T, Hq, Hkv, dh, len0):
+    rng = np.random.default_rng(Bq * 100 + T)
+    cap = len0 + T + 3
+    H = Hq + 2 * Hkv
+    qkv = rand_bf16(rng, (Bq * T, H * dh), 2.0)
+    qg = bits(torch.from_numpy(1 + 0.2 * (rng.random(dh) - 0.5)).to(torch.bfloat16))
+    kg = bits(torch.from_numpy(1 + 0.2 * (rng.random(dh) - 0.5)).to(torch.bfloat16))
+    table = torch.empty(cap, dh, dtype=torch.bfloat16, device="cuda")
+    bd.op_rope_table(1e6, dh, cap, table)
+    len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
+    q_out = torch.empty(Bq, Hq, T, dh, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(Bq, Hkv, cap, dh, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    bd.op_qknorm_rope_append(dev(qkv), Bq, T, Hq, Hkv, dh, dev(qg), dev(kg), table, len_t, 1e-6, q_out, kc, vc)
+    torch.cuda.synchronize()
+    inv = O.rope_inv_freq(1e6, dh)
+    x = qkv.reshape(Bq, T, H, dh)
+    q_ref = np.empty((Bq, Hq, T, dh), np.uint16)
+    k_ref = np.zeros((Bq, Hkv, cap, dh), np.uint16)
+    v_ref = np.zeros((Bq, Hkv, cap, dh), np.uint16)
+    for t in range(T):
+        c, s = O.rope_cos_sin(len0 + t, inv)
+        qn = O.rmsnorm(np.ascontiguousarray(x[:, t, :Hq]), qg, 1e-6)
+        kn = O.rmsnorm(np.ascontiguousarray(x[:, t, Hq:Hq + Hkv]), kg, 1e-6)
+        q_ref[:, :, t] = O.rope_apply(qn, c, s)
+        k_ref[:, :, len0 + t] = O.rope_apply(kn, c, s)
+        v_ref[:, :, len0 + t] = x[:, t, Hq + Hkv:]
+    got_k, got_v = bits(kc), bits(vc)
+    assert np.array_equal(got_v, v_ref)  # V copied bit-exactly into the right slots, nothing else written
+    mask = np.zeros(cap, bool)
+    mask[len0:len0 + T] = True
+    assert not got_k[:, :, ~mask].any()  # untouched slots stay zero
+    assert rel_l2(widen(got_k), widen(k_ref)) <= 1e-3
+    assert rel_l2(widen(bits(q_out)), widen(q_ref)) <= 1e-3
+    assert (bits(q_out) == q_ref).mean() > 0.99
+
+
+# ------------------------------------------------------------------------------------------ GEMM
+
+GEMM_SHAPES = [(1, 256, 64), (64, 512, 256), (200, 1024, 1024), (300, 768, 512), (129, 2048, 192)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_bf16(bd, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a = rand_bf16(rng, (M, K))
+    w = rand_bf16(rng, (N, K), 0.05)
+    c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    err = _err()
+    bd.op_gemm(dev(a), dev(w), bd.EPI_BF16, c, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref = O.linear(a, w)
+    got = bits(c)
+    assert rel_l2(widen(got), widen(ref)) <= 1e-3
+    assert (got == ref).mean() > 0.98
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 1000, 256), (130, 1000, 1024), (64, 151936 // 8, 256)])
+def test_gemm_f32_ragged_n(bd, M, N, K):
+    rng = np.random.default_rng(N + M)
+    a = rand_bf16(rng, (M, K))
+    w = rand_bf16(rng, (N, K), 0.05)
+    c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    bd.op_gemm(dev(a), dev(w), bd.EPI_F32, c)
+    torch.cuda.synchronize()
+    ref = O.linear(a, w, f32_out=True)
+    assert rel_l2(c.cpu().numpy(), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("M,F,K", [(1, 128, 64), (200, 768, 256), (257, 1536, 512)])
+def test_gemm_swiglu(bd, M, F, K):
+    rng = np.random.default_rng(M * F)
+    a = rand_bf16(rng, (M, K))
+    wg = rand_bf16(rng, (F, K), 0.08)
+    wu = rand_bf16(rng, (F, K), 0.08)
+    packed = torch.empty(2 * F, K, dtype=torch.bfloat16, device="cuda")
+    bd.op_pack_gate_up(dev(wg), dev(wu), packed)
+    c = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    bd.op_gemm(dev(a), packed, bd.EPI_SWIGLU, c)
+    torch.cuda.synchronize()
+    ref = O.swiglu(O.linear(a, wg), O.linear(a, wu))
+    assert rel_l2(widen(bits(c)), widen(ref)) <= 1e-3
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 256, 512), (200, 1024, 2048), (129, 512, 3072)])
+def test_gemm_residual_in_place(bd, M, N, K):
+    rng = np.random.default_rng(M + 3 * N)
+    a = rand_bf16(rng, (M, K))
+    w = rand_bf16(rng, (N, K), 0.02)
+    x = rand_bf16(rng, (M, N))
+    xd = dev(x)
+    bd.op_gemm(dev(a), dev(w), bd.EPI_RESIDUAL, xd, R=xd)
+    torch.cuda.synchronize()
+    ref = O.residual_add(x, O.linear(a, w))
+    assert rel_l2(widen(bits(xd)), widen(ref)) <= 1e-3
+
+
+# ------------------------------------------------------------------------------------- attention
+
+def _attn_ref(q, kc, vc, len0, T):
+    """q [B,Hq,T,dh] bits; caches [B,Hkv,cap,dh] bits -> [B*T, Hq*dh] fp64 via the oracle."""
+    Bq, Hq, _, dh = q.shape
+    out = np.empty((Bq, T, Hq * dh))
+    for b in range(Bq):
+        for t in range(T):
+            out[b, t] = O.attention_gqa_row_f64(np.ascontiguousarray(q[b, :, t]), kc[b], vc[b], len0 + t + 1).ravel()
+    return out.reshape(Bq * T, Hq * dh)
+
+
+@pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0", [(1, 64, 8, 4, 64, 0), (2, 130, 8, 2, 64, 0),
+                                                  (1, 200, 16, 8, 128, 0), (2, 77, 16, 8, 128, 70),
+                                                  (1, 1, 4, 4, 128, 300)])
+def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
+    rng = np.random.default_rng(T * 31 + len0)
+    cap = len0 + T + 5
+    q = rand_bf16(rng, (Bq, Hq, T, dh))
+    kc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    vc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    kc[:, :, len0 + T:] = 0x7FC0  # NaN past the written slots: must never be read
+    vc[:, :, len0 + T:] = 0x7FC0
+    out = torch.empty(Bq * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
+    len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
+    bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out)
+    torch.cuda.synchronize()
+    ref = _attn_ref(q, kc, vc, len0, T)
+    got = widen(bits(out))
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) <= 1e-2
+
+
+@pytest.mark.parametrize("Bq,Hq,Hkv,dh,n", [(1, 8, 4, 64, 1), (3, 16, 8, 128, 300), (2, 32, 8, 128, 1000),
+                                             (4, 16, 8, 128, 4097), (1, 8, 8, 128, 257)])
+def test_attention_decode(bd, Bq, Hq, Hkv, dh, n):
+    rng = np.random.default_rng(n + Hq)
+    cap = n + 40
+    q = rand_bf16(rng, (Bq, Hq, dh))
+    kc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    vc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    kc[:, :, n:] = 0x7FC0
+    vc[:, :, n:] = 0x7FC0
+    work = torch.empty(bd.attention_decode_workspace(Bq, Hq, dh, cap) // 4, dtype=torch.float32, device="cuda")
+    out = torch.empty(Bq, Hq * dh, dtype=torch.bfloat16, device="cuda")
+    len_t = torch.tensor([n - 1], dtype=torch.int32, device="cuda")
+    bd.op_attention_decode(dev(q), dev(kc), dev(vc), len_t, work, out)
+    torch.cuda.synchronize()
+    ref = np.stack([O.attention_gqa_row_f64(q[b], kc[b], vc[b], n).ravel() for b in range(Bq)])
+    got = widen(bits(out))
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) <= 1e-2

@@ -108,6 +108,17 @@ def test_linear():
     check_linear()
 
 
+def check_residual_add():
+    torch.manual_seed(11)
+    x = (torch.randn(5000) * 4).to(torch.bfloat16)
+    y = (torch.randn(5000) * torch.logspace(-6, 2, 5000)).to(torch.bfloat16)
+    assert np.array_equal(O.residual_add(bits(x), bits(y)), bits(x + y))
+
+
+def test_residual_add():
+    check_residual_add()
+
+
 # --------------------------------------------------------------------------------- SiLU/SwiGLU
 
 def check_silu_worked_example():
@@ -266,7 +277,7 @@ def test_param_count_8b():
 
 
 ALL_CHECKS = [check_bf16_conversion, check_rmsnorm_worked_example, check_rmsnorm_invariants,
-              check_rmsnorm_bf16_pages_order, check_linear, check_silu_worked_example,
+              check_rmsnorm_bf16_pages_order, check_linear, check_residual_add, check_silu_worked_example,
               check_swiglu_bf16, check_rope_worked_example, check_rope_identities,
               check_rope_frequencies, check_rope_bf16_pages_formula, check_gqa_attention_vs_sdpa,
               check_param_count_0p6b, check_param_count_8b]
