@@ -1,0 +1,396 @@
+"""Benchmark: Qwen3-style decoder prefill throughput on one GB300 (per process), through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one causal prefill (embedding, all layers, final norm, LM head on each sequence's last row)
+of the workload's batch of synthetic token ids, on random-init bf16 weights of the named shape. With
+N > 1 (torchrun, one process per GPU) every rank runs an independent replica ("replicas only": the
+forward pass has no exchange step); value = all ranks' tokens / the slowest rank's time.
+
+Prints one JSON line. ``value`` is device-timed (CUDA events, inputs resident in HBM); ``e2e`` times the
+same step through qwen3_prefill_host with pinned host buffers (ids host->device and logits
+device->host inside the timed region). ``roofline`` is for the kernel class with the largest share of
+the timed region, from per-launch CUDA events recorded by the library on the launch stream.
+``cpu_baseline`` / ``--impl reference`` time the oracle (single-threaded C++) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s and decode-step ms on 1 GB300; % of bf16-tensor / HBM roofline"
+DEFAULT_WORKLOAD = "0.6b-prefill-1x2048"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def kernel_work(cfg: dict, B: int, T: int) -> dict:
+    """Algorithmic FLOPs (tensor-bound classes) or bytes (memory-bound classes) of ONE launch of each
+    kernel class in a prefill of B x T starting at length 0. Causal attention counts the T(T+1)/2
+    visible query/key pairs: 4 * dh FLOPs per pair and query head (QK^T and PV)."""
+    d, dh, F, V = cfg["hidden"], cfg["head_dim"], cfg["intermediate"], cfg["vocab"]
+    hq, hkv = cfg["n_q_heads"], cfg["n_kv_heads"]
+    M = B * T
+    qkv_n = (hq + 2 * hkv) * dh
+    return {
+        "gemm_qkv": ("tensor", 2.0 * M * qkv_n * d),
+        "gemm_o_residual": ("tensor", 2.0 * M * d * hq * dh),
+        "gemm_gateup_swiglu": ("tensor", 2.0 * M * 2 * F * d),
+        "gemm_down_residual": ("tensor", 2.0 * M * d * F),
+        "gemm_lmhead": ("tensor", 2.0 * B * V * d),
+        "attn_prefill": ("tensor", 4.0 * B * hq * dh * T * (T + 1) / 2),
+        "rmsnorm": ("hbm", 2.0 * M * d * 2),
+        "qknorm_rope_append": ("hbm", 2.0 * M * qkv_n * 2),
+        "embed": ("hbm", 2.0 * M * d * 2),
+    }
+
+
+def step_flops(cfg: dict, B: int, T: int) -> float:
+    w = kernel_work(cfg, B, T)
+    L = cfg["n_layers"]
+    per_layer = sum(w[k][1] for k in ("gemm_qkv", "gemm_o_residual", "gemm_gateup_swiglu", "gemm_down_residual",
+                                       "attn_prefill"))
+    return L * per_layer + w["gemm_lmhead"][1]
+
+
+# ----------------------------------------------------------------------------- profiles
+
+def traffic_from_profiles(kernel_class: str, workload: str):
+    """Per-launch DRAM bytes of a kernel class from a committed ncu summary, or None when no summary
+    exists or the kernel source changed after the counters were taken (source hash recorded)."""
+    src = {"gemm": "gemm.cu", "attn": "attention.cu"}.get(kernel_class.split("_")[0], "kernels.cu")
+    path = os.path.join(ROOT, "profiles", f"{kernel_class}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, "qwen3_decoder_transformer_gb300", "csrc", src), "rb").read())
+    if cur.hexdigest()[:16] != h.group(1)[:16]:
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over the process group (identity when not distributed)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle baseline
+
+class OracleBench:
+    """The oracle (single-threaded C++, as it stands) on the workload's weights and token ids."""
+
+    def __init__(self, cfg: dict, seed: int):
+        import oracle as O
+        from qwen3_decoder_transformer_gb300 import synth
+        self.cfg = cfg
+        self.model = O.Model(cfg, synth.weights_to_numpy(synth.make_weights(cfg, seed)))
+        self.ids = synth.make_ids(cfg["vocab"], 1, 64, seed).numpy()
+
+    def run(self, tokens: int) -> float:
+        """Seconds for a full forward pass (all layers + LM head on the last row) of a `tokens` prefix."""
+        kc, vc = self.model.new_cache(1, tokens)
+        t0 = time.perf_counter()
+        self.model.forward(kc, vc, self.ids[:, :tokens], 0)
+        return time.perf_counter() - t0
+
+    def describe(self, tokens: int) -> str:
+        return (f"oracle forward (single-threaded C++, fp64 accumulation, bf16 emulation) of all "
+                f"{self.cfg['n_layers']} layers + LM head on a {tokens}-token prefix of the workload's ids, "
+                f"batch 1; tokens/s = {tokens} / wall time (its attention work is that of the prefix, "
+                f"not of the full sequence)")
+
+
+def flops_per_token(cfg: dict) -> float:
+    d, dh, F = cfg["hidden"], cfg["head_dim"], cfg["intermediate"]
+    per_layer = d * (cfg["n_q_heads"] + 2 * cfg["n_kv_heads"]) * dh + cfg["n_q_heads"] * dh * d + 3 * d * F
+    return 2.0 * cfg["n_layers"] * per_layer
+
+
+def sample_tokens(cfg: dict, budget_flops: float) -> int:
+    """Prefix length whose oracle pass costs about `budget_flops` (the oracle runs ~1-2 GFLOP/s)."""
+    return int(max(1, min(64, budget_flops / flops_per_token(cfg))))
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, wl):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from qwen3_decoder_transformer_gb300 import configs
+    cfg = wl["model"]
+    B, T = wl["prefill"]
+    ob = OracleBench(cfg, wl["seed"])
+    # whole run about 2-3 minutes of single-core work: ~2.5e11 FLOPs shared by the timed steps
+    toks = sample_tokens(cfg, 2.5e11 / max(1, args.steps))
+    for _ in range(args.warmup):
+        ob.run(1)
+    times = [ob.run(toks) for _ in range(args.steps)]
+    v = toks * len(times) / sum(times)
+    desc = ob.describe(toks)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/bf16-storage",
+            "data": "synthetic (random-init weights, uniform token ids)",
+            "config": {"workload": args.workload, "batch": B, "seq_len": T,
+                       "sample": f"{toks}-token prefix per step"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+
+    from qwen3_decoder_transformer_gb300 import binding, build, synth
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    build.build()
+    cfg = wl["model"]
+    B, T = wl["prefill"]
+    V = cfg["vocab"]
+    dev = torch.device("cuda", local)
+    w = synth.make_weights(cfg, wl["seed"], device=dev)
+    ids = synth.make_ids(V, B, T, wl["seed"], device=dev)
+    m = binding.Model(cfg, w, max_batch=B, capacity=T, max_tokens=B * T)
+    logits = torch.empty(B, V, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.set_length(0, 0)
+        m.prefill(ids, logits)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if m.get_error() != 0:
+        raise RuntimeError("device error flag set during warm-up")
+
+    # ---- device-timed region (per-launch events recorded by the library on this stream)
+    m.set_timing(True)
+    m.kernel_times()  # reset
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    kt = m.kernel_times()
+    m.set_timing(False)
+    rc = m.get_error()
+    if rc != 0:
+        raise RuntimeError(f"device error flag {rc} in the timed region")
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    value = world * B * T * args.steps / (elapsed_ms / 1e3)
+
+    # ---- end-to-end through the host-buffer entry point
+    h_ids = torch.empty(B, T, dtype=torch.int32, pin_memory=True)
+    h_ids.copy_(ids.cpu())
+    h_logits = torch.empty(B, V, dtype=torch.float32, pin_memory=True)
+    for _ in range(max(1, args.warmup)):
+        m.set_length(0, 0)
+        m.prefill_host(h_ids.numpy(), h_logits.numpy())
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        m.set_length(0, 0)
+        m.prefill_host(h_ids.numpy(), h_logits.numpy())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e = {"value": world * B * T * args.steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": B * T * 4, "d2h_bytes_per_step": B * V * 4}
+
+    # ---- roofline of the dominant kernel class
+    peaks, peak_src = load_peaks()
+    work = kernel_work(cfg, B, T)
+    per_kernel = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps,
+                      "share": v[0] / max(1e-9, sum(x[0] for x in kt.values()))} for k, v in kt.items() if v[1]}
+    dom = max((k for k in per_kernel if k in work), key=lambda k: kt[k][0])
+    bound, units = work[dom]
+    avg_ms = kt[dom][0] / kt[dom][1]
+    long_region = elapsed_ms > 1000.0
+    if bound == "tensor":
+        achieved = units / (avg_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = units / (avg_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    traffic = traffic_from_profiles(dom, args.workload)
+    roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": f"{peak_src} ({'sustained' if (bound == 'tensor' and long_region) else 'burst'})",
+            "algorithmic_per_launch": units, "avg_launch_ms": avg_ms}
+    step_tf = step_flops(cfg, B, T)
+    launches = m.launch_count(B, T) + 1  # + the length reset before each step
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init bf16 weights N(0,0.02), gains 1+U(-0.1,0.1), uniform token ids)",
+            "config": {"workload": args.workload, "batch": B, "seq_len": T, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: each step streams all weights (%.2f GB) through HBM"
+                             % (sum(t.numel() * 2 for k, t in _flat(w)) / 1e9)},
+            "e2e": e2e, "gpu_launches": launches * args.steps,
+            "roofline": roof,
+            "step_tflops": step_tf / 1e12, "step_frac_of_peak": step_tf / (elapsed_ms / args.steps / 1e3) / 1e12
+            / peaks["bf16_tflops"],
+            "clocks": clk.summary(), "kernels": per_kernel}
+    if world == 1 and not args.no_cpu_baseline:
+        ob = OracleBench(cfg, wl["seed"])
+        toks = sample_tokens(cfg, 1.5e10)
+        dt = ob.run(toks)
+        line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": ob.describe(toks), "seconds": dt}
+    print(json.dumps(line), flush=True)
+    m.close()
+
+
+def _flat(w):
+    for k, v in w.items():
+        if isinstance(v, list):
+            for t in v:
+                if t is not None:
+                    yield k, t
+        elif v is not None:
+            yield k, v
+
+
+def main():
+    from qwen3_decoder_transformer_gb300 import configs
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = configs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()
