@@ -223,6 +223,24 @@ QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, 
                               int Hq, int Hkv, int dh, int cap, const int* d_len0, void* d_work,
                               void* d_out, void* stream);
 
+/* Allocation-free variant of qwen3_op_attention_decode, for callers that cannot call cudaMalloc:
+ * code whose device memory belongs to another allocator (for example a framework's caching pool),
+ * code that must not trigger the device-wide synchronisation an allocation can cause, and code that
+ * may not allocate once it has started. Same arguments and result as qwen3_op_attention_decode,
+ * minus the workspace: the split partials go to a fixed array compiled into this library,
+ * QWEN3_DECODE_NOALLOC_MAX_BYTES (16 MiB) large, which every GPU that loads the library holds until
+ * the process exits. A call whose workspace (qwen3_attention_decode_workspace) is larger returns
+ * QWEN3_E_ARG and launches nothing. The call allocates nothing itself. Its first call on each device
+ * looks up the array's device address with that device current; make that first call before any
+ * stream capture. All calls on a device share the one array and it keeps the last call's contents:
+ * calls that overlap on the GPU (other streams, concurrent graph launches) race and corrupt each
+ * other's results, so serialise them. No part of the array has to start at zero: each call writes
+ * every partial it reads back. The pages have no counterpart to this entry point. */
+#define QWEN3_DECODE_NOALLOC_MAX_BYTES (16u << 20)
+QWEN3_API int qwen3_op_attention_decode_noalloc(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
+                                                int Hq, int Hkv, int dh, int cap, const int* d_len0, void* d_out,
+                                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

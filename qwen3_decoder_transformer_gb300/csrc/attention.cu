@@ -13,6 +13,7 @@
 // K and V (16-byte coalesced loads, 8 in flight per thread). Partial (max, sum, output) triples
 // go to a workspace; a second kernel merges the chunks by log-sum-exp.
 #include <cfloat>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -475,6 +476,38 @@ cudaError_t attention_prepare() {
     cudaError_t e2 = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           FA_BQ * 64 * 2 + 4 * FA_BKV * 64 * 2);
     return e1 != cudaSuccess ? e1 : e2;
+}
+
+}  // namespace q3
+
+namespace q3 {
+
+// Fixed scratch for the allocation-free decode entry point (qwen3_op_attention_decode_noalloc): the
+// split partials of attn_decode_launch live here instead of in a caller workspace. It is part of the
+// library image, so every GPU that loads the library holds it until the process exits.
+constexpr size_t kDecodeNoAllocBytes = 16u << 20;
+static __device__ __align__(256) float g_decode_noalloc_scratch[kDecodeNoAllocBytes / sizeof(float)];
+
+size_t attn_decode_noalloc_max_bytes() { return kDecodeNoAllocBytes; }
+
+// Device address of the fixed scratch on the current device. Looked up once per device, with that
+// device current; host code cannot use the array's name as a device pointer.
+cudaError_t attn_decode_noalloc_scratch(float** ptr) {
+    static std::mutex mu;
+    static float* cached[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        cached[dev] = static_cast<float*>(p);
+    }
+    *ptr = cached[dev];
+    return cudaSuccess;
 }
 
 }  // namespace q3

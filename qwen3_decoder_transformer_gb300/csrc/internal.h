@@ -60,6 +60,10 @@ cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, 
                                int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,
                                cudaStream_t st);
 int attn_decode_kernel_count();
+// Allocation-free decode attention: size of the library's fixed scratch, and its device address on
+// the current device (looked up on first use per device).
+size_t attn_decode_noalloc_max_bytes();
+cudaError_t attn_decode_noalloc_scratch(float** ptr);
 
 // One-time per-process kernel attribute setup (dynamic shared memory limits); idempotent, and must
 // run outside stream capture. Called by every entry point that launches these kernels.

@@ -631,4 +631,21 @@ int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int
                : QWEN3_E_CUDA;
 }
 
+int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh,
+                                      int cap, const int* len0, void* out, void* stream) {
+    if (!q || !kc || !vc || !len0 || !out || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || (dh != 64 && dh != 128) ||
+        cap < 1)
+        return QWEN3_E_ARG;
+    const int grp = Hq / Hkv;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
+    if (attn_decode_workspace(B, Hq, dh, cap) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
+    float* scratch = nullptr;
+    if (attn_decode_noalloc_scratch(&scratch) != cudaSuccess) return QWEN3_E_CUDA;
+    return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
+                              Hq, Hkv, dh, cap, len0, scratch, static_cast<bf16*>(out),
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
 }  // extern "C"
