@@ -277,9 +277,7 @@ def run_ours(args, wl):
     if m.get_error() != 0:
         raise RuntimeError("device error flag set during warm-up")
 
-    # ---- device-timed region (per-launch events recorded by the library on this stream)
-    m.set_timing(True)
-    m.kernel_times()  # reset
+    # ---- device-timed region: the headline value, no per-launch instrumentation
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(world)
@@ -291,13 +289,24 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         barrier(world)
     elapsed_ms = start.elapsed_time(stop)
-    kt = m.kernel_times()
-    m.set_timing(False)
     rc = m.get_error()
     if rc != 0:
         raise RuntimeError(f"device error flag {rc} in the timed region")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     value = world * B * T * args.steps / (elapsed_ms / 1e3)
+
+    # ---- same K steps again with per-launch CUDA events recorded by the library on this stream
+    m.set_timing(True)
+    m.kernel_times()  # reset
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    instrumented_ms = t_start.elapsed_time(t_stop)
+    kt = m.kernel_times()
+    m.set_timing(False)
 
     # ---- end-to-end through the host-buffer entry point
     h_ids = torch.empty(B, T, dtype=torch.int32, pin_memory=True)
@@ -323,7 +332,7 @@ def run_ours(args, wl):
     dom = max((k for k in per_kernel if k in work), key=lambda k: kt[k][0])
     bound, units = work[dom]
     avg_ms = kt[dom][0] / kt[dom][1]
-    long_region = elapsed_ms > 1000.0
+    long_region = instrumented_ms > 1000.0
     if bound == "tensor":
         achieved = units / (avg_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
@@ -352,7 +361,10 @@ def run_ours(args, wl):
             "roofline": roof,
             "step_tflops": step_tf / 1e12, "step_frac_of_peak": step_tf / (elapsed_ms / args.steps / 1e3) / 1e12
             / peaks["bf16_tflops"],
-            "clocks": clk.summary(), "kernels": per_kernel}
+            "clocks": clk.summary(), "kernels": per_kernel,
+            "kernels_note": "per-kernel times from a second run of the same steps with a CUDA event pair around "
+                            "every launch (%.3f ms/step with events vs %.3f without)"
+                            % (instrumented_ms / args.steps, elapsed_ms / args.steps)}
     if world == 1 and not args.no_cpu_baseline:
         ob = OracleBench(cfg, wl["seed"])
         toks = sample_tokens(cfg, 1.5e10)
