@@ -210,10 +210,11 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
 
 /* Causal GQA attention for prefill: for query row t of sequence b (position len0 + t) and query
  * head h, out = softmax(q k^T * dh^-0.5 over cache slots 0..len0+t of kv head h / (Hq/Hkv)) V.
- * q [B, Hq, T, dh]; caches [B, Hkv, cap, dh]; out [B*T, Hq*dh] bf16 (token-major, o_proj input). */
+ * q [B, Hq, T, dh]; caches [B, Hkv, cap, dh] with len0 + T <= cap; out [B*T, Hq*dh] bf16
+ * (token-major, the o_proj input). d_err (may be NULL) receives bit 2 if a bounded wait gave up. */
 QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                                int T, int Hq, int Hkv, int dh, int cap, const int* d_len0,
-                               void* d_out, void* stream);
+                               void* d_out, int* d_err, void* stream);
 
 /* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.

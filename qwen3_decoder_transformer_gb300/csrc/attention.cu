@@ -2,11 +2,8 @@
 // grouped KV heads and Q/K normalization; "Transformer architectures: modern", section 3: query head
 // h reads kv head floor(h / g), g = Hq / Hkv; scores scaled by head_dim^-0.5; causal mask).
 //
-// Prefill: flash attention with an online softmax. A CTA owns 64 query rows of one (sequence,
-// query head); four warps each own 16 rows. K/V tiles of 64 keys stream through a double-buffered,
-// XOR-swizzled shared-memory ring (cp.async); S = Q K^T and O += P V run on the tensor cores
-// (mma.m16n8k16 bf16, fp32 accumulate); P stays in registers as bf16. Tiles above the diagonal are
-// skipped; query tiles are scheduled longest-first.
+// Prefill: flash attention with an online softmax on the 5th-generation tensor cores (tcgen05,
+// accumulators in tensor memory, operands staged by TMA); see the kernel's own comment.
 //
 // Decode: one query per (sequence, query head) against the whole cache. A CTA owns a 256-key
 // chunk of one (sequence, kv head) and serves all g query heads of that group from one read of
@@ -23,217 +20,311 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                                  uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are CH chunks wide, XOR-swizzled
-// on the low three bits so that 8 consecutive rows at one logical chunk hit 8 different banks.
-template <int CH>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)(r * CH * 16 + ((c ^ (r & 7)) * 16));
-}
-
-constexpr int FA_BQ = 64, FA_BKV = 64, FA_THREADS = 128;
+// --------------------------------------------------------------------------- prefill (tcgen05)
+// One CTA = 128 query rows of one (sequence, query head); 6 warps:
+//   warp 0     TMA: the Q tile once, then K_j / V_j tiles (128 keys) into a 2-stage ring.
+//   warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32 TMEM
+//              buffers, O += P_j V_j into a DH-column TMEM accumulator. S_{j+1} is issued before
+//              O += P_j V_j so the tensor cores work on the next scores while softmax runs.
+//   warps 2-5  softmax: thread r owns query row r (TMEM lane r). Online softmax in base 2 with lazy
+//              rescaling: O and l are rescaled only when the running max grows by more than 8
+//              (so P <= 256); P_j is written as bf16 to shared memory in the UMMA K-major 128-byte
+//              swizzled layout (two buffers). At the end each thread normalises its O row.
+// Causal mask and the tail: key k is visible to query t iff k <= len0 + t; tiles wholly above the
+// diagonal are not loaded; V rows past the last valid key are zeroed in shared memory before use so
+// stale cache contents cannot reach O through 0 * NaN.
+constexpr int TC_BM = 128, TC_BN = 128, TC_THREADS = 192, TC_STAGES = 2;
 
 template <int DH>
-__global__ void __launch_bounds__(FA_THREADS)
-    attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
-                        const __nv_bfloat16* __restrict__ vc, int T, int Hq, int Hkv, int cap,
-                        const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out) {
-    constexpr int CH = DH / 8;  // 16-byte chunks per row
-    constexpr int TILE_BYTES = FA_BKV * DH * 2;
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* sQ = smem;
-    uint8_t* sK = smem + FA_BQ * DH * 2;  // 2 stages
-    uint8_t* sV = sK + 2 * TILE_BYTES;    // 2 stages
+struct TcLayout {
+    static constexpr int NCH = DH / 64;             // 64-element (128-byte) column chunks
+    static constexpr int Q_BYTES = TC_BM * DH * 2;  // [NCH][128 rows][128 B]
+    static constexpr int KV_BYTES = TC_BN * DH * 2;
+    static constexpr int P_BYTES = TC_BM * TC_BN * 2;  // [2 chunks][128 rows][128 B]
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + Q_BYTES;
+    static constexpr int V_OFF = K_OFF + TC_STAGES * KV_BYTES;
+    static constexpr int P_OFF = V_OFF + TC_STAGES * KV_BYTES;
+    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;
+};
 
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest (highest) query tiles first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int j = h / (Hq / Hkv);
+template <int DH>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv,
+                           const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out, int* err) {
+    using Ly = TcLayout<DH>;
+    constexpr int NCH = Ly::NCH;
+    constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
+    constexpr uint32_t IDESC_O = idesc_bf16(TC_BM, DH, true);
+    constexpr uint32_t TM_O = 2 * TC_BN;  // O accumulator column base
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR_OFF);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;    // [2]
+    uint64_t* v_full = bars + 3;    // [2]
+    uint64_t* kv_empty = bars + 5;  // [2]
+    uint64_t* s_full = bars + 7;    // [2]
+    uint64_t* p_full = bars + 9;    // [2]
+    uint64_t* o_done = bars + 11;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 13);
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int jkv = h / (Hq / Hkv);
     const int len0 = *len0p;
-    const int q_begin = qt * FA_BQ;
-    const int q_end = min(T, q_begin + FA_BQ);
-    const int n_valid = len0 + q_end;  // keys 0 .. n_valid-1 may be visible to this tile
-    const int n_tiles = (n_valid + FA_BKV - 1) / FA_BKV;
+    const int q0 = qt * TC_BM;
+    const int q_end = min(T, q0 + TC_BM);
+    const int n_valid = len0 + q_end;
+    const int n_tiles = (n_valid + TC_BN - 1) / TC_BN;
 
-    const __nv_bfloat16* qb = q + (((size_t)b * Hq + h) * T) * DH;
-    const __nv_bfloat16* kb = kc + (((size_t)b * Hkv + j) * cap) * DH;
-    const __nv_bfloat16* vb = vc + (((size_t)b * Hkv + j) * cap) * DH;
-
-    // Q tile (rows past T are zero-filled)
-    for (int i = threadIdx.x; i < FA_BQ * CH; i += FA_THREADS) {
-        const int r = i / CH, c = i % CH;
-        const int t = q_begin + r;
-        cp_async16(smem_u32(sQ) + swz<CH>(r, c), qb + (size_t)min(t, T - 1) * DH + c * 8, t < T ? 16 : 0);
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+        }
+        mbar_init(o_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
     }
-    auto load_kv = [&](int tile, int stage) {
-        const int k0 = tile * FA_BKV;
-        for (int i = threadIdx.x; i < FA_BKV * CH; i += FA_THREADS) {
-            const int r = i / CH, c = i % CH;
-            const int s = k0 + r;
-            const int nb = s < n_valid ? 16 : 0;
-            const size_t off = (size_t)min(s, n_valid - 1) * DH + c * 8;
-            cp_async16(smem_u32(sK + stage * TILE_BYTES) + swz<CH>(r, c), kb + off, nb);
-            cp_async16(smem_u32(sV + stage * TILE_BYTES) + swz<CH>(r, c), vb + off, nb);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
-
-    // per-thread rows: g = lane/4 and g+8 within the warp's 16 rows
-    const int g = lane >> 2, cq = lane & 3;
-    const int row0 = q_begin + warp * 16 + g, row1 = row0 + 8;
-    const int p0 = len0 + row0, p1 = len0 + row1;  // absolute positions
-    const float sl2 = kLog2e / sqrtf((float)DH);
-
-    uint32_t qf[DH / 16][4];
-    float o[DH / 8][4];
-#pragma unroll
-    for (int n = 0; n < DH / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int tile = 0; tile < n_tiles; ++tile) {
-        const int stage = tile & 1;
-        if (tile + 1 < n_tiles) load_kv(tile + 1, stage ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (tile == 0) {
-#pragma unroll
-            for (int kk = 0; kk < DH / 16; ++kk) {
-                const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int c = kk * 2 + (lane >> 4);
-                ldmatrix_x4(smem_u32(sQ) + swz<CH>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-            }
-        }
-        const uint32_t kbase = smem_u32(sK + stage * TILE_BYTES), vbase = smem_u32(sV + stage * TILE_BYTES);
-        // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
-        float s[FA_BKV / 8][4];
-#pragma unroll
-        for (int n = 0; n < FA_BKV / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-#pragma unroll
-            for (int np = 0; np < FA_BKV / 16; ++np) {
-                const int r = np * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int c = kk * 2 + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(kbase + swz<CH>(r, c), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], qf[kk], b0, b1);
-                mma_bf16_16816(s[2 * np + 1], qf[kk], b2, b3);
-            }
-        }
-        // causal mask where the tile reaches past the first row's position
-        const int k0 = tile * FA_BKV;
-        if (k0 + FA_BKV - 1 > len0 + q_begin) {
-#pragma unroll
-            for (int n = 0; n < FA_BKV / 8; ++n) {
-                const int key = k0 + n * 8 + 2 * cq;
-                if (key > p0 || key >= n_valid) s[n][0] = -INFINITY;
-                if (key + 1 > p0 || key + 1 >= n_valid) s[n][1] = -INFINITY;
-                if (key > p1 || key >= n_valid) s[n][2] = -INFINITY;
-                if (key + 1 > p1 || key + 1 >= n_valid) s[n][3] = -INFINITY;
-            }
-        }
-        // online softmax (base 2): rows g (s[.][0..1]) and g+8 (s[.][2..3])
-        float mx0 = m0, mx1 = m1;
-#pragma unroll
-        for (int n = 0; n < FA_BKV / 8; ++n) {
-            mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]) * sl2);
-            mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]) * sl2);
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float c0 = exp2f(m0 - mx0), c1 = exp2f(m1 - mx1);  // m = -inf initially -> 0
-        m0 = mx0;
-        m1 = mx1;
-        float rs0 = 0.f, rs1 = 0.f;
-        uint32_t pf[FA_BKV / 16][4];
-#pragma unroll
-        for (int n = 0; n < FA_BKV / 8; ++n) {
-            const float e0 = exp2f(s[n][0] * sl2 - mx0), e1 = exp2f(s[n][1] * sl2 - mx0);
-            const float e2 = exp2f(s[n][2] * sl2 - mx1), e3 = exp2f(s[n][3] * sl2 - mx1);
-            rs0 += e0 + e1;
-            rs1 += e2 + e3;
-            pf[n / 2][(n & 1) * 2 + 0] = pack_bf16(e0, e1);
-            pf[n / 2][(n & 1) * 2 + 1] = pack_bf16(e2, e3);
-        }
-        l0 = l0 * c0 + rs0;
-        l1 = l1 * c1 + rs1;
-#pragma unroll
-        for (int n = 0; n < DH / 8; ++n) {
-            o[n][0] *= c0;
-            o[n][1] *= c0;
-            o[n][2] *= c1;
-            o[n][3] *= c1;
-        }
-        // O += P V: k-steps of 16 keys, n-tiles of 8 head features
-#pragma unroll
-        for (int kk = 0; kk < FA_BKV / 16; ++kk) {
-            const uint32_t a[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
-#pragma unroll
-            for (int np = 0; np < DH / 16; ++np) {
-                const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int c = np * 2 + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(vbase + swz<CH>(r, c), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], a, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], a, b2, b3);
-            }
-        }
-        __syncthreads();  // the stage is reloaded next iteration
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
     }
-    cp_async_wait<0>();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
 
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-    const size_t ld = (size_t)Hq * DH;
-    __nv_bfloat16* ob = out + ((size_t)b * T) * ld + (size_t)h * DH;
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(q_full, Ly::Q_BYTES);
+            for (int c = 0; c < NCH; ++c)
+                tma_load_3d(smem + Ly::Q_OFF + c * TC_BM * 128, &tmQ, q_full, c * 64, q0, b * Hq + h);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmK, &k_full[s], c * 64,
+                                j * TC_BN, b * Hkv + jkv);
+                mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmV, &v_full[s], c * 64,
+                                j * TC_BN, b * Hkv + jkv);
+            }
+        }
+    } else if (warp == 1) {
+        // all lanes walk the schedule (so the warp can zero V tails together); lane 0 issues
+        auto issue_s = [&](int j) -> bool {
+            const int s = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag))) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sq = smem_u32(smem + Ly::Q_OFF), sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
 #pragma unroll
-    for (int n = 0; n < DH / 8; ++n) {
-        const int col = n * 8 + 2 * cq;
-        if (row0 < T)
-            *reinterpret_cast<uint32_t*>(ob + (size_t)row0 * ld + col) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-        if (row1 < T)
-            *reinterpret_cast<uint32_t*>(ob + (size_t)row1 * ld + col) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+                for (int kk = 0; kk < DH / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
+                    umma_bf16_ss(tmem + s * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), IDESC_S,
+                                 kk > 0);
+                }
+                umma_commit(&s_full[s]);
+            }
+            __syncwarp();
+            return true;
+        };
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+        if (ok) ok = issue_s(0);
+        if (ok && n_tiles > 1) ok = issue_s(1);
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const int s = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag))) { ok = false; break; }
+            uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
+            const int r0 = n_valid - j * TC_BN;  // first stale key row of this tile
+            if (r0 < TC_BN) {
+                for (int i = lane; i < (TC_BN - r0) * 8 * NCH; i += 32) {
+                    const int c = i / ((TC_BN - r0) * 8), rem = i % ((TC_BN - r0) * 8);
+                    reinterpret_cast<uint4*>(sv + c * TC_BN * 128 + (r0 + rem / 8) * 128)[rem % 8] =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s], (j >> 1) & 1, abort_flag))) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sp = smem_u32(smem + Ly::P_OFF + s * Ly::P_BYTES), svv = smem_u32(sv);
+#pragma unroll
+                for (int kk = 0; kk < TC_BN / 16; ++kk) {
+                    const uint64_t ad = sdesc_kmajor_sw128(sp + (kk >> 2) * TC_BM * 128 + (kk & 3) * 32);
+                    const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
+                    umma_bf16_ss(tmem + TM_O, ad, bd, IDESC_O, (j | kk) != 0);
+                }
+                umma_commit(o_done);
+                umma_commit(&kv_empty[s]);
+            }
+            __syncwarp();
+            if (j + 2 < n_tiles) ok = issue_s(j + 2);
+        }
+    } else {
+        // softmax warps: thread <-> query row
+        const int quarter = warp & 3, row = quarter * 32 + lane;
+        const int t = q0 + row, pos = len0 + t;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = 1.4426950408889634f / sqrtf((float)DH);
+        float m_used = -INFINITY, l = 0.f;
+        int pv_seen = 0;  // PV completions confirmed so far
+        auto confirm_pv = [&](int upto) -> bool {
+            while (pv_seen < upto) {
+                if (!mbar_wait(o_done, pv_seen & 1, abort_flag)) return false;
+                ++pv_seen;
+            }
+            return true;
+        };
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j & 1;
+            const bool w = mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[TC_BN];
+#pragma unroll
+            for (int c = 0; c < TC_BN / 32; ++c)
+                tmem_ld_32x32b_x32(tmem + lane_off + s * TC_BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tmem_ld_wait();
+            const int k0 = j * TC_BN;
+            const bool need_mask = k0 + TC_BN - 1 > len0 + q0;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < TC_BN; ++i) {
+                float v = __uint_as_float(sr[i]) * sl2;
+                if (need_mask && k0 + i > pos) v = -INFINITY;
+                sr[i] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
+            }
+            // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
+            const bool grow = mx > m_used + 8.0f;
+            const float alpha = grow ? exp2f(m_used - mx) : 1.0f;
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // rescale O once the previous P V product has landed
+                const bool w = confirm_pv(j);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < DH / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                }
+                tmem_st_wait();
+            }
+            if (grow) {
+                l *= alpha;
+                m_used = mx;
+            }
+            // P = exp2(s - m) as bf16, written to the K-major swizzled tile (two 64-key chunks)
+            uint8_t* prow = smem + Ly::P_OFF + s * Ly::P_BYTES + row * 128;
+            float rs = 0.f;
+#pragma unroll
+            for (int u = 0; u < TC_BN / 8; ++u) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = exp2f(__uint_as_float(sr[u * 8 + 2 * e]) - m_used);
+                    const float p1 = exp2f(__uint_as_float(sr[u * 8 + 2 * e + 1]) - m_used);
+                    rs += p0 + p1;
+                    wv[e] = pack_bf16(p0, p1);
+                }
+                const int c = u >> 3, uu = u & 7;
+                *reinterpret_cast<uint4*>(prow + c * TC_BM * 128 + ((uu ^ (row & 7)) * 16)) =
+                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            l += rs;
+            // Observe the previous P V completion before releasing this P: o_done is then never more
+            // than one phase ahead of this thread, so its parity waits stay unambiguous.
+            if (j > 0) {
+                const bool w = confirm_pv(j);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&p_full[s]);
+        }
+        // epilogue: O / l
+        if (ok) ok = confirm_pv(n_tiles);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            __nv_bfloat16* orow = out + (((size_t)b * T + t) * Hq + h) * DH;
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                tmem_ld_wait();
+                if (t < T) {
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        reinterpret_cast<uint4*>(orow + c * 32)[v] =
+                            make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                }
+            }
+        }
     }
+    if (!ok) {
+        *abort_flag = 1;
+        if (err) atomicOr(err, ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------------------------------- decode
 constexpr int DEC_CHUNK = 256, DEC_THREADS = 128, DEC_UNROLL = 8;
-
-__device__ __forceinline__ int dec_splits(int cap) { return (cap + DEC_CHUNK - 1) / DEC_CHUNK; }
 
 // Workspace layout per (b, q-head, split): [m, l] floats, then DH floats of unnormalised output.
 template <int DH, int G>
@@ -436,21 +527,25 @@ cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, co
 
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                              int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, cudaStream_t st) {
-    constexpr int smem = FA_BQ * DH * 2 + 4 * FA_BKV * DH * 2;
-    dim3 grid((T + FA_BQ - 1) / FA_BQ, Hq, B);
-    attn_prefill_kernel<DH><<<grid, FA_THREADS, smem, st>>>(q, kc, vc, T, Hq, Hkv, cap, len0, out);
+                              int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, int* err,
+                              cudaStream_t st) {
+    CUtensorMap tq, tk, tv;
+    if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
+        !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
+        return cudaErrorInvalidValue;
+    dim3 grid((T + TC_BM - 1) / TC_BM, Hq, B);
+    attn_prefill_tc_kernel<DH><<<grid, TC_THREADS, TcLayout<DH>::SMEM, st>>>(tq, tk, tv, T, Hq, Hkv, len0, out, err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out,
+                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
                                 cudaStream_t st) {
     if (B <= 0 || T <= 0) return cudaSuccess;
-    if (dh == 128) return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, st);
-    if (dh == 64) return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, st);
+    if (dh == 128) return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, st);
+    if (dh == 64) return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, st);
     return cudaErrorInvalidValue;
 }
 
@@ -471,10 +566,10 @@ cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, 
 int attn_decode_kernel_count() { return 2; }
 
 cudaError_t attention_prepare() {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          FA_BQ * 128 * 2 + 4 * FA_BKV * 128 * 2);
-    cudaError_t e2 = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          FA_BQ * 64 * 2 + 4 * FA_BKV * 64 * 2);
+    cudaError_t e1 = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          TcLayout<128>::SMEM);
+    cudaError_t e2 = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          TcLayout<64>::SMEM);
     return e1 != cudaSuccess ? e1 : e2;
 }
 

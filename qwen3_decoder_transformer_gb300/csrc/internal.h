@@ -54,7 +54,8 @@ cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention (attention.cu)
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, cudaStream_t st);
+                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
+                                cudaStream_t st);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap);
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,

@@ -173,7 +173,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         } else {
             TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
                 return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
-                                           c->capacity, c->d_len, c->attn, st);
+                                           c->capacity, c->d_len, c->attn, c->d_err, st);
             }));
         }
         TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], M, d, c->q_width, EPI_RESIDUAL, c->x, d, c->x, d, st));
@@ -603,13 +603,13 @@ int qwen3_op_qknorm_rope_append(const void* qkv, int B, int T, int Hq, int Hkv, 
 }
 
 int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, int B, int T, int Hq, int Hkv, int dh,
-                               int cap, const int* len0, void* out, void* stream) {
+                               int cap, const int* len0, void* out, int* err, void* stream) {
     if (!q || !kc || !vc || !len0 || !out || B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (dh != 64 && dh != 128) || cap < 1)
         return QWEN3_E_ARG;
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
-                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out),
+                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out), err,
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

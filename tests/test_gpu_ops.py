@@ -217,7 +217,8 @@ def _attn_ref(q, kc, vc, len0, T):
 
 @pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0", [(1, 64, 8, 4, 64, 0), (2, 130, 8, 2, 64, 0),
                                                   (1, 200, 16, 8, 128, 0), (2, 77, 16, 8, 128, 70),
-                                                  (1, 1, 4, 4, 128, 300)])
+                                                  (1, 1, 4, 4, 128, 300), (1, 700, 8, 2, 128, 0),
+                                                  (1, 384, 4, 1, 64, 129), (3, 257, 8, 8, 128, 511)])
 def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
     rng = np.random.default_rng(T * 31 + len0)
     cap = len0 + T + 5
@@ -228,8 +229,10 @@ def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
     vc[:, :, len0 + T:] = 0x7FC0
     out = torch.empty(Bq * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
     len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
-    bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out)
+    err = _err()
+    bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err)
     torch.cuda.synchronize()
+    assert err.item() == 0
     ref = _attn_ref(q, kc, vc, len0, T)
     got = widen(bits(out))
     assert np.isfinite(got).all()
