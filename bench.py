@@ -365,6 +365,13 @@ def run_ours(args, wl):
             "kernels_note": "per-kernel times from a second run of the same steps with a CUDA event pair around "
                             "every launch (%.3f ms/step with events vs %.3f without)"
                             % (instrumented_ms / args.steps, elapsed_ms / args.steps)}
+    if wl["decode_steps"] > 0:
+        m.close()
+        line["decode"] = measure_decode(binding, synth, torch, cfg, wl, w, dev, args.decode_steps)
+        peaks_hbm = peaks["hbm_gbs"]
+        line["decode"]["attention_roofline"]["peak"] = peaks_hbm
+        line["decode"]["attention_roofline"]["frac"] = line["decode"]["attention_roofline"]["achieved"] / peaks_hbm
+        line["decode"]["step_hbm_frac"] = line["decode"]["step_hbm_gbs"] / peaks_hbm
     if world == 1 and not args.no_cpu_baseline:
         ob = OracleBench(cfg, wl["seed"])
         toks = sample_tokens(cfg, 1.5e10)
@@ -373,6 +380,57 @@ def run_ours(args, wl):
                                 "sample": ob.describe(toks), "seconds": dt}
     print(json.dumps(line), flush=True)
     m.close()
+
+
+def measure_decode(binding, synth, torch, cfg, wl, w, dev, steps_cap: int):
+    """Decode-step latency at the workload's pre-filled context, through qwen3_decode_step (graph replay).
+    The cache holds bf16 N(0,1) K/V for the first `ctx` positions of every sequence."""
+    Bd, ctx = wl["decode_batch"], wl["prefilled_ctx"]
+    steps = min(wl["decode_steps"], steps_cap)
+    L, V, Hkv, dh = cfg["n_layers"], cfg["vocab"], cfg["n_kv_heads"], cfg["head_dim"]
+    m = binding.Model(cfg, w, max_batch=Bd, capacity=ctx + wl["decode_steps"], max_tokens=max(Bd, 128))
+    for layer in range(L):
+        k, v = m.kv_view(layer)
+        shape = (Bd, Hkv, ctx, dh)
+        k[:, :, :ctx].copy_(synth.make_kv_normal(shape, wl["seed"], layer, "k", device=dev))
+        v[:, :, :ctx].copy_(synth.make_kv_normal(shape, wl["seed"], layer, "v", device=dev))
+    ids = synth.make_ids(V, Bd, 1, wl["seed"] + 100, device=dev).reshape(Bd)
+    logits = torch.empty(Bd, V, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):  # warm-up (the first call captures the graph)
+        m.set_length(ctx, Bd)
+        m.decode_step(ids, logits)
+    torch.cuda.synchronize()
+    m.set_length(ctx, Bd)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        m.decode_step(ids, logits)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if m.get_error() != 0:
+        raise RuntimeError("device error flag set during decode")
+    ms = a.elapsed_time(b) / steps
+    # per-kernel breakdown: the same steps, eager, with per-launch events
+    m.set_length(ctx, Bd)
+    m.set_timing(True)
+    m.kernel_times()
+    for _ in range(steps):
+        m.decode_step(ids, logits)
+    kt = m.kernel_times()
+    m.set_timing(False)
+    kv_bytes = 2.0 * Bd * Hkv * dh * 2 * (ctx + (steps + 1) / 2.0)  # K and V read per layer, mean context
+    att_ms = kt["attn_decode"][0] / kt["attn_decode"][1] * 2  # two launches (split + merge) per timed pair
+    w_bytes = float(sum(t.numel() * 2 for _, t in _flat(w)))
+    out = {"batch": Bd, "context": ctx, "steps": steps, "ms_per_step": ms,
+           "kernels": {k: {"ms_per_step": v[0] / steps, "launches_per_step": v[1] / steps}
+                       for k, v in kt.items() if v[1]},
+           "attention_roofline": {"bound": "hbm", "achieved": kv_bytes / (att_ms / 1e3) / 1e9,
+                                  "unit": "GB/s", "algorithmic_bytes_per_launch": kv_bytes,
+                                  "avg_launch_ms": att_ms},
+           "step_hbm_gbs": (w_bytes + L * kv_bytes) / (ms / 1e3) / 1e9}
+    m.close()
+    return out
 
 
 def _flat(w):
@@ -394,6 +452,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(configs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=128, help="cap on timed decode steps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
