@@ -433,6 +433,85 @@ def measure_decode(binding, synth, torch, cfg, wl, w, dev, steps_cap: int):
     return out
 
 
+def run_op(args, wl):
+    """Time one kernel alone through its single-operation C entry point at the workload's shapes
+    (small device footprint, for ncu captures and isolated roofline numbers)."""
+    import torch
+
+    from qwen3_decoder_transformer_gb300 import binding, build
+    build.build()
+    torch.cuda.set_device(0)
+    cfg = wl["model"]
+    B, T = wl["prefill"]
+    d, dh, F, V = cfg["hidden"], cfg["head_dim"], cfg["intermediate"], cfg["vocab"]
+    hq, hkv = cfg["n_q_heads"], cfg["n_kv_heads"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(wl["seed"])
+    rnd = lambda *shape: torch.randn(*shape, generator=g, device="cuda").to(torch.bfloat16)
+    len0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M = B * T
+    if args.op == "attn_prefill":
+        q, kc, vc = rnd(B, hq, T, dh), rnd(B, hkv, T, dh), rnd(B, hkv, T, dh)
+        out = torch.empty(M, hq * dh, dtype=torch.bfloat16, device="cuda")
+        fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out)
+        work, unit, bound = 4.0 * B * hq * dh * T * (T + 1) / 2, "TFLOP/s", "tensor"
+    elif args.op == "attn_decode":
+        Bd, ctx = wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
+        q, kc, vc = rnd(Bd, hq, dh), rnd(Bd, hkv, ctx + 8, dh), rnd(Bd, hkv, ctx + 8, dh)
+        len0.fill_(ctx - 1)
+        ws = torch.empty(binding.attention_decode_workspace(Bd, hq, dh, ctx + 8) // 4, dtype=torch.float32,
+                         device="cuda")
+        out = torch.empty(Bd, hq * dh, dtype=torch.bfloat16, device="cuda")
+        fn = lambda: binding.op_attention_decode(q, kc, vc, len0, ws, out)
+        work, unit, bound = 2.0 * Bd * hkv * ctx * dh * 2, "GB/s", "hbm"
+    elif args.op in ("gemm_gateup", "gemm_qkv", "gemm_o", "gemm_down"):
+        N, K, epi = {"gemm_gateup": (2 * F, d, binding.EPI_SWIGLU), "gemm_qkv": ((hq + 2 * hkv) * dh, d, binding.EPI_BF16),
+                     "gemm_o": (d, hq * dh, binding.EPI_RESIDUAL), "gemm_down": (d, F, binding.EPI_RESIDUAL)}[args.op]
+        Mx = args.rows or M
+        act, wt = rnd(Mx, K), rnd(N, K)
+        c = torch.empty(Mx, N // 2 if epi == binding.EPI_SWIGLU else N, dtype=torch.bfloat16, device="cuda")
+        fn = lambda: binding.op_gemm(act, wt, epi, c, R=c if epi == binding.EPI_RESIDUAL else None)
+        work, unit, bound = 2.0 * Mx * N * K, "TFLOP/s", "tensor"
+        if Mx <= 256:
+            work, unit, bound = 2.0 * N * K + 2.0 * Mx * K + 2.0 * Mx * c.shape[1], "GB/s", "hbm"
+    elif args.op == "qknorm_rope":
+        H = hq + 2 * hkv
+        qkv = rnd(M, H * dh)
+        table = torch.empty(T, dh, dtype=torch.bfloat16, device="cuda")
+        binding.op_rope_table(cfg["rope_theta"], dh, T, table)
+        gq, gk = rnd(dh), rnd(dh)
+        qo = torch.empty(B, hq, T, dh, dtype=torch.bfloat16, device="cuda")
+        kc, vc = torch.empty(B, hkv, T, dh, dtype=torch.bfloat16, device="cuda"), torch.empty(
+            B, hkv, T, dh, dtype=torch.bfloat16, device="cuda")
+        fn = lambda: binding.op_qknorm_rope_append(qkv, B, T, hq, hkv, dh, gq, gk, table, len0, 1e-6, qo, kc, vc)
+        work, unit, bound = 2.0 * M * H * dh * 2, "GB/s", "hbm"
+    elif args.op == "rmsnorm":
+        Mx = args.rows or M
+        x, gm = rnd(Mx, d), rnd(d)
+        y = torch.empty_like(x)
+        fn = lambda: binding.op_rmsnorm(x, gm, 1e-6, y)
+        work, unit, bound = 2.0 * Mx * d * 2, "GB/s", "hbm"
+    else:
+        raise SystemExit(f"unknown op {args.op}")
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        fn()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"]
+    ach = work / (ms / 1e3) / scale
+    print(json.dumps({"op": args.op, "workload": args.workload, "ms_per_launch": ms, "bound": bound,
+                      "achieved": ach, "unit": unit, "peak": peak, "frac": ach / peak,
+                      "algorithmic_per_launch": work, "peak_source": src + " (burst)"}), flush=True)
+
+
 def _flat(w):
     for k, v in w.items():
         if isinstance(v, list):
@@ -453,11 +532,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=128, help="cap on timed decode steps")
+    ap.add_argument("--op", default=None, help="time one kernel alone: attn_prefill, attn_decode, gemm_gateup, "
+                                                "gemm_qkv, gemm_o, gemm_down, qknorm_rope, rmsnorm")
+    ap.add_argument("--rows", type=int, default=0, help="row count for --op gemm_*/rmsnorm (default B*T)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = configs.WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.op:
+        run_op(args, wl)
+    elif args.impl == "reference":
         run_reference(args, wl)
     else:
         run_ours(args, wl)

@@ -21,44 +21,46 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // --------------------------------------------------------------------------- prefill (tcgen05)
-// One CTA = 128 query rows of one (sequence, query head); 6 warps:
-//   warp 0     TMA: the Q tile once, then K_j / V_j tiles (128 keys) into a 2-stage ring.
-//   warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32 TMEM
-//              buffers, O += P_j V_j into a DH-column TMEM accumulator. S_{j+1} is issued before
-//              O += P_j V_j so the tensor cores work on the next scores while softmax runs.
-//   warps 2-5  softmax: thread r owns query row r (TMEM lane r). Online softmax in base 2 with lazy
-//              rescaling: O and l are rescaled only when the running max grows by more than 8
-//              (so P <= 256); P_j is written as bf16 to shared memory in the UMMA K-major 128-byte
-//              swizzled layout (two buffers). At the end each thread normalises its O row.
-// Causal mask and the tail: key k is visible to query t iff k <= len0 + t; tiles wholly above the
-// diagonal are not loaded; V rows past the last valid key are zeroed in shared memory before use so
-// stale cache contents cannot reach O through 0 * NaN.
-constexpr int TC_BM = 128, TC_BN = 128, TC_THREADS = 192, TC_STAGES = 2;
+// One CTA = 128 query rows of NH query heads that share one kv head (NH = 2 when the group size
+// allows), so every K/V tile is loaded once for both heads. Warps:
+//   warp 0          TMA: the NH Q tiles once, then K_j / V_j tiles (128 keys) into a 2-stage ring.
+//   warp 1          TMEM owner and MMA issuer. Per head h: S_h = Q_h K_j^T into 128 fp32 TMEM
+//                   columns; softmax overwrites the first 64 of them with P_h as packed bf16; then
+//                   O_h += P_h V_j reads P_h straight from TMEM (A operand in tensor memory) and V_j as
+//                   an MN-major shared-memory operand. Order per tile: PV_0, S_0(next), PV_1, S_1(next),
+//                   so one head's scores are computed while the other head's softmax runs. The MMA
+//                   pipe executes in issue order, which makes S_h(next) overwriting P_h safe.
+//   warps 2..2+4NH  softmax, four warps per head; thread r owns query row r (TMEM lane r). Online
+//                   softmax in base 2 with lazy rescaling: O and l are rescaled only when the running
+//                   max grows by more than 8 (so P <= 256). At the end each thread normalises its row.
+// Causal mask: key k is visible to query t iff k <= len0 + t; tiles wholly above the diagonal are
+// not loaded, and only tiles crossing it are masked. V rows past the last valid key are zeroed in
+// shared memory before use so stale cache contents cannot reach O through 0 * NaN.
+constexpr int TC_BM = 128, TC_BN = 128, TC_STAGES = 2;
 
-template <int DH>
+template <int DH, int NH>
 struct TcLayout {
     static constexpr int NCH = DH / 64;             // 64-element (128-byte) column chunks
-    static constexpr int Q_BYTES = TC_BM * DH * 2;  // [NCH][128 rows][128 B]
+    static constexpr int Q_BYTES = TC_BM * DH * 2;  // per head: [NCH][128 rows][128 B]
     static constexpr int KV_BYTES = TC_BN * DH * 2;
-    static constexpr int P_BYTES = TC_BM * TC_BN * 2;  // [2 chunks][128 rows][128 B]
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + Q_BYTES;
+    static constexpr int K_OFF = NH * Q_BYTES;
     static constexpr int V_OFF = K_OFF + TC_STAGES * KV_BYTES;
-    static constexpr int P_OFF = V_OFF + TC_STAGES * KV_BYTES;
-    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+    static constexpr int BAR_OFF = V_OFF + TC_STAGES * KV_BYTES;
     static constexpr int SMEM = BAR_OFF + 256 + 1024;
+    static constexpr int THREADS = 64 + 128 * NH;
 };
 
-template <int DH>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+template <int DH, int NH>
+__global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv,
                            const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out, int* err) {
-    using Ly = TcLayout<DH>;
+    using Ly = TcLayout<DH, NH>;
     constexpr int NCH = Ly::NCH;
     constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
     constexpr uint32_t IDESC_O = idesc_bf16(TC_BM, DH, true);
-    constexpr uint32_t TM_O = 2 * TC_BN;  // O accumulator column base
+    constexpr uint32_t TM_O = 2 * TC_BN;  // O_h at TM_O + h * 128
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -67,16 +69,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t* k_full = bars + 1;    // [2]
     uint64_t* v_full = bars + 3;    // [2]
     uint64_t* kv_empty = bars + 5;  // [2]
-    uint64_t* s_full = bars + 7;    // [2]
-    uint64_t* p_full = bars + 9;    // [2]
-    uint64_t* o_done = bars + 11;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 13);
+    uint64_t* s_full = bars + 7;    // [NH]
+    uint64_t* p_full = bars + 9;    // [NH]
+    uint64_t* o_done = bars + 11;   // [NH]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int jkv = h / (Hq / Hkv);
+    const int h0 = blockIdx.y * NH, b = blockIdx.z;
+    const int jkv = h0 / (Hq / Hkv);
     const int len0 = *len0p;
     const int q0 = qt * TC_BM;
     const int q_end = min(T, q0 + TC_BM);
@@ -89,10 +91,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&k_full[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&kv_empty[i], 1);
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
         }
-        mbar_init(o_done, 1);
+        for (int hh = 0; hh < NH; ++hh) {
+            mbar_init(&s_full[hh], 1);
+            mbar_init(&p_full[hh], 128);
+            mbar_init(&o_done[hh], 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -111,9 +115,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_expect_tx(q_full, Ly::Q_BYTES);
-            for (int c = 0; c < NCH; ++c)
-                tma_load_3d(smem + Ly::Q_OFF + c * TC_BM * 128, &tmQ, q_full, c * 64, q0, b * Hq + h);
+            mbar_expect_tx(q_full, NH * Ly::Q_BYTES);
+            for (int hh = 0; hh < NH; ++hh)
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(smem + Ly::Q_OFF + hh * Ly::Q_BYTES + c * TC_BM * 128, &tmQ, q_full, c * 64, q0,
+                                b * Hq + h0 + hh);
             for (int j = 0; j < n_tiles; ++j) {
                 const int s = j & 1;
                 if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -129,26 +135,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp == 1) {
         // all lanes walk the schedule (so the warp can zero V tails together); lane 0 issues
-        auto issue_s = [&](int j) -> bool {
+        auto issue_s = [&](int hh, int j) -> bool {
             const int s = j & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag))) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t sq = smem_u32(smem + Ly::Q_OFF), sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
+                const uint32_t sq = smem_u32(smem + Ly::Q_OFF + hh * Ly::Q_BYTES);
+                const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
-                    umma_bf16_ss(tmem + s * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), IDESC_S,
+                    umma_bf16_ss(tmem + hh * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), IDESC_S,
                                  kk > 0);
                 }
-                umma_commit(&s_full[s]);
+                umma_commit(&s_full[hh]);
             }
             __syncwarp();
             return true;
         };
         ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
-        if (ok) ok = issue_s(0);
-        if (ok && n_tiles > 1) ok = issue_s(1);
+        for (int hh = 0; ok && hh < NH; ++hh) ok = issue_s(hh, 0);
         for (int j = 0; ok && j < n_tiles; ++j) {
             const int s = j & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag))) { ok = false; break; }
@@ -163,73 +169,78 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 fence_proxy_async_smem();
             }
             __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s], (j >> 1) & 1, abort_flag))) { ok = false; break; }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t sp = smem_u32(smem + Ly::P_OFF + s * Ly::P_BYTES), svv = smem_u32(sv);
+            for (int hh = 0; ok && hh < NH; ++hh) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[hh], j & 1, abort_flag))) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t svv = smem_u32(sv);
 #pragma unroll
-                for (int kk = 0; kk < TC_BN / 16; ++kk) {
-                    const uint64_t ad = sdesc_kmajor_sw128(sp + (kk >> 2) * TC_BM * 128 + (kk & 3) * 32);
-                    const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
-                    umma_bf16_ss(tmem + TM_O, ad, bd, IDESC_O, (j | kk) != 0);
+                    for (int kk = 0; kk < TC_BN / 16; ++kk) {
+                        const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
+                        umma_bf16_ts(tmem + TM_O + hh * 128, tmem + hh * TC_BN + kk * 8, bd, IDESC_O, (j | kk) != 0);
+                    }
+                    umma_commit(&o_done[hh]);
+                    if (hh == NH - 1) umma_commit(&kv_empty[s]);
                 }
-                umma_commit(o_done);
-                umma_commit(&kv_empty[s]);
+                __syncwarp();
+                if (j + 1 < n_tiles) ok = issue_s(hh, j + 1);
             }
-            __syncwarp();
-            if (j + 2 < n_tiles) ok = issue_s(j + 2);
         }
     } else {
-        // softmax warps: thread <-> query row
+        // softmax warps: head hh, thread <-> query row
+        const int hh = (warp - 2) >> 2;
         const int quarter = warp & 3, row = quarter * 32 + lane;
         const int t = q0 + row, pos = len0 + t;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const float sl2 = 1.4426950408889634f / sqrtf((float)DH);
-        float m_used = -INFINITY, l = 0.f;
-        int pv_seen = 0;  // PV completions confirmed so far
+        const uint32_t tm_s = tmem + lane_off + hh * TC_BN, tm_o = tmem + lane_off + TM_O + hh * 128;
+        const float sl2 = kLog2e / sqrtf((float)DH);
+        float m_used = -INFINITY, l = 0.f;  // m_used in scaled (log2) units
+        int pv_seen = 0;                    // PV completions confirmed so far
         auto confirm_pv = [&](int upto) -> bool {
             while (pv_seen < upto) {
-                if (!mbar_wait(o_done, pv_seen & 1, abort_flag)) return false;
+                if (!mbar_wait(&o_done[hh], pv_seen & 1, abort_flag)) return false;
                 ++pv_seen;
             }
             return true;
         };
         for (int j = 0; j < n_tiles; ++j) {
-            const int s = j & 1;
-            const bool w = mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[hh], j & 1, abort_flag))) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[TC_BN];
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c)
-                tmem_ld_32x32b_x32(tmem + lane_off + s * TC_BN + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                tmem_ld_32x32b_x32(tm_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_ld_wait();
             const int k0 = j * TC_BN;
-            const bool need_mask = k0 + TC_BN - 1 > len0 + q0;
             float mx = -INFINITY;
+            if (k0 + TC_BN - 1 > len0 + q0) {  // tile crosses the diagonal: mask keys past pos
+                const int lim = pos - k0;
 #pragma unroll
-            for (int i = 0; i < TC_BN; ++i) {
-                float v = __uint_as_float(sr[i]) * sl2;
-                if (need_mask && k0 + i > pos) v = -INFINITY;
-                sr[i] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < TC_BN; ++i) {
+                    const float v = i <= lim ? __uint_as_float(sr[i]) : -INFINITY;
+                    sr[i] = __float_as_uint(v);
+                    mx = fmaxf(mx, v);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < TC_BN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
             }
+            mx *= sl2;
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
-            const float alpha = grow ? exp2f(m_used - mx) : 1.0f;
+            const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                // rescale O once the previous P V product has landed
-                const bool w = confirm_pv(j);
+                const bool w = confirm_pv(j);  // O must hold P V of the previous tile before it is scaled
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < DH / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                    tmem_ld_32x32b_x32(tm_o + c * 32, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                    tmem_st_32x32b_x32(tm_o + c * 32, o);
                 }
                 tmem_st_wait();
             }
@@ -237,23 +248,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 l *= alpha;
                 m_used = mx;
             }
-            // P = exp2(s - m) as bf16, written to the K-major swizzled tile (two 64-key chunks)
-            uint8_t* prow = smem + Ly::P_OFF + s * Ly::P_BYTES + row * 128;
+            // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region
+            const float nm = -m_used;
             float rs = 0.f;
 #pragma unroll
-            for (int u = 0; u < TC_BN / 8; ++u) {
-                uint32_t wv[4];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = exp2f(__uint_as_float(sr[u * 8 + 2 * e]) - m_used);
-                    const float p1 = exp2f(__uint_as_float(sr[u * 8 + 2 * e + 1]) - m_used);
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
                     rs += p0 + p1;
-                    wv[e] = pack_bf16(p0, p1);
+                    pk[e] = pack_bf16(p0, p1);
                 }
-                const int c = u >> 3, uu = u & 7;
-                *reinterpret_cast<uint4*>(prow + c * TC_BM * 128 + ((uu ^ (row & 7)) * 16)) =
-                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                tmem_st_32x32b_x32(tm_s + half * 32, pk);
             }
+            tmem_st_wait();
             l += rs;
             // Observe the previous P V completion before releasing this P: o_done is then never more
             // than one phase ahead of this thread, so its parity waits stay unambiguous.
@@ -261,9 +271,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const bool w = confirm_pv(j);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&p_full[s]);
+            mbar_arrive(&p_full[hh]);
         }
         // epilogue: O / l
         if (ok) ok = confirm_pv(n_tiles);
@@ -271,11 +280,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
-            __nv_bfloat16* orow = out + (((size_t)b * T + t) * Hq + h) * DH;
+            __nv_bfloat16* orow = out + (((size_t)b * T + t) * Hq + h0 + hh) * DH;
 #pragma unroll 1
             for (int c = 0; c < DH / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld_32x32b_x32(tmem + lane_off + TM_O + c * 32, o);
+                tmem_ld_32x32b_x32(tm_o + c * 32, o);
                 tmem_ld_wait();
                 if (t < T) {
                     uint32_t wv[16];
@@ -525,6 +534,15 @@ cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, co
     return cudaErrorInvalidValue;
 }
 
+template <int DH, int NH>
+cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int B, int T, int Hq,
+                              int Hkv, const int* len0, __nv_bfloat16* out, int* err, cudaStream_t st) {
+    using Ly = TcLayout<DH, NH>;
+    dim3 grid((T + TC_BM - 1) / TC_BM, Hq / NH, B);
+    attn_prefill_tc_kernel<DH, NH><<<grid, Ly::THREADS, Ly::SMEM, st>>>(tq, tk, tv, T, Hq, Hkv, len0, out, err);
+    return cudaGetLastError();
+}
+
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                               int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, int* err,
@@ -533,9 +551,8 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
         return cudaErrorInvalidValue;
-    dim3 grid((T + TC_BM - 1) / TC_BM, Hq, B);
-    attn_prefill_tc_kernel<DH><<<grid, TC_THREADS, TcLayout<DH>::SMEM, st>>>(tq, tk, tv, T, Hq, Hkv, len0, out, err);
-    return cudaGetLastError();
+    if ((Hq / Hkv) % 2 == 0) return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
+    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
 }
 
 }  // namespace
@@ -566,11 +583,14 @@ cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, 
 int attn_decode_kernel_count() { return 2; }
 
 cudaError_t attention_prepare() {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          TcLayout<128>::SMEM);
-    cudaError_t e2 = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          TcLayout<64>::SMEM);
-    return e1 != cudaSuccess ? e1 : e2;
+    const void* fns[] = {(const void*)attn_prefill_tc_kernel<128, 1>, (const void*)attn_prefill_tc_kernel<128, 2>,
+                         (const void*)attn_prefill_tc_kernel<64, 1>, (const void*)attn_prefill_tc_kernel<64, 2>};
+    const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM};
+    for (int i = 0; i < 4; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace q3
