@@ -55,7 +55,7 @@ def kernel_work(cfg: dict, B: int, T: int) -> dict:
     M = B * T
     qkv_n = (hq + 2 * hkv) * dh
     return {
-        "gemm_qkv": ("tensor", 2.0 * M * qkv_n * d),
+        "gemm_qkv_norm_rope_append": ("tensor", 2.0 * M * qkv_n * d),
         "gemm_o_residual": ("tensor", 2.0 * M * d * hq * dh),
         "gemm_gateup_swiglu": ("tensor", 2.0 * M * 2 * F * d),
         "gemm_down_residual": ("tensor", 2.0 * M * d * F),
@@ -70,8 +70,8 @@ def kernel_work(cfg: dict, B: int, T: int) -> dict:
 def step_flops(cfg: dict, B: int, T: int) -> float:
     w = kernel_work(cfg, B, T)
     L = cfg["n_layers"]
-    per_layer = sum(w[k][1] for k in ("gemm_qkv", "gemm_o_residual", "gemm_gateup_swiglu", "gemm_down_residual",
-                                       "attn_prefill"))
+    per_layer = sum(w[k][1] for k in ("gemm_qkv_norm_rope_append", "gemm_o_residual", "gemm_gateup_swiglu",
+                                       "gemm_down_residual", "attn_prefill"))
     return L * per_layer + w["gemm_lmhead"][1]
 
 

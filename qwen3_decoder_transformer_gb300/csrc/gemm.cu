@@ -9,6 +9,9 @@
 //                 blocks of gate and up rows, so one 256-wide tile holds matching g and u columns)
 //   EPI_RESIDUAL  C = bf16(R + bf16(acc)), R may alias C            (o_proj and down_proj)
 //   EPI_F32       C = acc in fp32                                   (LM head logits)
+//   EPI_QKV_ROPE  fused QKV projection + per-head q_norm/k_norm + RoPE + KV-cache append: each
+//                 accumulator row of a tile holds whole head vectors of one token, so the RMS over
+//                 head_dim, the rotate-half pairs (i, i + dh/2) and the stores stay in one thread
 //
 // Design (sm_103a): a persistent kernel, one CTA per SM, 6 warps.
 //   warp 0      TMA producer: 128x64 A and 256x64 B boxes (128-byte swizzle) into a 4-stage ring.
@@ -41,12 +44,121 @@ constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 struct Tile {
     int m0, n0;
 };
-__device__ __forceinline__ Tile tile_of(int t, int m_tiles) { return {(t % m_tiles) * BM, (t / m_tiles) * BN}; }
+// Tiles are walked in groups of up to 32 M-tiles: within a group M runs fastest, so the CTAs resident
+// at one time share a few weight (B) tiles and a bounded slice of A through L2.
+constexpr int GROUP_M = 32;
+__device__ __forceinline__ Tile tile_of(int t, int m_tiles, int n_tiles) {
+    const int per_group = GROUP_M * n_tiles;
+    const int g = t / per_group, first = g * GROUP_M;
+    const int gm = min(GROUP_M, m_tiles - first);
+    const int local = t - g * per_group;
+    return {(first + local % gm) * BM, (local / gm) * BN};
+}
+
+// Fused epilogue of the QKV projection for one accumulator row (token) of a 256-wide tile: the
+// projection output is rounded to bf16 as the unfused path stores it, then V heads go to the cache
+// unchanged and Q/K heads get RMSNorm over head_dim (fp32 reduce, bf16 cast, then gamma) and RoPE
+// (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the pair (i, i + dh/2)).
+template <int DH>
+__device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+    const QkvRopeArgs& q = a.qkv;
+    const bool row_ok = row < a.M;
+    const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
+    const int pos = *q.len0 + t;
+    constexpr int HALF = DH / 2;
+#pragma unroll 1
+    for (int lh = 0; lh < BN / DH; ++lh) {
+        const int hg = n0 / DH + lh;
+        const uint32_t th = tacc + lh * DH;
+        if (hg >= q.Hq + q.Hkv) {  // V head: copy to the cache slot
+            __nv_bfloat16* dst = q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + pos) * DH;
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(th + c * 32, r);
+                tmem_ld_wait();
+                if (!row_ok) continue;
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    reinterpret_cast<uint4*>(dst + c * 32)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            }
+            continue;
+        }
+        const bool is_q = hg < q.Hq;
+        // pass 1: sum of squares of the bf16-rounded projection
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(th + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float x = rbf(__uint_as_float(r[j]));
+                ss = fmaf(x, x, ss);
+            }
+        }
+        const float rn = __frsqrt_rn(ss / (float)DH + q.eps);
+        const __nv_bfloat16* gam = is_q ? q.q_gamma : q.k_gamma;
+        const __nv_bfloat16* cs = q.table + (size_t)pos * DH;
+        __nv_bfloat16* dst = is_q ? q.q_out + (((size_t)b * q.Hq + hg) * q.T + t) * DH
+                                  : q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + pos) * DH;
+        // pass 2: 32 rotation pairs at a time, (i, i + HALF)
+#pragma unroll 1
+        for (int c = 0; c < HALF / 32; ++c) {
+            uint32_t lo[32], hi[32];
+            tmem_ld_32x32b_x32(th + c * 32, lo);
+            tmem_ld_32x32b_x32(th + HALF + c * 32, hi);
+            tmem_ld_wait();
+            if (!row_ok) continue;
+            uint32_t wlo[16], whi[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam + c * 32) + v);
+                const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF + c * 32) + v);
+                const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs + c * 32) + v);
+                const uint4 sn = __ldg(reinterpret_cast<const uint4*>(cs + HALF + c * 32) + v);
+                const uint32_t G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
+                const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float o_lo[2], o_hi[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int j = 8 * v + 2 * e + k;
+                        const float ga = k ? bf16_hi(G0[e]) : bf16_lo(G0[e]);
+                        const float gb = k ? bf16_hi(G1[e]) : bf16_lo(G1[e]);
+                        const float co = k ? bf16_hi(C[e]) : bf16_lo(C[e]);
+                        const float si = k ? bf16_hi(S[e]) : bf16_lo(S[e]);
+                        const float av = rbf(ga * rbf(rbf(__uint_as_float(lo[j])) * rn));
+                        const float bv = rbf(gb * rbf(rbf(__uint_as_float(hi[j])) * rn));
+                        o_lo[k] = rbf(av * co) + rbf(-(bv * si));
+                        o_hi[k] = rbf(bv * co) + rbf(av * si);
+                    }
+                    wlo[4 * v + e] = pack_bf16(o_lo[0], o_lo[1]);
+                    whi[4 * v + e] = pack_bf16(o_hi[0], o_hi[1]);
+                }
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                reinterpret_cast<uint4*>(dst + c * 32)[v] = make_uint4(wlo[4 * v], wlo[4 * v + 1], wlo[4 * v + 2], wlo[4 * v + 3]);
+                reinterpret_cast<uint4*>(dst + HALF + c * 32)[v] =
+                    make_uint4(whi[4 * v], whi[4 * v + 1], whi[4 * v + 2], whi[4 * v + 3]);
+            }
+        }
+    }
+}
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunks(const GemmArgs& a, uint32_t tacc, int row, int n0) {
     const bool row_ok = row < a.M;
-    if constexpr (EPI == EPI_SWIGLU) {
+    if constexpr (EPI == EPI_QKV_ROPE) {
+        if (a.qkv.dh == 128) epilogue_qkv_rope<128>(a, tacc, row, n0);
+        else epilogue_qkv_rope<64>(a, tacc, row, n0);
+    } else if constexpr (EPI == EPI_SWIGLU) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.C) + (size_t)row * a.ldc + n0 / 2;
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
@@ -178,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- TMA producer
         int it = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = tile_of(t, m_tiles);
+            const Tile tl = tile_of(t, m_tiles, n_tiles);
             for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -224,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!mbar_wait(&acc_full[acc], aph, abort_flag)) { ok = false; }
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             tc_fence_after();
-            const Tile tl = tile_of(t, m_tiles);
+            const Tile tl = tile_of(t, m_tiles, n_tiles);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
             epilogue_chunks<EPI>(args, tacc, tl.m0 + quarter * 32 + lane, tl.n0);
             tc_fence_before();
@@ -284,7 +396,8 @@ int device_sm_count() {
 cudaError_t gemm_prepare() {
     cudaError_t e = cudaSuccess;
     const void* fns[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16>, (const void*)gemm_tcgen05_kernel<EPI_SWIGLU>,
-                         (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL>, (const void*)gemm_tcgen05_kernel<EPI_F32>};
+                         (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL>, (const void*)gemm_tcgen05_kernel<EPI_F32>,
+                         (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE>};
     for (const void* f : fns) {
         cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (r != cudaSuccess) e = r;
@@ -326,6 +439,7 @@ cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
         case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(ta, tb, a, st);
         case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(ta, tb, a, st);
         case EPI_F32: return launch_epi<EPI_F32>(ta, tb, a, st);
+        case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE>(ta, tb, a, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -11,7 +11,7 @@ namespace q3 {
 // Device error-flag bits (one int per context, read by qwen3_get_error).
 enum : int { ERR_TOKEN = 1, ERR_TIMEOUT = 2 };
 
-enum Epilogue : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_RESIDUAL = 2, EPI_F32 = 3 };
+enum Epilogue : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_RESIDUAL = 2, EPI_F32 = 3, EPI_QKV_ROPE = 4 };
 
 // ---------------------------------------------------------------- host utilities (gemm.cu)
 int device_sm_count();
@@ -21,6 +21,15 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
                          uint32_t box_inner, uint32_t box_outer);
 
 // ---------------------------------------------------------------- GEMM (gemm.cu)
+// Extra operands of EPI_QKV_ROPE: the accumulator row of a QKV tile is one token's q/k/v head
+// vectors; the epilogue applies q_norm/k_norm and RoPE and writes Q [B, Hq, T, dh] and the cache.
+struct QkvRopeArgs {
+    const __nv_bfloat16 *q_gamma, *k_gamma, *table;  // table [cap][dh]: cos then sin per position
+    const int* len0;                                  // device cache length (first position)
+    __nv_bfloat16 *q_out, *k_cache, *v_cache;        // caches [B][Hkv][cap][dh]
+    int T, Hq, Hkv, dh, cap;
+    float eps;
+};
 struct GemmArgs {
     int M, N, K;
     int epi;
@@ -29,6 +38,7 @@ struct GemmArgs {
     const __nv_bfloat16* R;
     long long ldr;
     int* err;
+    QkvRopeArgs qkv;
 };
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
 // A: [rows >= M, K] activations; B: [N, K] weights. Both maps are built with encode_gemm_maps.

@@ -19,7 +19,6 @@ enum KernelClass : int {
     K_EMBED = 0,
     K_RMSNORM,
     K_GEMM_QKV,
-    K_QKNORM_ROPE,
     K_ATTN_PREFILL,
     K_GEMM_O,
     K_GEMM_GATEUP,
@@ -29,9 +28,16 @@ enum KernelClass : int {
     K_LENGTH,
     K_NUM_CLASSES
 };
-const char* kClassNames[K_NUM_CLASSES] = {"embed",  "rmsnorm",     "gemm_qkv",    "qknorm_rope_append",
-                                          "attn_prefill", "gemm_o_residual", "gemm_gateup_swiglu",
-                                          "gemm_down_residual", "gemm_lmhead", "attn_decode", "length_update"};
+const char* kClassNames[K_NUM_CLASSES] = {"embed",
+                                          "rmsnorm",
+                                          "gemm_qkv_norm_rope_append",
+                                          "attn_prefill",
+                                          "gemm_o_residual",
+                                          "gemm_gateup_swiglu",
+                                          "gemm_down_residual",
+                                          "gemm_lmhead",
+                                          "attn_decode",
+                                          "length_update"};
 
 struct TimedLaunch {
     int cls;
@@ -74,7 +80,7 @@ struct qwen3_ctx {
     std::vector<const bf16*> in_norm, q_norm, k_norm, post_norm, o_proj, down_proj;
     // owned device memory
     bf16 *wqkv = nullptr, *wgu = nullptr, *kcache = nullptr, *vcache = nullptr, *rope = nullptr;
-    bf16 *x = nullptr, *xn = nullptr, *qkv = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
+    bf16 *x = nullptr, *xn = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
     float* dec_work = nullptr;
     int* d_len = nullptr;
     int* d_err = nullptr;
@@ -140,7 +146,7 @@ int timed(qwen3_ctx* c, int cls, int launches, cudaStream_t st, F&& fn) {
 
 int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int epi, void* C,
          long long ldc, const bf16* R, long long ldr, cudaStream_t st) {
-    GemmArgs a{M, N, K, epi, C, ldc, R, ldr, c->d_err};
+    GemmArgs a{M, N, K, epi, C, ldc, R, ldr, c->d_err, {}};
     return timed(c, cls, 1, st, [&] { return gemm_launch(ta, tb, a, st); });
 }
 
@@ -159,12 +165,13 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
                 return QWEN3_E_CUDA;
         TRY(timed(c, K_RMSNORM, 1, st,
                   [&] { return rmsnorm_launch(c->x, c->in_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
-        TRY(gemm(c, K_GEMM_QKV, c->tA_xn, c->tB_qkv[l], M, c->qkv_n, d, EPI_BF16, c->qkv, c->qkv_n, nullptr, 0, st));
-        TRY(timed(c, K_QKNORM_ROPE, 1, st, [&] {
-            return qknorm_rope_append_launch(c->qkv, B, T, g.n_q_heads, g.n_kv_heads, dh, c->q_norm[l], c->k_norm[l],
-                                             c->rope, c->d_len, g.rms_eps, c->q, layer_k(c, l), layer_v(c, l),
-                                             c->capacity, st);
-        }));
+        {
+            // fused: Q/K/V projection, q_norm/k_norm, RoPE, Q to attention layout, K/V into the cache
+            GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, nullptr, 0, nullptr, 0, c->d_err,
+                       QkvRopeArgs{c->q_norm[l], c->k_norm[l], c->rope, c->d_len, c->q, layer_k(c, l), layer_v(c, l), T,
+                                   g.n_q_heads, g.n_kv_heads, dh, c->capacity, g.rms_eps}};
+            TRY(timed(c, K_GEMM_QKV, 1, st, [&] { return gemm_launch(c->tA_xn, c->tB_qkv[l], a, st); }));
+        }
         if (decode) {
             TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
                 return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
@@ -220,8 +227,8 @@ void release(qwen3_ctx* c) {
     }
     for (auto e : c->free_events) cudaEventDestroy(e);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
-    void* bufs[] = {c->wqkv, c->wgu, c->kcache, c->vcache, c->rope, c->x,     c->xn,        c->qkv,         c->q,
-                    c->attn, c->h,   c->hn,     c->dec_work, c->d_len, c->d_err, c->d_ids_buf, c->d_logits_buf};
+    void* bufs[] = {c->wqkv, c->wgu, c->kcache,  c->vcache, c->rope,  c->x,         c->xn,          c->q,
+                    c->attn, c->h,   c->hn,      c->dec_work, c->d_len, c->d_err, c->d_ids_buf, c->d_logits_buf};
     for (void* p : bufs)
         if (p) cudaFree(p);
     delete c;
@@ -316,7 +323,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
               dmalloc(&c->vcache, (size_t)L * c->layer_elems) == cudaSuccess &&
               dmalloc(&c->rope, (size_t)capacity * dh) == cudaSuccess &&
               dmalloc(&c->x, rows * d) == cudaSuccess && dmalloc(&c->xn, arows * d) == cudaSuccess &&
-              dmalloc(&c->qkv, rows * c->qkv_n) == cudaSuccess && dmalloc(&c->q, rows * c->q_width) == cudaSuccess &&
+              dmalloc(&c->q, rows * c->q_width) == cudaSuccess &&
               dmalloc(&c->attn, arows * c->q_width) == cudaSuccess && dmalloc(&c->h, arows * F) == cudaSuccess &&
               dmalloc(&c->hn, arows * d) == cudaSuccess &&
               dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, capacity) / 4) ==
@@ -526,7 +533,7 @@ int qwen3_launch_count(const qwen3_ctx* c, int B, int T, int flags, int decode) 
     (void)T;
     (void)flags;
     if (!c) return -1;
-    const int per_layer = 7 + (decode ? attn_decode_kernel_count() : 1);
+    const int per_layer = 6 + (decode ? attn_decode_kernel_count() : 1);
     return 1 + c->cfg.n_layers * per_layer + 3;
 }
 
@@ -569,7 +576,7 @@ int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, vo
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     CUtensorMap ta, tb;
     if (!encode_gemm_maps(&ta, &tb, A, (uint64_t)M, B, (uint64_t)N, (uint64_t)K)) return QWEN3_E_CUDA;
-    GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err};
+    GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
     return gemm_launch(ta, tb, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
