@@ -79,11 +79,8 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     const int qt = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
     const int h0 = blockIdx.y * NH, b = blockIdx.z;
     const int jkv = h0 / (Hq / Hkv);
-    const int len0 = *len0p;
     const int q0 = qt * TC_BM;
     const int q_end = min(T, q0 + TC_BM);
-    const int n_valid = len0 + q_end;
-    const int n_tiles = (n_valid + TC_BN - 1) / TC_BN;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -112,6 +109,11 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    pdl_wait();  // Q and the cache come from the previous kernel
+    pdl_trigger();
+    const int len0 = *len0p;
+    const int n_valid = len0 + q_end;
+    const int n_tiles = (n_valid + TC_BN - 1) / TC_BN;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -349,6 +351,8 @@ __global__ void __launch_bounds__(DEC_THREADS)
     __shared__ float red[DEC_THREADS / 32][G][DH];
     __shared__ float stat[G][2];
 
+    pdl_wait();
+    pdl_trigger();
     const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int nsplit = gridDim.x;
     const int n = *len0p + 1;
@@ -496,6 +500,8 @@ template <int DH>
 __global__ void attn_decode_combine_kernel(const float* __restrict__ work, int Hq, int nsplit,
                                            __nv_bfloat16* __restrict__ out) {
     constexpr int REC = DH + 2;
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const float* wb = work + ((size_t)b * Hq + h) * nsplit * REC;
     float M = -INFINITY;
@@ -515,11 +521,10 @@ template <int DH, int G>
 cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                             int Hkv, int cap, const int* len0, float* work, __nv_bfloat16* out, cudaStream_t st) {
     const int nsplit = (cap + DEC_CHUNK - 1) / DEC_CHUNK;
-    attn_decode_split_kernel<DH, G><<<dim3(nsplit, Hkv, B), DEC_THREADS, 0, st>>>(q, kc, vc, Hq, Hkv, cap, len0, work);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(attn_decode_split_kernel<DH, G>, dim3(nsplit, Hkv, B), dim3(DEC_THREADS), 0, st, q, kc, vc,
+                               Hq, Hkv, cap, len0, work);
     if (e != cudaSuccess) return e;
-    attn_decode_combine_kernel<DH><<<dim3(Hq, B), DH, 0, st>>>(work, Hq, nsplit, out);
-    return cudaGetLastError();
+    return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, out);
 }
 
 template <int DH>
@@ -539,8 +544,8 @@ cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               int Hkv, const int* len0, __nv_bfloat16* out, int* err, cudaStream_t st) {
     using Ly = TcLayout<DH, NH>;
     dim3 grid((T + TC_BM - 1) / TC_BM, Hq / NH, B);
-    attn_prefill_tc_kernel<DH, NH><<<grid, Ly::THREADS, Ly::SMEM, st>>>(tq, tk, tv, T, Hq, Hkv, len0, out, err);
-    return cudaGetLastError();
+    return launch_pdl(attn_prefill_tc_kernel<DH, NH>, grid, dim3(Ly::THREADS), Ly::SMEM, st, tq, tk, tv, T, Hq, Hkv, len0,
+                      out, err);
 }
 
 template <int DH>
@@ -551,6 +556,8 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
         return cudaErrorInvalidValue;
+    // Two heads per CTA share each K/V tile (measured faster than one head per CTA even when the
+    // grid is smaller than the SM count).
     if ((Hq / Hkv) % 2 == 0) return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
     return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
 }

@@ -32,14 +32,20 @@
 namespace q3 {
 namespace {
 
-constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK, STAGES = 4;
+constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+// Per tile width BN (256, or 128 when 256-wide tiles cannot fill the SMs): stage size, ring depth,
+// TMEM columns (two accumulators) and the instruction descriptor.
+template <int BN>
+struct Cfg {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+};
 
 struct Tile {
     int m0, n0;
@@ -47,6 +53,7 @@ struct Tile {
 // Tiles are walked in groups of up to 32 M-tiles: within a group M runs fastest, so the CTAs resident
 // at one time share a few weight (B) tiles and a bounded slice of A through L2.
 constexpr int GROUP_M = 32;
+template <int BN>
 __device__ __forceinline__ Tile tile_of(int t, int m_tiles, int n_tiles) {
     const int per_group = GROUP_M * n_tiles;
     const int g = t / per_group, first = g * GROUP_M;
@@ -59,7 +66,7 @@ __device__ __forceinline__ Tile tile_of(int t, int m_tiles, int n_tiles) {
 // projection output is rounded to bf16 as the unfused path stores it, then V heads go to the cache
 // unchanged and Q/K heads get RMSNorm over head_dim (fp32 reduce, bf16 cast, then gamma) and RoPE
 // (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the pair (i, i + dh/2)).
-template <int DH>
+template <int DH, int BN>
 __device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t tacc, int row, int n0) {
     const QkvRopeArgs& q = a.qkv;
     const bool row_ok = row < a.M;
@@ -152,12 +159,12 @@ __device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t ta
     }
 }
 
-template <int EPI>
+template <int EPI, int BN>
 __device__ __forceinline__ void epilogue_chunks(const GemmArgs& a, uint32_t tacc, int row, int n0) {
     const bool row_ok = row < a.M;
     if constexpr (EPI == EPI_QKV_ROPE) {
-        if (a.qkv.dh == 128) epilogue_qkv_rope<128>(a, tacc, row, n0);
-        else epilogue_qkv_rope<64>(a, tacc, row, n0);
+        if (a.qkv.dh == 128) epilogue_qkv_rope<128, BN>(a, tacc, row, n0);
+        else epilogue_qkv_rope<64, BN>(a, tacc, row, n0);
     } else if constexpr (EPI == EPI_SWIGLU) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.C) + (size_t)row * a.ldc + n0 / 2;
 #pragma unroll 1
@@ -243,10 +250,13 @@ __device__ __forceinline__ void epilogue_chunks(const GemmArgs& a, uint32_t tacc
     }
 }
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs args) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, TMEM_COLS = C::TMEM_COLS;
+    constexpr uint32_t IDESC = C::IDESC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -285,12 +295,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     bool ok = true;
+    pdl_wait();  // inputs of this GEMM come from the previous kernel
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
         int it = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = tile_of(t, m_tiles, n_tiles);
+            const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
             for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -298,7 +310,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t* sa = smem + s * STAGE_BYTES;
                 mbar_expect_tx(&full_bar[s], STAGE_BYTES);
                 tma_load_2d(sa, &tmA, &full_bar[s], kb * BK, tl.m0);
-                tma_load_2d(sa + A_BYTES, &tmB, &full_bar[s], kb * BK, tl.n0);
+#pragma unroll
+                for (int nb = 0; nb < BN / kGemmBoxN; ++nb)
+                    tma_load_2d(sa + A_BYTES + nb * kGemmBoxN * BK * 2, &tmB, &full_bar[s], kb * BK, tl.n0 + nb * kGemmBoxN);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -336,9 +350,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!mbar_wait(&acc_full[acc], aph, abort_flag)) { ok = false; }
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             tc_fence_after();
-            const Tile tl = tile_of(t, m_tiles, n_tiles);
+            const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-            epilogue_chunks<EPI>(args, tacc, tl.m0 + quarter * 32 + lane, tl.n0);
+            epilogue_chunks<EPI, BN>(args, tacc, tl.m0 + quarter * 32 + lane, tl.n0);
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
         }
@@ -370,12 +384,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int EPI>
+template <int EPI, int BN>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int grid = std::min(tiles, device_sm_count());
-    gemm_tcgen05_kernel<EPI><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(THREADS), Cfg<BN>::SMEM_BYTES, st, ta, tb, a);
 }
 
 }  // namespace
@@ -395,11 +408,17 @@ int device_sm_count() {
 
 cudaError_t gemm_prepare() {
     cudaError_t e = cudaSuccess;
-    const void* fns[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16>, (const void*)gemm_tcgen05_kernel<EPI_SWIGLU>,
-                         (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL>, (const void*)gemm_tcgen05_kernel<EPI_F32>,
-                         (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE>};
-    for (const void* f : fns) {
-        cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const void* f256[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16, 256>, (const void*)gemm_tcgen05_kernel<EPI_SWIGLU, 256>,
+                          (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL, 256>, (const void*)gemm_tcgen05_kernel<EPI_F32, 256>,
+                          (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 256>};
+    const void* f128[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16, 128>, (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL, 128>,
+                          (const void*)gemm_tcgen05_kernel<EPI_F32, 128>, (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 128>};
+    for (const void* f : f256) {
+        cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<256>::SMEM_BYTES);
+        if (r != cudaSuccess) e = r;
+    }
+    for (const void* f : f128) {
+        cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::SMEM_BYTES);
         if (r != cudaSuccess) e = r;
     }
     return e;
@@ -429,17 +448,27 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
 
 bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t a_rows, const void* B, uint64_t N,
                       uint64_t K) {
-    return encode_tmap_bf16_2d(ta, A, K, a_rows, K * 2, BK, BM) && encode_tmap_bf16_2d(tb, B, K, N, K * 2, BK, BN);
+    return encode_tmap_bf16_2d(ta, A, K, a_rows, K * 2, BK, BM) && encode_tmap_bf16_2d(tb, B, K, N, K * 2, BK, kGemmBoxN);
+}
+
+int gemm_tile_n(int M, int N, int epi) {
+    // 128-wide tiles when 256-wide ones would leave SMs idle (SwiGLU needs the 256-wide gate|up tile)
+    if (epi == EPI_SWIGLU) return 256;
+    const long long tiles256 = (long long)((M + BM - 1) / BM) * ((N + 255) / 256);
+    return tiles256 < device_sm_count() ? 128 : 256;
 }
 
 cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
+    const bool narrow = gemm_tile_n(a.M, a.N, a.epi) == 128;
     switch (a.epi) {
-        case EPI_BF16: return launch_epi<EPI_BF16>(ta, tb, a, st);
-        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(ta, tb, a, st);
-        case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(ta, tb, a, st);
-        case EPI_F32: return launch_epi<EPI_F32>(ta, tb, a, st);
-        case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE>(ta, tb, a, st);
+        case EPI_BF16: return narrow ? launch_epi<EPI_BF16, 128>(ta, tb, a, st) : launch_epi<EPI_BF16, 256>(ta, tb, a, st);
+        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, 256>(ta, tb, a, st);
+        case EPI_RESIDUAL:
+            return narrow ? launch_epi<EPI_RESIDUAL, 128>(ta, tb, a, st) : launch_epi<EPI_RESIDUAL, 256>(ta, tb, a, st);
+        case EPI_F32: return narrow ? launch_epi<EPI_F32, 128>(ta, tb, a, st) : launch_epi<EPI_F32, 256>(ta, tb, a, st);
+        case EPI_QKV_ROPE:
+            return narrow ? launch_epi<EPI_QKV_ROPE, 128>(ta, tb, a, st) : launch_epi<EPI_QKV_ROPE, 256>(ta, tb, a, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -6,7 +6,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace q3 {
+
+// Launch with programmatic stream serialization, so the kernel's prologue can overlap the tail of the
+// previous kernel on the stream; every kernel of this library calls pdl_wait() before touching memory
+// that earlier kernels produce or read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device error-flag bits (one int per context, read by qwen3_get_error).
 enum : int { ERR_TOKEN = 1, ERR_TIMEOUT = 2 };
@@ -40,7 +61,8 @@ struct GemmArgs {
     int* err;
     QkvRopeArgs qkv;
 };
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
+// Tile rows of A, TMA box rows of B (a 256-wide tile loads two boxes), K per stage.
+constexpr int kGemmBM = 128, kGemmBoxN = 128, kGemmBK = 64;
 // A: [rows >= M, K] activations; B: [N, K] weights. Both maps are built with encode_gemm_maps.
 bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t a_rows, const void* B, uint64_t N,
                       uint64_t K);

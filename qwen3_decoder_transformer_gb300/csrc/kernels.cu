@@ -16,6 +16,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // x = E[ids] ("A modern architecture: Qwen3", The whole model: embed_tokens(ids)). One warp per row.
 __global__ void embed_kernel(const __nv_bfloat16* __restrict__ E, int V, int d, const int32_t* __restrict__ ids, int M,
                              __nv_bfloat16* __restrict__ out, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
@@ -60,6 +62,8 @@ template <int CACHE>
 __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int rows,
                                int n, long long in_stride, long long in_offset, float eps,
                                __nv_bfloat16* __restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -115,6 +119,8 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
                                           const __nv_bfloat16* __restrict__ table, const int* __restrict__ len0p,
                                           float eps, __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
                                           __nv_bfloat16* __restrict__ vc, int cap) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int E = DH / 32;  // 2 or 4 features per lane
     constexpr int HALF = DH / 2;
     const int H = Hq + 2 * Hkv;
@@ -181,8 +187,16 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
     else *reinterpret_cast<uint32_t*>(dst) = o[0];
 }
 
-__global__ void set_len_kernel(int* len, int value) { *len = value; }
-__global__ void add_len_kernel(int* len, int delta) { *len += delta; }
+__global__ void set_len_kernel(int* len, int value) {
+    pdl_wait();
+    pdl_trigger();
+    *len = value;
+}
+__global__ void add_len_kernel(int* len, int delta) {
+    pdl_wait();
+    pdl_trigger();
+    *len += delta;
+}
 
 }  // namespace
 
@@ -190,8 +204,8 @@ cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* id
                          cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
     const int threads = 256, rows_per_block = threads / 32;
-    embed_kernel<<<(M + rows_per_block - 1) / rows_per_block, threads, 0, st>>>(E, V, d, ids, M, out, err);
-    return cudaGetLastError();
+    return launch_pdl(embed_kernel, dim3((M + rows_per_block - 1) / rows_per_block), dim3(threads), 0, st, E, V, d, ids,
+                      M, out, err);
 }
 
 cudaError_t rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* g, int rows, int n, long long in_stride,
@@ -199,9 +213,10 @@ cudaError_t rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* g, int r
     if (rows <= 0) return cudaSuccess;
     const int threads = 128, rpb = threads / 32;
     const int blocks = (rows + rpb - 1) / rpb;
-    if (n <= 32 * 8 * 4) rmsnorm_kernel<4><<<blocks, threads, 0, st>>>(x, g, rows, n, in_stride, in_offset, eps, y);
-    else rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, g, rows, n, in_stride, in_offset, eps, y);
-    return cudaGetLastError();
+    if (n <= 32 * 8 * 4)
+        return launch_pdl(rmsnorm_kernel<4>, dim3(blocks), dim3(threads), 0, st, x, g, rows, n, in_stride, in_offset, eps,
+                          y);
+    return launch_pdl(rmsnorm_kernel<16>, dim3(blocks), dim3(threads), 0, st, x, g, rows, n, in_stride, in_offset, eps, y);
 }
 
 cudaError_t rope_table_launch(float theta, int dh, int n_pos, __nv_bfloat16* table, cudaStream_t st) {
@@ -231,24 +246,20 @@ cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, in
     const int threads = 256, wpb = threads / 32;
     const unsigned blocks = (unsigned)((warps + wpb - 1) / wpb);
     if (dh == 128)
-        qknorm_rope_append_kernel<128>
-            <<<blocks, threads, 0, st>>>(qkv, B, T, Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
-    else if (dh == 64)
-        qknorm_rope_append_kernel<64>
-            <<<blocks, threads, 0, st>>>(qkv, B, T, Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_pdl(qknorm_rope_append_kernel<128>, dim3(blocks), dim3(threads), 0, st, qkv, B, T, Hq, Hkv, qg, kg,
+                          table, len0, eps, q_out, kc, vc, cap);
+    if (dh == 64)
+        return launch_pdl(qknorm_rope_append_kernel<64>, dim3(blocks), dim3(threads), 0, st, qkv, B, T, Hq, Hkv, qg, kg,
+                          table, len0, eps, q_out, kc, vc, cap);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t set_len_launch(int* len, int value, cudaStream_t st) {
-    set_len_kernel<<<1, 1, 0, st>>>(len, value);
-    return cudaGetLastError();
+    return launch_pdl(set_len_kernel, dim3(1), dim3(1), 0, st, len, value);
 }
 
 cudaError_t add_len_launch(int* len, int delta, cudaStream_t st) {
-    add_len_kernel<<<1, 1, 0, st>>>(len, delta);
-    return cudaGetLastError();
+    return launch_pdl(add_len_kernel, dim3(1), dim3(1), 0, st, len, delta);
 }
 
 }  // namespace q3

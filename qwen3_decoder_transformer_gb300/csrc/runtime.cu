@@ -361,18 +361,18 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          encode_tmap_bf16_2d(&c->tA_attn, c->attn, c->q_width, arows, (uint64_t)c->q_width * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tA_h, c->h, F, arows, (uint64_t)F * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
-         encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBN);
+         encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN);
     c->tB_qkv.resize(L);
     c->tB_o.resize(L);
     c->tB_gu.resize(L);
     c->tB_down.resize(L);
     for (int l = 0; ok && l < L; ++l) {
         ok = encode_tmap_bf16_2d(&c->tB_qkv[l], c->wqkv + (size_t)l * c->qkv_n * d, d, c->qkv_n, (uint64_t)d * 2,
-                                 kGemmBK, kGemmBN) &&
-             encode_tmap_bf16_2d(&c->tB_o[l], c->o_proj[l], c->q_width, d, (uint64_t)c->q_width * 2, kGemmBK, kGemmBN) &&
+                                 kGemmBK, kGemmBoxN) &&
+             encode_tmap_bf16_2d(&c->tB_o[l], c->o_proj[l], c->q_width, d, (uint64_t)c->q_width * 2, kGemmBK, kGemmBoxN) &&
              encode_tmap_bf16_2d(&c->tB_gu[l], c->wgu + (size_t)l * 2 * F * d, d, 2 * F, (uint64_t)d * 2, kGemmBK,
-                                 kGemmBN) &&
-             encode_tmap_bf16_2d(&c->tB_down[l], c->down_proj[l], F, d, (uint64_t)F * 2, kGemmBK, kGemmBN);
+                                 kGemmBoxN) &&
+             encode_tmap_bf16_2d(&c->tB_down[l], c->down_proj[l], F, d, (uint64_t)F * 2, kGemmBK, kGemmBoxN);
     }
     ok = ok && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
