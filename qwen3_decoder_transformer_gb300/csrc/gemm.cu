@@ -35,6 +35,8 @@ namespace {
 constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int THREADS = 192;
+constexpr int STG_BYTES = 32768;
+constexpr int EPI_LEADER = 64;  // thread 0 of warp 2 issues the epilogue's TMA loads and stores
 // Per tile width BN (256, or 128 when 256-wide tiles cannot fill the SMs): stage size, ring depth,
 // TMEM columns (two accumulators) and the instruction descriptor.
 template <int BN>
@@ -43,7 +45,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int STG_OFF = STAGES * STAGE_BYTES;  // epilogue staging: 2 boxes of [128 rows][128 B]
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 };
 
@@ -67,192 +71,237 @@ __device__ __forceinline__ Tile tile_of(int t, int m_tiles, int n_tiles) {
 // unchanged and Q/K heads get RMSNorm over head_dim (fp32 reduce, bf16 cast, then gamma) and RoPE
 // (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the pair (i, i + dh/2)).
 template <int DH, int BN>
-__device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t tacc, int row, int n0) {
+__device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t tacc, int row, int n0, uint64_t* acc_empty) {
     const QkvRopeArgs& q = a.qkv;
     const bool row_ok = row < a.M;
     const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
     const int pos = *q.len0 + t;
     constexpr int HALF = DH / 2;
+    constexpr int NHEAD = BN / DH;
 #pragma unroll 1
-    for (int lh = 0; lh < BN / DH; ++lh) {
+    for (int lh = 0; lh < NHEAD; ++lh) {
         const int hg = n0 / DH + lh;
-        const uint32_t th = tacc + lh * DH;
+        uint32_t x[DH];
+#pragma unroll
+        for (int c = 0; c < DH / 32; ++c)
+            tmem_ld_32x32b_x32(tacc + lh * DH + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+        tmem_ld_wait();
+        if (lh == NHEAD - 1) {
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+        }
+        if (!row_ok) continue;
         if (hg >= q.Hq + q.Hkv) {  // V head: copy to the cache slot
             __nv_bfloat16* dst = q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + pos) * DH;
-#pragma unroll 1
-            for (int c = 0; c < DH / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(th + c * 32, r);
-                tmem_ld_wait();
-                if (!row_ok) continue;
-                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            for (int v = 0; v < DH / 8; ++v) {
+                uint32_t w[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    reinterpret_cast<uint4*>(dst + c * 32)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                for (int e = 0; e < 4; ++e) w[e] = pack_bf16(__uint_as_float(x[8 * v + 2 * e]), __uint_as_float(x[8 * v + 2 * e + 1]));
+                reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
             }
             continue;
         }
         const bool is_q = hg < q.Hq;
-        // pass 1: sum of squares of the bf16-rounded projection
         float ss = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(th + c * 32, r);
-            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float x = rbf(__uint_as_float(r[j]));
-                ss = fmaf(x, x, ss);
-            }
+        for (int j = 0; j < DH; ++j) {
+            const float xv = rbf(__uint_as_float(x[j]));
+            x[j] = __float_as_uint(xv);
+            ss = fmaf(xv, xv, ss);
         }
         const float rn = __frsqrt_rn(ss / (float)DH + q.eps);
         const __nv_bfloat16* gam = is_q ? q.q_gamma : q.k_gamma;
         const __nv_bfloat16* cs = q.table + (size_t)pos * DH;
         __nv_bfloat16* dst = is_q ? q.q_out + (((size_t)b * q.Hq + hg) * q.T + t) * DH
                                   : q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + pos) * DH;
-        // pass 2: 32 rotation pairs at a time, (i, i + HALF)
-#pragma unroll 1
-        for (int c = 0; c < HALF / 32; ++c) {
-            uint32_t lo[32], hi[32];
-            tmem_ld_32x32b_x32(th + c * 32, lo);
-            tmem_ld_32x32b_x32(th + HALF + c * 32, hi);
-            tmem_ld_wait();
-            if (!row_ok) continue;
-            uint32_t wlo[16], whi[16];
+        // rotation pairs (i, i + HALF), 8 at a time
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam + c * 32) + v);
-                const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF + c * 32) + v);
-                const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs + c * 32) + v);
-                const uint4 sn = __ldg(reinterpret_cast<const uint4*>(cs + HALF + c * 32) + v);
-                const uint32_t G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
-                const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
+        for (int v = 0; v < HALF / 8; ++v) {
+            const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam) + v);
+            const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF) + v);
+            const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs) + v);
+            const uint4 sn = __ldg(reinterpret_cast<const uint4*>(cs + HALF) + v);
+            const uint32_t G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
+            const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
+            uint32_t wlo[4], whi[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float o_lo[2], o_hi[2];
+            for (int e = 0; e < 4; ++e) {
+                float o_lo[2], o_hi[2];
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int j = 8 * v + 2 * e + k;
-                        const float ga = k ? bf16_hi(G0[e]) : bf16_lo(G0[e]);
-                        const float gb = k ? bf16_hi(G1[e]) : bf16_lo(G1[e]);
-                        const float co = k ? bf16_hi(C[e]) : bf16_lo(C[e]);
-                        const float si = k ? bf16_hi(S[e]) : bf16_lo(S[e]);
-                        const float av = rbf(ga * rbf(rbf(__uint_as_float(lo[j])) * rn));
-                        const float bv = rbf(gb * rbf(rbf(__uint_as_float(hi[j])) * rn));
-                        o_lo[k] = rbf(av * co) + rbf(-(bv * si));
-                        o_hi[k] = rbf(bv * co) + rbf(av * si);
-                    }
-                    wlo[4 * v + e] = pack_bf16(o_lo[0], o_lo[1]);
-                    whi[4 * v + e] = pack_bf16(o_hi[0], o_hi[1]);
+                for (int k = 0; k < 2; ++k) {
+                    const int j = 8 * v + 2 * e + k;
+                    const float ga = k ? bf16_hi(G0[e]) : bf16_lo(G0[e]);
+                    const float gb = k ? bf16_hi(G1[e]) : bf16_lo(G1[e]);
+                    const float co = k ? bf16_hi(C[e]) : bf16_lo(C[e]);
+                    const float si = k ? bf16_hi(S[e]) : bf16_lo(S[e]);
+                    const float av = rbf(ga * rbf(__uint_as_float(x[j]) * rn));
+                    const float bv = rbf(gb * rbf(__uint_as_float(x[j + HALF]) * rn));
+                    o_lo[k] = rbf(av * co) + rbf(-(bv * si));
+                    o_hi[k] = rbf(bv * co) + rbf(av * si);
                 }
+                wlo[e] = pack_bf16(o_lo[0], o_lo[1]);
+                whi[e] = pack_bf16(o_hi[0], o_hi[1]);
             }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                reinterpret_cast<uint4*>(dst + c * 32)[v] = make_uint4(wlo[4 * v], wlo[4 * v + 1], wlo[4 * v + 2], wlo[4 * v + 3]);
-                reinterpret_cast<uint4*>(dst + HALF + c * 32)[v] =
-                    make_uint4(whi[4 * v], whi[4 * v + 1], whi[4 * v + 2], whi[4 * v + 3]);
-            }
+            reinterpret_cast<uint4*>(dst)[v] = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+            reinterpret_cast<uint4*>(dst + HALF)[v] = make_uint4(whi[0], whi[1], whi[2], whi[3]);
         }
     }
 }
 
+// Address of 16-byte chunk u (0..15) of tile row r in the staging buffer: two TMA boxes of
+// [128 rows][128 bytes] in the 128-byte swizzle pattern (chunk index XOR row % 8).
+__device__ __forceinline__ uint8_t* stg_chunk(uint8_t* stg, int r, int u) {
+    return stg + (u >> 3) * 16384 + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+}
+
+struct EpiSync {
+    uint64_t* res_bar;  // residual tile arrival (TMA load, tx count)
+    uint32_t res_phase;
+    volatile int* fail;  // set by any epilogue warp whose wait gave up
+};
+
+// Make a warp's wait outcome uniform over the four epilogue warps: every thread reaches the barrier
+// (the waits before it are bounded), so all four warps take the same branch afterwards.
+__device__ __forceinline__ bool epi_agree(bool ok, volatile int* fail) {
+    if (!__all_sync(0xffffffffu, ok) && (threadIdx.x & 31) == 0) *fail = 1;
+    named_barrier(1, 128);
+    return *fail == 0;
+}
+
+// Staging-buffer hand-off between passes: the previous TMA store must have read it.
+__device__ __forceinline__ void stg_acquire() {
+    if (threadIdx.x == EPI_LEADER) bulk_wait_read();
+    named_barrier(1, 128);
+}
+// Publish the staging buffer (generic-proxy writes) to the TMA store and issue it.
+__device__ __forceinline__ void stg_store(uint8_t* stg, const CUtensorMap* tmC, int x0, int x1, int y) {
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (threadIdx.x == EPI_LEADER) {
+        tma_store_2d(tmC, stg, x0, y);
+        tma_store_2d(tmC, stg + 16384, x1, y);
+        bulk_commit();
+    }
+}
+
+// Load 128 consecutive accumulator columns of this thread's row (4 loads, one wait).
+__device__ __forceinline__ void tmem_ld_128(uint32_t taddr, uint32_t (&r)[128]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+    tmem_ld_wait();
+}
+
+// Epilogue of one tile for the staged epilogues (BF16, RESIDUAL, SWIGLU, F32). The accumulator is
+// released (acc_empty) as soon as its last columns are in registers; outputs go through the staging
+// buffer and TMA stores, so each warp writes whole swizzled rows to shared memory and the copy to
+// global memory is one coalesced bulk operation per box. Returns false if a wait gave up.
 template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_chunks(const GemmArgs& a, uint32_t tacc, int row, int n0) {
-    const bool row_ok = row < a.M;
-    if constexpr (EPI == EPI_QKV_ROPE) {
-        if (a.qkv.dh == 128) epilogue_qkv_rope<128, BN>(a, tacc, row, n0);
-        else epilogue_qkv_rope<64, BN>(a, tacc, row, n0);
-    } else if constexpr (EPI == EPI_SWIGLU) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.C) + (size_t)row * a.ldc + n0 / 2;
+__device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmR,
+                                                uint8_t* stg, EpiSync& es, uint32_t tacc, int r, int m0, int n0,
+                                                uint64_t* acc_empty, uint64_t* acc_full, uint32_t aph,
+                                                volatile int* abort_flag) {
+    bool ok = true;
+    // passes of 128 bf16 (or 64 fp32) output columns, each filling the 32 KB staging buffer
+    constexpr int PASSES = EPI == EPI_SWIGLU ? 1 : (EPI == EPI_F32 ? BN / 64 : BN / 128);
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32b_x32(tacc + c * 32, g);
-            tmem_ld_32x32b_x32(tacc + BN / 2 + c * 32, u);
-            tmem_ld_wait();
-            if (!row_ok) continue;
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float g0 = rbf(__uint_as_float(g[2 * j])), g1 = rbf(__uint_as_float(g[2 * j + 1]));
-                float s0 = rbf(g0 / (1.0f + expf(-g0))), s1 = rbf(g1 / (1.0f + expf(-g1)));
-                w[j] = pack_bf16(s0 * rbf(__uint_as_float(u[2 * j])), s1 * rbf(__uint_as_float(u[2 * j + 1])));
+    for (int p = 0; p < PASSES; ++p) {
+        stg_acquire();
+        if constexpr (EPI == EPI_RESIDUAL) {
+            if (threadIdx.x == EPI_LEADER) {
+                mbar_expect_tx(es.res_bar, STG_BYTES);
+                tma_load_2d(stg, tmR, es.res_bar, n0 + p * 128, m0);
+                tma_load_2d(stg + 16384, tmR, es.res_bar, n0 + p * 128 + 64, m0);
             }
-            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
-    } else {
+        if (p == 0) {
+            // the accumulator of this tile
+            const bool w = mbar_wait(acc_full, aph, abort_flag);
+            if (!epi_agree(w, es.fail)) return false;
+            tc_fence_after();
+        }
+        if constexpr (EPI == EPI_SWIGLU) {
+            // gate columns [0, BN/2), up columns [BN/2, BN): 64 outputs per half
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tacc + c * 32, r);
-            tmem_ld_wait();
-            const int col0 = n0 + c * 32;
-            if (!row_ok || col0 >= a.N) continue;
-            const bool full = col0 + 32 <= a.N;
-            if constexpr (EPI == EPI_F32) {
-                float* dst = reinterpret_cast<float*>(a.C) + (size_t)row * a.ldc + col0;
-                if (full) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        reinterpret_cast<float4*>(dst)[v] =
-                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                } else {
-                    for (int j = 0; j < a.N - col0; ++j) dst[j] = __uint_as_float(r[j]);
+            for (int hf = 0; hf < BN / 128; ++hf) {
+                uint32_t g[64], u[64];
+                tmem_ld_32x32b_x32(tacc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+                tmem_ld_32x32b_x32(tacc + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+                tmem_ld_32x32b_x32(tacc + BN / 2 + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+                tmem_ld_32x32b_x32(tacc + BN / 2 + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld_wait();
+                if (hf == BN / 128 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(acc_empty);
                 }
-            } else {
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.C) + (size_t)row * a.ldc + col0;
-                float add[32];
-                if constexpr (EPI == EPI_RESIDUAL) {
-                    const __nv_bfloat16* src = a.R + (size_t)row * a.ldr + col0;
-                    if (full) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 q = reinterpret_cast<const uint4*>(src)[v];
-                            uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t wv[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                add[8 * v + 2 * e] = bf16_lo(qq[e]);
-                                add[8 * v + 2 * e + 1] = bf16_hi(qq[e]);
-                            }
-                        }
-                    } else {
-                        for (int j = 0; j < 32; ++j) add[j] = (col0 + j < a.N) ? bf16f(src[j]) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = q * 8 + 2 * e;
+                        const float g0 = rbf(__uint_as_float(g[j])), g1 = rbf(__uint_as_float(g[j + 1]));
+                        const float s0 = rbf(__fdividef(g0, 1.0f + __expf(-g0)));
+                        const float s1 = rbf(__fdividef(g1, 1.0f + __expf(-g1)));
+                        wv[e] = pack_bf16(s0 * rbf(__uint_as_float(u[j])), s1 * rbf(__uint_as_float(u[j + 1])));
                     }
-                }
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float x0 = __uint_as_float(r[2 * j]), x1 = __uint_as_float(r[2 * j + 1]);
-                    if constexpr (EPI == EPI_RESIDUAL) {
-                        x0 = add[2 * j] + rbf(x0);
-                        x1 = add[2 * j + 1] + rbf(x1);
-                    }
-                    w[j] = pack_bf16(x0, x1);
-                }
-                if (full) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-                } else {
-                    for (int j = 0; j < a.N - col0; ++j) {
-                        uint32_t h = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-                        reinterpret_cast<uint16_t*>(dst)[j] = (uint16_t)h;
-                    }
+                    *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
+            stg_store(stg, tmC, n0 / 2, n0 / 2 + 64, m0);
+        } else if constexpr (EPI == EPI_F32) {
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(tacc + p * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(tacc + p * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+            if (p == PASSES - 1) {
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            stg_store(stg, tmC, n0 + p * 64, n0 + p * 64 + 32, m0);
+        } else {
+            uint32_t v[128];
+            tmem_ld_128(tacc + p * 128, v);
+            if (p == PASSES - 1) {
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+            }
+            if constexpr (EPI == EPI_RESIDUAL) {
+                const bool w = mbar_wait(es.res_bar, es.res_phase & 1, abort_flag);
+                ++es.res_phase;
+                if (!epi_agree(w, es.fail)) return false;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, u));
+                uint32_t wv[4];
+                if constexpr (EPI == EPI_RESIDUAL) {
+                    const uint4 q = *cp;
+                    const uint32_t rr[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wv[e] = pack_bf16(bf16_lo(rr[e]) + rbf(__uint_as_float(v[8 * u + 2 * e])),
+                                          bf16_hi(rr[e]) + rbf(__uint_as_float(v[8 * u + 2 * e + 1])));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wv[e] = pack_bf16(__uint_as_float(v[8 * u + 2 * e]), __uint_as_float(v[8 * u + 2 * e + 1]));
+                }
+                *cp = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            stg_store(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
         }
     }
+    return ok;
 }
 
 template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                         const GemmArgs args) {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, TMEM_COLS = C::TMEM_COLS;
@@ -260,12 +309,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* stg = smem + C::STG_OFF;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty_bar = full_bar + STAGES;
     uint64_t* acc_full = empty_bar + STAGES;
     uint64_t* acc_empty = acc_full + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* res_bar = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(res_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* epi_fail = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
@@ -281,10 +333,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 128);
         }
+        mbar_init(res_bar, 1);
         *abort_flag = 0;
+        *epi_fail = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (EPI != EPI_QKV_ROPE) tma_prefetch_desc(&tmC);
+        if constexpr (EPI == EPI_RESIDUAL) tma_prefetch_desc(&tmR);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -342,19 +398,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp >= 2) {
         // ---------------- epilogue
         const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // tile row = TMEM lane
+        EpiSync es{res_bar, 0, epi_fail};
         int local = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
-            // every lane waits, so the warp stays converged for the .sync.aligned TMEM loads
-            if (!mbar_wait(&acc_full[acc], aph, abort_flag)) { ok = false; }
-            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-            tc_fence_after();
             const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-            epilogue_chunks<EPI, BN>(args, tacc, tl.m0 + quarter * 32 + lane, tl.n0);
-            tc_fence_before();
-            mbar_arrive(&acc_empty[acc]);
+            if constexpr (EPI == EPI_QKV_ROPE) {
+                // every lane waits, so the warp stays converged for the .sync.aligned TMEM loads
+                const bool w = mbar_wait(&acc_full[acc], aph, abort_flag);
+                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                tc_fence_after();
+                if (args.qkv.dh == 128) epilogue_qkv_rope<128, BN>(args, tacc, tl.m0 + r, tl.n0, &acc_empty[acc]);
+                else epilogue_qkv_rope<64, BN>(args, tacc, tl.m0 + r, tl.n0, &acc_empty[acc]);
+            } else {
+                if (!epilogue_staged<EPI, BN>(args, &tmC, &tmR, stg, es, tacc, r, tl.m0, tl.n0, &acc_empty[acc],
+                                              &acc_full[acc], aph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        // the last TMA stores must finish before the CTA exits
+        if constexpr (EPI != EPI_QKV_ROPE) {
+            if (threadIdx.x == EPI_LEADER) bulk_wait_all();
         }
     }
     if (!ok) {
@@ -385,10 +454,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int EPI, int BN>
-cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_epi(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int grid = std::min(tiles, device_sm_count());
-    return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(THREADS), Cfg<BN>::SMEM_BYTES, st, ta, tb, a);
+    return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(THREADS), Cfg<BN>::SMEM_BYTES, st, m.a, m.b, m.c,
+                      m.r, a);
 }
 
 }  // namespace
@@ -432,18 +502,27 @@ bool device_is_sm103() {
     return major == 10 && minor == 3;
 }
 
-bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                         uint32_t box_inner, uint32_t box_outer) {
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes, box_inner, box_outer);
+}
+
+bool encode_tmap_out(CUtensorMap* map, const void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t ld) {
+    if (f32) return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, cols, rows, ld * 4, 32, kGemmBM);
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, ld * 2, 64, kGemmBM);
 }
 
 bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t a_rows, const void* B, uint64_t N,
@@ -458,17 +537,15 @@ int gemm_tile_n(int M, int N, int epi) {
     return tiles256 < device_sm_count() ? 128 : 256;
 }
 
-cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, cudaStream_t st) {
+cudaError_t gemm_launch(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
     const bool narrow = gemm_tile_n(a.M, a.N, a.epi) == 128;
     switch (a.epi) {
-        case EPI_BF16: return narrow ? launch_epi<EPI_BF16, 128>(ta, tb, a, st) : launch_epi<EPI_BF16, 256>(ta, tb, a, st);
-        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, 256>(ta, tb, a, st);
-        case EPI_RESIDUAL:
-            return narrow ? launch_epi<EPI_RESIDUAL, 128>(ta, tb, a, st) : launch_epi<EPI_RESIDUAL, 256>(ta, tb, a, st);
-        case EPI_F32: return narrow ? launch_epi<EPI_F32, 128>(ta, tb, a, st) : launch_epi<EPI_F32, 256>(ta, tb, a, st);
-        case EPI_QKV_ROPE:
-            return narrow ? launch_epi<EPI_QKV_ROPE, 128>(ta, tb, a, st) : launch_epi<EPI_QKV_ROPE, 256>(ta, tb, a, st);
+        case EPI_BF16: return narrow ? launch_epi<EPI_BF16, 128>(m, a, st) : launch_epi<EPI_BF16, 256>(m, a, st);
+        case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, 256>(m, a, st);
+        case EPI_RESIDUAL: return narrow ? launch_epi<EPI_RESIDUAL, 128>(m, a, st) : launch_epi<EPI_RESIDUAL, 256>(m, a, st);
+        case EPI_F32: return narrow ? launch_epi<EPI_F32, 128>(m, a, st) : launch_epi<EPI_F32, 256>(m, a, st);
+        case EPI_QKV_ROPE: return narrow ? launch_epi<EPI_QKV_ROPE, 128>(m, a, st) : launch_epi<EPI_QKV_ROPE, 256>(m, a, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -66,7 +66,14 @@ constexpr int kGemmBM = 128, kGemmBoxN = 128, kGemmBK = 64;
 // A: [rows >= M, K] activations; B: [N, K] weights. Both maps are built with encode_gemm_maps.
 bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t a_rows, const void* B, uint64_t N,
                       uint64_t K);
-cudaError_t gemm_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t st);
+// Output / residual map for the staged epilogues: a [rows, cols] matrix with row stride ld elements,
+// boxes of 128 rows x 128 bytes (64 bf16 or 32 fp32 columns).
+bool encode_tmap_out(CUtensorMap* map, const void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t ld);
+// The four tensor maps of one GEMM launch: A, B, the output C (staged epilogues) and the residual R.
+struct GemmMaps {
+    CUtensorMap a, b, c, r;
+};
+cudaError_t gemm_launch(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
 
 // ---------------------------------------------------------------- small kernels (kernels.cu)
 cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* ids, int M, __nv_bfloat16* out, int* err,

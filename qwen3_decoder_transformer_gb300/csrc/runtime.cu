@@ -92,6 +92,7 @@ struct qwen3_ctx {
     int len = 0, batch = 0;
     // tensor maps: A operands (activation buffers) and B operands (weights) per layer
     CUtensorMap tA_xn, tA_attn, tA_h, tA_hn;
+    CUtensorMap tC_x, tC_h;  // staged-epilogue outputs: residual stream (also the residual input), SwiGLU output
     std::vector<CUtensorMap> tB_qkv, tB_o, tB_gu, tB_down;
     CUtensorMap tB_head;
     // decode graphs
@@ -144,10 +145,17 @@ int timed(qwen3_ctx* c, int cls, int launches, cudaStream_t st, F&& fn) {
         if (_rc != QWEN3_OK) return _rc;    \
     } while (0)
 
-int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int epi, void* C,
-         long long ldc, const bf16* R, long long ldr, cudaStream_t st) {
+int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tc,
+         const CUtensorMap* tr, int M, int N, int K, int epi, void* C, long long ldc, const bf16* R, long long ldr,
+         cudaStream_t st) {
     GemmArgs a{M, N, K, epi, C, ldc, R, ldr, c->d_err, {}};
-    return timed(c, cls, 1, st, [&] { return gemm_launch(ta, tb, a, st); });
+    GemmMaps m;
+    std::memset(&m, 0, sizeof(m));
+    m.a = ta;
+    m.b = tb;
+    if (tc) m.c = *tc;
+    if (tr) m.r = *tr;
+    return timed(c, cls, 1, st, [&] { return gemm_launch(m, a, st); });
 }
 
 bf16* layer_k(qwen3_ctx* c, int l) { return c->kcache + (size_t)l * c->layer_elems; }
@@ -170,7 +178,11 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, nullptr, 0, nullptr, 0, c->d_err,
                        QkvRopeArgs{c->q_norm[l], c->k_norm[l], c->rope, c->d_len, c->q, layer_k(c, l), layer_v(c, l), T,
                                    g.n_q_heads, g.n_kv_heads, dh, c->capacity, g.rms_eps}};
-            TRY(timed(c, K_GEMM_QKV, 1, st, [&] { return gemm_launch(c->tA_xn, c->tB_qkv[l], a, st); }));
+            GemmMaps m;
+            std::memset(&m, 0, sizeof(m));
+            m.a = c->tA_xn;
+            m.b = c->tB_qkv[l];
+            TRY(timed(c, K_GEMM_QKV, 1, st, [&] { return gemm_launch(m, a, st); }));
         }
         if (decode) {
             TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
@@ -183,11 +195,14 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
                                            c->capacity, c->d_len, c->attn, c->d_err, st);
             }));
         }
-        TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], M, d, c->q_width, EPI_RESIDUAL, c->x, d, c->x, d, st));
+        TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
+                 c->x, d, st));
         TRY(timed(c, K_RMSNORM, 1, st,
                   [&] { return rmsnorm_launch(c->x, c->post_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
-        TRY(gemm(c, K_GEMM_GATEUP, c->tA_xn, c->tB_gu[l], M, 2 * F, d, EPI_SWIGLU, c->h, F, nullptr, 0, st));
-        TRY(gemm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], M, d, F, EPI_RESIDUAL, c->x, d, c->x, d, st));
+        TRY(gemm(c, K_GEMM_GATEUP, c->tA_xn, c->tB_gu[l], &c->tC_h, nullptr, M, 2 * F, d, EPI_SWIGLU, c->h, F,
+                 nullptr, 0, st));
+        TRY(gemm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], &c->tC_x, &c->tC_x, M, d, F, EPI_RESIDUAL, c->x, d, c->x, d,
+                 st));
         if (l == c->tap_layer && c->tap_out)
             if (cudaMemcpyAsync(c->tap_out, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
                 return QWEN3_E_CUDA;
@@ -198,7 +213,10 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         return all_rows ? rmsnorm_launch(c->x, c->final_norm, rows, d, 1, 0, g.rms_eps, c->hn, st)
                         : rmsnorm_launch(c->x, c->final_norm, rows, d, T, T - 1, g.rms_eps, c->hn, st);
     }));
-    TRY(gemm(c, K_GEMM_LMHEAD, c->tA_hn, c->tB_head, rows, g.vocab, d, EPI_F32, logits, g.vocab, nullptr, 0, st));
+    CUtensorMap t_logits;
+    if (!encode_tmap_out(&t_logits, logits, true, g.vocab, rows, g.vocab)) return QWEN3_E_CUDA;
+    TRY(gemm(c, K_GEMM_LMHEAD, c->tA_hn, c->tB_head, &t_logits, nullptr, rows, g.vocab, d, EPI_F32, logits, g.vocab,
+             nullptr, 0, st));
     TRY(timed(c, K_LENGTH, 1, st, [&] { return add_len_launch(c->d_len, T, st); }));
     return QWEN3_OK;
 }
@@ -361,7 +379,8 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          encode_tmap_bf16_2d(&c->tA_attn, c->attn, c->q_width, arows, (uint64_t)c->q_width * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tA_h, c->h, F, arows, (uint64_t)F * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
-         encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN);
+         encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN) &&
+         encode_tmap_out(&c->tC_x, c->x, false, d, rows, d) && encode_tmap_out(&c->tC_h, c->h, false, F, arows, F);
     c->tB_qkv.resize(L);
     c->tB_o.resize(L);
     c->tB_gu.resize(L);
@@ -574,10 +593,15 @@ int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, vo
         return QWEN3_E_ARG;
     if (M == 0) return QWEN3_OK;
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
-    CUtensorMap ta, tb;
-    if (!encode_gemm_maps(&ta, &tb, A, (uint64_t)M, B, (uint64_t)N, (uint64_t)K)) return QWEN3_E_CUDA;
+    GemmMaps m;
+    std::memset(&m, 0, sizeof(m));
+    if (!encode_gemm_maps(&m.a, &m.b, A, (uint64_t)M, B, (uint64_t)N, (uint64_t)K)) return QWEN3_E_CUDA;
+    const uint64_t out_cols = epi == EPI_SWIGLU ? (uint64_t)N / 2 : (uint64_t)N;
+    if (!encode_tmap_out(&m.c, C, epi == EPI_F32, out_cols, (uint64_t)M, (uint64_t)ldc)) return QWEN3_E_CUDA;
+    if (epi == EPI_RESIDUAL && !encode_tmap_out(&m.r, R, false, (uint64_t)N, (uint64_t)M, (uint64_t)ldr))
+        return QWEN3_E_CUDA;
     GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
-    return gemm_launch(ta, tb, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
+    return gemm_launch(m, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
 int qwen3_op_pack_gate_up(const void* gate, const void* up, int F, int d, void* out, void* stream) {
