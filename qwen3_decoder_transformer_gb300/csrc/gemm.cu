@@ -70,85 +70,6 @@ __device__ __forceinline__ Tile tile_of(int t, int m_tiles, int n_tiles) {
 // projection output is rounded to bf16 as the unfused path stores it, then V heads go to the cache
 // unchanged and Q/K heads get RMSNorm over head_dim (fp32 reduce, bf16 cast, then gamma) and RoPE
 // (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the pair (i, i + dh/2)).
-template <int DH, int BN>
-__device__ __forceinline__ void epilogue_qkv_rope(const GemmArgs& a, uint32_t tacc, int row, int n0, uint64_t* acc_empty) {
-    const QkvRopeArgs& q = a.qkv;
-    const bool row_ok = row < a.M;
-    const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
-    const int pos = *q.len0 + t;
-    constexpr int HALF = DH / 2;
-    constexpr int NHEAD = BN / DH;
-#pragma unroll 1
-    for (int lh = 0; lh < NHEAD; ++lh) {
-        const int hg = n0 / DH + lh;
-        uint32_t x[DH];
-#pragma unroll
-        for (int c = 0; c < DH / 32; ++c)
-            tmem_ld_32x32b_x32(tacc + lh * DH + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-        tmem_ld_wait();
-        if (lh == NHEAD - 1) {
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-        }
-        if (!row_ok) continue;
-        if (hg >= q.Hq + q.Hkv) {  // V head: copy to the cache slot
-            __nv_bfloat16* dst = q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + pos) * DH;
-#pragma unroll
-            for (int v = 0; v < DH / 8; ++v) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = pack_bf16(__uint_as_float(x[8 * v + 2 * e]), __uint_as_float(x[8 * v + 2 * e + 1]));
-                reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            continue;
-        }
-        const bool is_q = hg < q.Hq;
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < DH; ++j) {
-            const float xv = rbf(__uint_as_float(x[j]));
-            x[j] = __float_as_uint(xv);
-            ss = fmaf(xv, xv, ss);
-        }
-        const float rn = __frsqrt_rn(ss / (float)DH + q.eps);
-        const __nv_bfloat16* gam = is_q ? q.q_gamma : q.k_gamma;
-        const __nv_bfloat16* cs = q.table + (size_t)pos * DH;
-        __nv_bfloat16* dst = is_q ? q.q_out + (((size_t)b * q.Hq + hg) * q.T + t) * DH
-                                  : q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + pos) * DH;
-        // rotation pairs (i, i + HALF), 8 at a time
-#pragma unroll
-        for (int v = 0; v < HALF / 8; ++v) {
-            const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam) + v);
-            const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF) + v);
-            const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs) + v);
-            const uint4 sn = __ldg(reinterpret_cast<const uint4*>(cs + HALF) + v);
-            const uint32_t G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
-            const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
-            uint32_t wlo[4], whi[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float o_lo[2], o_hi[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int j = 8 * v + 2 * e + k;
-                    const float ga = k ? bf16_hi(G0[e]) : bf16_lo(G0[e]);
-                    const float gb = k ? bf16_hi(G1[e]) : bf16_lo(G1[e]);
-                    const float co = k ? bf16_hi(C[e]) : bf16_lo(C[e]);
-                    const float si = k ? bf16_hi(S[e]) : bf16_lo(S[e]);
-                    const float av = rbf(ga * rbf(__uint_as_float(x[j]) * rn));
-                    const float bv = rbf(gb * rbf(__uint_as_float(x[j + HALF]) * rn));
-                    o_lo[k] = rbf(av * co) + rbf(-(bv * si));
-                    o_hi[k] = rbf(bv * co) + rbf(av * si);
-                }
-                wlo[e] = pack_bf16(o_lo[0], o_lo[1]);
-                whi[e] = pack_bf16(o_hi[0], o_hi[1]);
-            }
-            reinterpret_cast<uint4*>(dst)[v] = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-            reinterpret_cast<uint4*>(dst + HALF)[v] = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-        }
-    }
-}
-
 // Address of 16-byte chunk u (0..15) of tile row r in the staging buffer: two TMA boxes of
 // [128 rows][128 bytes] in the 128-byte swizzle pattern (chunk index XOR row % 8).
 __device__ __forceinline__ uint8_t* stg_chunk(uint8_t* stg, int r, int u) {
@@ -298,11 +219,119 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
     return ok;
 }
 
+// Fused QKV epilogue for one tile: per head of the tile, each thread (one token row) rounds its
+// projection to bf16, then V heads are copied and Q/K heads get RMSNorm over head_dim (fp32 reduce,
+// bf16 cast, then gamma) and RoPE (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the
+// pair (i, i + dh/2)). When the tile's 128 rows are consecutive tokens of one sequence (prefill with
+// T % 128 == 0), each head's [128 x dh] block is written through the staging buffer with one 3-D TMA
+// store into Q [B*Hq][T][dh] or the cache [B*Hkv][cap][dh]; otherwise (decode) rows are stored directly.
+template <int DH, int BN>
+__device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                                  const CUtensorMap* tmV, uint8_t* stg, EpiSync& es, uint32_t tacc,
+                                                  int r, int m0, int n0, uint64_t* acc_empty, uint64_t* acc_full,
+                                                  uint32_t aph, volatile int* abort_flag) {
+    const QkvRopeArgs& q = a.qkv;
+    const int row = m0 + r;
+    const bool row_ok = row < a.M;
+    const bool staged = (q.T % BM) == 0;
+    const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
+    constexpr int HALF = DH / 2;
+    constexpr int NHEAD = BN / DH;
+    {
+        const bool w = mbar_wait(acc_full, aph, abort_flag);
+        if (staged) {
+            if (!epi_agree(w, es.fail)) return false;
+        } else if (!__all_sync(0xffffffffu, w)) {
+            return false;
+        }
+        tc_fence_after();
+    }
+    const int len0 = *q.len0;
+    const int pos = len0 + t;
+#pragma unroll 1
+    for (int lh = 0; lh < NHEAD; ++lh) {
+        const int hg = n0 / DH + lh;
+        uint32_t x[DH];
+#pragma unroll
+        for (int c = 0; c < DH / 32; ++c)
+            tmem_ld_32x32b_x32(tacc + lh * DH + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+        tmem_ld_wait();
+        if (lh == NHEAD - 1) {
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+        }
+        const int kind = hg < q.Hq ? 0 : (hg < q.Hq + q.Hkv ? 1 : 2);  // q, k, v
+        uint32_t o[DH / 2];  // packed bf16 outputs of this row
+        if (kind == 2) {
+#pragma unroll
+            for (int j = 0; j < DH / 2; ++j) o[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+        } else {
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < DH; ++j) {
+                const float xv = rbf(__uint_as_float(x[j]));
+                x[j] = __float_as_uint(xv);
+                ss = fmaf(xv, xv, ss);
+            }
+            const float rn = __frsqrt_rn(ss / (float)DH + q.eps);
+            const __nv_bfloat16* gam = kind == 0 ? q.q_gamma : q.k_gamma;
+            const __nv_bfloat16* cs = q.table + (size_t)(row_ok ? pos : 0) * DH;
+            // bf16x2 arithmetic: each packed multiply / add rounds once to bf16, as the definition does
+#pragma unroll
+            for (int v = 0; v < HALF / 8; ++v) {
+                const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam) + v);
+                const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF) + v);
+                const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs) + v);
+                const uint4 sn = __ldg(reinterpret_cast<const uint4*>(cs + HALF) + v);
+                const uint32_t G0[4] = {g0.x, g0.y, g0.z, g0.w}, G1[4] = {g1.x, g1.y, g1.z, g1.w};
+                const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 8 * v + 2 * e;
+                    // normalised, cast, then times gamma: a = first-half pair, bb = second-half pair
+                    const uint32_t na = pack_bf16(__uint_as_float(x[j]) * rn, __uint_as_float(x[j + 1]) * rn);
+                    const uint32_t nb = pack_bf16(__uint_as_float(x[j + HALF]) * rn, __uint_as_float(x[j + HALF + 1]) * rn);
+                    const __nv_bfloat162 av = __hmul2_rn(as_bf2(G0[e]), as_bf2(na));
+                    const __nv_bfloat162 bv = __hmul2_rn(as_bf2(G1[e]), as_bf2(nb));
+                    const __nv_bfloat162 co = as_bf2(C[e]), si = as_bf2(S[e]);
+                    o[4 * v + e] = as_u32(__hsub2(__hmul2_rn(av, co), __hmul2_rn(bv, si)));
+                    o[HALF / 2 + 4 * v + e] = as_u32(__hadd2(__hmul2_rn(bv, co), __hmul2_rn(av, si)));
+                }
+            }
+        }
+        if (staged) {
+            stg_acquire();
+#pragma unroll
+            for (int u = 0; u < DH / 8; ++u)
+                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            fence_proxy_async_smem();
+            named_barrier(1, 128);
+            if (threadIdx.x == EPI_LEADER) {
+                const int bt = m0 / q.T, t0 = m0 % q.T;
+                const CUtensorMap* map = kind == 0 ? tmQ : (kind == 1 ? tmK : tmV);
+                const int y = kind == 0 ? t0 : len0 + t0;
+                const int z = kind == 0 ? bt * q.Hq + hg : bt * q.Hkv + (kind == 1 ? hg - q.Hq : hg - q.Hq - q.Hkv);
+#pragma unroll
+                for (int c = 0; c < DH / 64; ++c) tma_store_3d(map, stg + c * 16384, c * 64, y, z);
+                bulk_commit();
+            }
+        } else if (row_ok) {
+            __nv_bfloat16* dst = kind == 0 ? q.q_out + (((size_t)b * q.Hq + hg) * q.T + t) * DH
+                               : kind == 1 ? q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + pos) * DH
+                                           : q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + pos) * DH;
+#pragma unroll
+            for (int u = 0; u < DH / 8; ++u)
+                reinterpret_cast<uint4*>(dst)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+    }
+    return true;
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
-                        const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmV, const GemmArgs args) {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, TMEM_COLS = C::TMEM_COLS;
     constexpr uint32_t IDESC = C::IDESC;
@@ -341,6 +370,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmB);
         if constexpr (EPI != EPI_QKV_ROPE) tma_prefetch_desc(&tmC);
         if constexpr (EPI == EPI_RESIDUAL) tma_prefetch_desc(&tmR);
+        if constexpr (EPI == EPI_QKV_ROPE) {
+            if (args.qkv.T % BM == 0) {
+                tma_prefetch_desc(&tmC);
+                tma_prefetch_desc(&tmR);
+                tma_prefetch_desc(&tmV);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -407,12 +443,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
             if constexpr (EPI == EPI_QKV_ROPE) {
-                // every lane waits, so the warp stays converged for the .sync.aligned TMEM loads
-                const bool w = mbar_wait(&acc_full[acc], aph, abort_flag);
-                if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                tc_fence_after();
-                if (args.qkv.dh == 128) epilogue_qkv_rope<128, BN>(args, tacc, tl.m0 + r, tl.n0, &acc_empty[acc]);
-                else epilogue_qkv_rope<64, BN>(args, tacc, tl.m0 + r, tl.n0, &acc_empty[acc]);
+                const bool w = args.qkv.dh == 128
+                                   ? epilogue_qkv_rope<128, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0,
+                                                                &acc_empty[acc], &acc_full[acc], aph, abort_flag)
+                                   : epilogue_qkv_rope<64, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0,
+                                                               &acc_empty[acc], &acc_full[acc], aph, abort_flag);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
             } else {
                 if (!epilogue_staged<EPI, BN>(args, &tmC, &tmR, stg, es, tacc, r, tl.m0, tl.n0, &acc_empty[acc],
                                               &acc_full[acc], aph, abort_flag)) {
@@ -422,9 +461,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // the last TMA stores must finish before the CTA exits
-        if constexpr (EPI != EPI_QKV_ROPE) {
-            if (threadIdx.x == EPI_LEADER) bulk_wait_all();
-        }
+        if (threadIdx.x == EPI_LEADER) bulk_wait_all();
     }
     if (!ok) {
         *abort_flag = 1;
@@ -458,7 +495,7 @@ cudaError_t launch_epi(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int grid = std::min(tiles, device_sm_count());
     return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(THREADS), Cfg<BN>::SMEM_BYTES, st, m.a, m.b, m.c,
-                      m.r, a);
+                      m.r, m.v, a);
 }
 
 }  // namespace
@@ -518,6 +555,19 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                          uint32_t box_inner, uint32_t box_outer) {
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes, box_inner, box_outer);
+}
+
+// [d2][d1][d0] bf16 tensor, boxes of 64 x 128 x 1 in the 128-byte swizzle.
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_tmap_out(CUtensorMap* map, const void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t ld) {

@@ -69,10 +69,13 @@ bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t 
 // Output / residual map for the staged epilogues: a [rows, cols] matrix with row stride ld elements,
 // boxes of 128 rows x 128 bytes (64 bf16 or 32 fp32 columns).
 bool encode_tmap_out(CUtensorMap* map, const void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t ld);
-// The four tensor maps of one GEMM launch: A, B, the output C (staged epilogues) and the residual R.
+// The tensor maps of one GEMM launch: A, B, the output C (staged epilogues) and the residual R. The
+// fused QKV epilogue uses c, r, v as the 3-D store maps of Q [B*Hq][T][dh] and the K / V caches
+// [B*Hkv][cap][dh] (boxes of 64 x 128 x 1, encode_tmap_bf16_3d).
 struct GemmMaps {
-    CUtensorMap a, b, c, r;
+    CUtensorMap a, b, c, r, v;
 };
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2);
 cudaError_t gemm_launch(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
 
 // ---------------------------------------------------------------- small kernels (kernels.cu)

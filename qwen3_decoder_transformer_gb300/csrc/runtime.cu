@@ -94,6 +94,7 @@ struct qwen3_ctx {
     CUtensorMap tA_xn, tA_attn, tA_h, tA_hn;
     CUtensorMap tC_x, tC_h;  // staged-epilogue outputs: residual stream (also the residual input), SwiGLU output
     std::vector<CUtensorMap> tB_qkv, tB_o, tB_gu, tB_down;
+    std::vector<CUtensorMap> tK3, tV3;  // per-layer cache maps [max_batch*Hkv][cap][dh] for the fused QKV stores
     CUtensorMap tB_head;
     // decode graphs
     std::vector<DecodeGraph> graphs;
@@ -167,6 +168,9 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
     const qwen3_config& g = c->cfg;
     const int M = B * T, d = g.hidden, dh = g.head_dim, F = g.intermediate;
     TRY(timed(c, K_EMBED, 1, st, [&] { return embed_launch(c->embed, g.vocab, d, ids, M, c->x, c->d_err, st); }));
+    // Q [B*Hq][T][dh] store map for the fused QKV epilogue (used when T is a multiple of 128)
+    CUtensorMap tq3;
+    if (!encode_tmap_bf16_3d(&tq3, c->q, dh, T, (uint64_t)B * g.n_q_heads)) return QWEN3_E_CUDA;
     for (int l = 0; l < g.n_layers; ++l) {
         if (l == c->tap_layer && c->tap_in)
             if (cudaMemcpyAsync(c->tap_in, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -182,6 +186,9 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             std::memset(&m, 0, sizeof(m));
             m.a = c->tA_xn;
             m.b = c->tB_qkv[l];
+            m.c = tq3;
+            m.r = c->tK3[l];
+            m.v = c->tV3[l];
             TRY(timed(c, K_GEMM_QKV, 1, st, [&] { return gemm_launch(m, a, st); }));
         }
         if (decode) {
@@ -381,6 +388,13 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN) &&
          encode_tmap_out(&c->tC_x, c->x, false, d, rows, d) && encode_tmap_out(&c->tC_h, c->h, false, F, arows, F);
+    c->tK3.resize(L);
+    c->tV3.resize(L);
+    for (int l = 0; ok && l < L; ++l)
+        ok = encode_tmap_bf16_3d(&c->tK3[l], c->kcache + (size_t)l * c->layer_elems, dh, capacity,
+                                 (uint64_t)max_batch * g->n_kv_heads) &&
+             encode_tmap_bf16_3d(&c->tV3[l], c->vcache + (size_t)l * c->layer_elems, dh, capacity,
+                                 (uint64_t)max_batch * g->n_kv_heads);
     c->tB_qkv.resize(L);
     c->tB_o.resize(L);
     c->tB_gu.resize(L);
