@@ -211,10 +211,15 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
 /* Causal GQA attention for prefill: for query row t of sequence b (position len0 + t) and query
  * head h, out = softmax(q k^T * dh^-0.5 over cache slots 0..len0+t of kv head h / (Hq/Hkv)) V.
  * q [B, Hq, T, dh]; caches [B, Hkv, cap, dh] with len0 + T <= cap; out [B*T, Hq*dh] bf16
- * (token-major, the o_proj input). d_err (may be NULL) receives bit 2 if a bounded wait gave up. */
+ * (token-major, the o_proj input). kv_split > 0 cuts each 128-row query tile's key range into at most
+ * kv_chunks chunks of at least kv_split 128-key tiles, computed by separate CTAs and merged by
+ * log-sum-exp in the last one to finish; d_work then holds qwen3_attention_prefill_workspace() bytes
+ * whose first 256 bytes are zero on the first call (each call leaves them zero). kv_split = 0: one CTA
+ * per query tile, d_work unused. d_err (may be NULL) receives bit 2 if a bounded wait gave up. */
+QWEN3_API size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int kv_chunks);
 QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
-                               int T, int Hq, int Hkv, int dh, int cap, const int* d_len0,
-                               void* d_out, int* d_err, void* stream);
+                               int T, int Hq, int Hkv, int dh, int cap, const int* d_len0, int kv_split,
+                               int kv_chunks, void* d_work, void* d_out, int* d_err, void* stream);
 
 /* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.

@@ -9,6 +9,7 @@
 // chunk of one (sequence, kv head) and serves all g query heads of that group from one read of
 // K and V (16-byte coalesced loads, 8 in flight per thread). Partial (max, sum, output) triples
 // go to a workspace; a second kernel merges the chunks by log-sum-exp.
+#include <algorithm>
 #include <cfloat>
 #include <mutex>
 
@@ -55,7 +56,8 @@ template <int DH, int NH>
 __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv,
-                           const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out, int* err) {
+                           const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out, int* err, int split,
+                           int max_chunks, float* __restrict__ ws, int* __restrict__ tickets) {
     using Ly = TcLayout<DH, NH>;
     constexpr int NCH = Ly::NCH;
     constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
@@ -74,9 +76,12 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     uint64_t* o_done = bars + 11;   // [NH]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+    volatile int* merge_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
+    const int n_qt = gridDim.x / max_chunks;
+    const int qt = n_qt - 1 - (int)(blockIdx.x / max_chunks);  // longest query tiles first
+    const int chunk = (int)(blockIdx.x % max_chunks);
     const int h0 = blockIdx.y * NH, b = blockIdx.z;
     const int jkv = h0 / (Hq / Hkv);
     const int q0 = qt * TC_BM;
@@ -114,17 +119,23 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     const int len0 = *len0p;
     const int n_valid = len0 + q_end;
     const int n_tiles = (n_valid + TC_BN - 1) / TC_BN;
+    // KV range of this CTA: the whole causal range, or one chunk of it (split > 0: chunks of at least
+    // `split` tiles, at most max_chunks of them, merged by the last CTA of the query tile to finish)
+    const int chunk_tiles = split > 0 ? max(split, (n_tiles + max_chunks - 1) / max_chunks) : n_tiles;
+    const int n_chunks = (n_tiles + chunk_tiles - 1) / chunk_tiles;
+    const int j0 = chunk * chunk_tiles;
+    const int nt = chunk < n_chunks ? min(n_tiles, j0 + chunk_tiles) - j0 : 0;  // tiles of this CTA
 
     if (warp == 0) {
-        if (lane == 0) {
+        if (lane == 0 && nt > 0) {
             mbar_expect_tx(q_full, NH * Ly::Q_BYTES);
             for (int hh = 0; hh < NH; ++hh)
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(smem + Ly::Q_OFF + hh * Ly::Q_BYTES + c * TC_BM * 128, &tmQ, q_full, c * 64, q0,
                                 b * Hq + h0 + hh);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            for (int i = 0; i < nt; ++i) {
+                const int s = i & 1, j = j0 + i;
+                if (!mbar_wait(&kv_empty[s], ((i >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmK, &k_full[s], c * 64,
@@ -135,11 +146,12 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                                 j * TC_BN, b * Hkv + jkv);
             }
         }
-    } else if (warp == 1) {
-        // all lanes walk the schedule (so the warp can zero V tails together); lane 0 issues
-        auto issue_s = [&](int hh, int j) -> bool {
-            const int s = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (j >> 1) & 1, abort_flag))) return false;
+    } else if (warp == 1 && nt > 0) {
+        // all lanes walk the schedule (so the warp can zero V tails together); lane 0 issues.
+        // i counts this CTA's tiles (barrier phases); j = j0 + i is the absolute KV tile.
+        auto issue_s = [&](int hh, int i) -> bool {
+            const int s = i & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (i >> 1) & 1, abort_flag))) return false;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t sq = smem_u32(smem + Ly::Q_OFF + hh * Ly::Q_BYTES);
@@ -157,9 +169,9 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
         };
         ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
         for (int hh = 0; ok && hh < NH; ++hh) ok = issue_s(hh, 0);
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const int s = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag))) { ok = false; break; }
+        for (int i = 0; ok && i < nt; ++i) {
+            const int s = i & 1, j = j0 + i;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (i >> 1) & 1, abort_flag))) { ok = false; break; }
             uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
             const int r0 = n_valid - j * TC_BN;  // first stale key row of this tile
             if (r0 < TC_BN) {
@@ -172,23 +184,23 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             }
             __syncwarp();
             for (int hh = 0; ok && hh < NH; ++hh) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[hh], j & 1, abort_flag))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[hh], i & 1, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t svv = smem_u32(sv);
 #pragma unroll
                     for (int kk = 0; kk < TC_BN / 16; ++kk) {
                         const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
-                        umma_bf16_ts(tmem + TM_O + hh * 128, tmem + hh * TC_BN + kk * 8, bd, IDESC_O, (j | kk) != 0);
+                        umma_bf16_ts(tmem + TM_O + hh * 128, tmem + hh * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
                     }
                     umma_commit(&o_done[hh]);
                     if (hh == NH - 1) umma_commit(&kv_empty[s]);
                 }
                 __syncwarp();
-                if (j + 1 < n_tiles) ok = issue_s(hh, j + 1);
+                if (i + 1 < nt) ok = issue_s(hh, i + 1);
             }
         }
-    } else {
+    } else if (warp >= 2 && nt > 0) {
         // softmax warps: head hh, thread <-> query row
         const int hh = (warp - 2) >> 2;
         const int quarter = warp & 3, row = quarter * 32 + lane;
@@ -205,8 +217,9 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             }
             return true;
         };
-        for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[hh], j & 1, abort_flag))) { ok = false; break; }
+        for (int i = 0; i < nt; ++i) {
+            const int j = j0 + i;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[hh], i & 1, abort_flag))) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[TC_BN];
 #pragma unroll
@@ -231,8 +244,8 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
             const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                const bool w = confirm_pv(j);  // O must hold P V of the previous tile before it is scaled
+            if (i > 0 && __any_sync(0xffffffffu, grow)) {
+                const bool w = confirm_pv(i);  // O must hold P V of the previous tile before it is scaled
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
@@ -250,8 +263,9 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 l *= alpha;
                 m_used = mx;
             }
-            // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region
-            const float nm = -m_used;
+            // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region (a row
+            // with no visible key yet keeps m = -inf and gets P = 0)
+            const float nm = m_used == -INFINITY ? 0.f : -m_used;
             float rs = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -269,20 +283,21 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             l += rs;
             // Observe the previous P V completion before releasing this P: o_done is then never more
             // than one phase ahead of this thread, so its parity waits stay unambiguous.
-            if (j > 0) {
-                const bool w = confirm_pv(j);
+            if (i > 0) {
+                const bool w = confirm_pv(i);
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_before();
             mbar_arrive(&p_full[hh]);
         }
-        // epilogue: O / l
-        if (ok) ok = confirm_pv(n_tiles);
+        // epilogue
+        if (ok) ok = confirm_pv(nt);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        __nv_bfloat16* orow = out + (((size_t)b * T + t) * Hq + h0 + hh) * DH;
+        if (ok && n_chunks == 1) {
+            // O / l straight to the output
             tc_fence_after();
             const float inv = 1.f / l;
-            __nv_bfloat16* orow = out + (((size_t)b * T + t) * Hq + h0 + hh) * DH;
 #pragma unroll 1
             for (int c = 0; c < DH / 32; ++c) {
                 uint32_t o[32];
@@ -298,6 +313,66 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                         reinterpret_cast<uint4*>(orow + c * 32)[v] =
                             make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
                 }
+            }
+        } else if (n_chunks > 1) {
+            // partial (unnormalised O, running max, sum) of this chunk; the last chunk to finish merges
+            constexpr int REC = DH + 4;  // floats per (head, row) record, 16-byte multiple
+            const int item = (b * (Hq / NH) + (int)blockIdx.y) * n_qt + qt;
+            float* rec0 = ws + ((size_t)item * max_chunks * NH + hh) * TC_BM * REC + (size_t)row * REC;
+            const size_t chunk_stride = (size_t)NH * TC_BM * REC;
+            if (ok) {
+                tc_fence_after();
+                float* rec = rec0 + chunk * chunk_stride;
+#pragma unroll 1
+                for (int c = 0; c < DH / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tm_o + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        reinterpret_cast<float4*>(rec + c * 32)[v] =
+                            make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                        __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                }
+                rec[DH] = m_used;
+                rec[DH + 1] = l;
+            }
+            __threadfence();
+            named_barrier(2, 128 * NH);
+            if (threadIdx.x == 64) *merge_flag = ok && atomicAdd(&tickets[item], 1) == n_chunks - 1;
+            named_barrier(2, 128 * NH);
+            if (*merge_flag) {
+                __threadfence();
+                float M = -INFINITY;
+                for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, rec0[c * chunk_stride + DH]);
+                float L = 0.f, acc[DH];
+#pragma unroll
+                for (int d = 0; d < DH; ++d) acc[d] = 0.f;
+                for (int c = 0; c < n_chunks; ++c) {
+                    const float* rc = rec0 + c * chunk_stride;
+                    const float mc = rc[DH];
+                    const float wgt = mc == -INFINITY ? 0.f : ex2_approx(mc - M);
+                    L = fmaf(rc[DH + 1], wgt, L);
+#pragma unroll
+                    for (int v = 0; v < DH / 4; ++v) {
+                        const float4 q4 = reinterpret_cast<const float4*>(rc)[v];
+                        acc[4 * v] = fmaf(q4.x, wgt, acc[4 * v]);
+                        acc[4 * v + 1] = fmaf(q4.y, wgt, acc[4 * v + 1]);
+                        acc[4 * v + 2] = fmaf(q4.z, wgt, acc[4 * v + 2]);
+                        acc[4 * v + 3] = fmaf(q4.w, wgt, acc[4 * v + 3]);
+                    }
+                }
+                const float inv = 1.f / L;
+                if (t < T) {
+#pragma unroll
+                    for (int v = 0; v < DH / 8; ++v)
+                        reinterpret_cast<uint4*>(orow)[v] =
+                            make_uint4(pack_bf16(acc[8 * v] * inv, acc[8 * v + 1] * inv),
+                                       pack_bf16(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
+                                       pack_bf16(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
+                                       pack_bf16(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+                }
+                if (threadIdx.x == 64) tickets[item] = 0;  // ready for the next launch
             }
         }
     }
@@ -520,38 +595,81 @@ cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, co
     return cudaErrorInvalidValue;
 }
 
+int attn_heads_per_cta(int Hq, int Hkv) { return (Hq / Hkv) % 2 == 0 ? 2 : 1; }
+// Ticket counters (one int per work item), padded to 256 bytes, at the start of the workspace.
+size_t attn_tickets_floats(int B, int T, int Hq, int Hkv) {
+    const size_t items = (size_t)((T + TC_BM - 1) / TC_BM) * (Hq / attn_heads_per_cta(Hq, Hkv)) * B;
+    return (items + 63) / 64 * 64;
+}
+
 template <int DH, int NH>
 cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int B, int T, int Hq,
-                              int Hkv, const int* len0, __nv_bfloat16* out, int* err, cudaStream_t st) {
+                              int Hkv, const int* len0, __nv_bfloat16* out, int* err, int split, int max_chunks,
+                              float* ws, cudaStream_t st) {
     using Ly = TcLayout<DH, NH>;
-    dim3 grid((T + TC_BM - 1) / TC_BM, Hq / NH, B);
+    const int n_qt = (T + TC_BM - 1) / TC_BM;
+    dim3 grid(n_qt * max_chunks, Hq / NH, B);
+    int* tickets = reinterpret_cast<int*>(ws);
+    float* parts = ws ? ws + attn_tickets_floats(B, T, Hq, Hkv) : nullptr;
     return launch_pdl(attn_prefill_tc_kernel<DH, NH>, grid, dim3(Ly::THREADS), Ly::SMEM, st, tq, tk, tv, T, Hq, Hkv, len0,
-                      out, err);
+                      out, err, split, max_chunks, parts, tickets);
 }
 
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                              int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, int* err,
-                              cudaStream_t st) {
+                              int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, int* err, int split,
+                              int max_chunks, float* ws, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
         return cudaErrorInvalidValue;
+    if (split <= 0 || !ws) {
+        split = 0;
+        max_chunks = 1;
+    }
     // Two heads per CTA share each K/V tile (measured faster than one head per CTA even when the
     // grid is smaller than the SM count).
-    if ((Hq / Hkv) % 2 == 0) return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
-    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, st);
+    if ((Hq / Hkv) % 2 == 0)
+        return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, split, max_chunks, ws, st);
+    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, split, max_chunks, ws, st);
 }
 
 }  // namespace
 
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
-                                cudaStream_t st) {
+                                int split, int max_chunks, float* ws, cudaStream_t st) {
     if (B <= 0 || T <= 0) return cudaSuccess;
-    if (dh == 128) return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, st);
-    if (dh == 64) return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, st);
+    if (dh == 128)
+        return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, split, max_chunks, ws, st);
+    if (dh == 64) return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, split, max_chunks, ws, st);
     return cudaErrorInvalidValue;
+}
+
+size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks) {
+    if (max_chunks <= 1) return 0;
+    const int nh = attn_heads_per_cta(Hq, Hkv);
+    const size_t items = (size_t)((T + TC_BM - 1) / TC_BM) * (Hq / nh) * B;
+    return (attn_tickets_floats(B, T, Hq, Hkv) + items * max_chunks * nh * TC_BM * (dh + 4)) * sizeof(float);
+}
+
+void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks) {
+    // Split the KV range only when the query tiles would occupy at most a quarter of the SMs over a
+    // long key range (a short prefill chunk after a long context): then one CTA per query tile leaves
+    // most SMs idle. On larger grids the per-CTA prologue and the merge cost more than the shorter
+    // critical path saves (measured at 16 query tiles x 8 head pairs).
+    const int nh = attn_heads_per_cta(Hq, Hkv);
+    const long long items = (long long)((T + TC_BM - 1) / TC_BM) * (Hq / nh) * B;
+    const int max_tiles = (kv_len + TC_BN - 1) / TC_BN;
+    const int sms = device_sm_count();
+    if (items * 4 <= sms && max_tiles >= 8) {
+        const int want = (int)std::min<long long>(16, std::min<long long>(sms / items, max_tiles / 4));
+        *split = (max_tiles + want - 1) / want;
+        *max_chunks = (max_tiles + *split - 1) / *split;
+    } else {
+        *split = 0;
+        *max_chunks = 1;
+    }
 }
 
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap) {

@@ -95,9 +95,14 @@ cudaError_t set_len_launch(int* len, int value, cudaStream_t st);
 cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention (attention.cu)
+// split > 0: cut each query tile's KV range into at most max_chunks chunks of >= split tiles, merged by
+// the last CTA to finish; ws then holds attn_prefill_workspace() bytes whose leading ticket counters
+// are zero on entry (each launch leaves them zero).
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
-                                cudaStream_t st);
+                                int split, int max_chunks, float* ws, cudaStream_t st);
+size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
+void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap);
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,

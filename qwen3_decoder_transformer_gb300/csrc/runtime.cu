@@ -82,6 +82,8 @@ struct qwen3_ctx {
     bf16 *wqkv = nullptr, *wgu = nullptr, *kcache = nullptr, *vcache = nullptr, *rope = nullptr;
     bf16 *x = nullptr, *xn = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
     float* dec_work = nullptr;
+    float* attn_ws = nullptr;  // split prefill attention: tickets + partials (zeroed at init)
+    size_t attn_ws_bytes = 0;
     int* d_len = nullptr;
     int* d_err = nullptr;
     int32_t* d_ids_buf = nullptr;
@@ -197,9 +199,15 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
                                           c->capacity, c->d_len, c->dec_work, c->attn, st);
             }));
         } else {
+            int split = 0, chunks = 1;
+            attn_prefill_split_plan(B, T, g.n_q_heads, g.n_kv_heads, c->len + T, &split, &chunks);
+            if (attn_prefill_workspace(B, T, g.n_q_heads, g.n_kv_heads, dh, chunks) > c->attn_ws_bytes) {
+                split = 0;
+                chunks = 1;
+            }
             TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
                 return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
-                                           c->capacity, c->d_len, c->attn, c->d_err, st);
+                                           c->capacity, c->d_len, c->attn, c->d_err, split, chunks, c->attn_ws, st);
             }));
         }
         TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
@@ -252,8 +260,9 @@ void release(qwen3_ctx* c) {
     }
     for (auto e : c->free_events) cudaEventDestroy(e);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
-    void* bufs[] = {c->wqkv, c->wgu, c->kcache,  c->vcache, c->rope,  c->x,         c->xn,          c->q,
-                    c->attn, c->h,   c->hn,      c->dec_work, c->d_len, c->d_err, c->d_ids_buf, c->d_logits_buf};
+    void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
+                    c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->d_len,
+                    c->d_err, c->d_ids_buf, c->d_logits_buf};
     for (void* p : bufs)
         if (p) cudaFree(p);
     delete c;
@@ -355,6 +364,14 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
                   cudaSuccess &&
               dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
               dmalloc(&c->d_ids_buf, rows) == cudaSuccess;
+    // split-attention workspace: sized for the largest split the planner can choose (work items up to
+    // the SM count, up to 4 chunks each)
+    if (ok) {
+        const int nh = (g->n_q_heads / g->n_kv_heads) % 2 == 0 ? 2 : 1;
+        c->attn_ws_bytes = ((size_t)device_sm_count() / 4 + 1) * 16 * nh * 128 * (dh + 4) * sizeof(float) + 4096;
+        ok = dmalloc(&c->attn_ws, c->attn_ws_bytes / sizeof(float)) == cudaSuccess &&
+             cudaMemsetAsync(c->attn_ws, 0, c->attn_ws_bytes, st) == cudaSuccess;
+    }
     if (!ok) {
         cudaGetLastError();
         release(c);
@@ -647,14 +664,21 @@ int qwen3_op_qknorm_rope_append(const void* qkv, int B, int T, int Hq, int Hkv, 
                : QWEN3_E_CUDA;
 }
 
+size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int kv_chunks) {
+    if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv) return 0;
+    return attn_prefill_workspace(B, T, Hq, Hkv, dh, kv_chunks);
+}
+
 int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, int B, int T, int Hq, int Hkv, int dh,
-                               int cap, const int* len0, void* out, int* err, void* stream) {
+                               int cap, const int* len0, int kv_split, int kv_chunks, void* work, void* out, int* err,
+                               void* stream) {
     if (!q || !kc || !vc || !len0 || !out || B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
-        (dh != 64 && dh != 128) || cap < 1)
+        (dh != 64 && dh != 128) || cap < 1 || kv_split < 0 || kv_chunks > 64 || (kv_split > 0 && !work))
         return QWEN3_E_ARG;
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
-                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out), err,
+                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out), err, kv_split,
+                               kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work),
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

@@ -104,3 +104,26 @@ def test_tiny_errors(bd, tiny):
         bd.Model(dict(cfg, max_positions=8), w, max_batch=1, capacity=16)
     assert e.value.code == 2  # capacity above max_positions
     m.close()
+
+
+def test_tiny_chunked_prefill_long_context(bd, tiny):
+    """A short prefill chunk after a long context: the attention splits each query tile's key range
+    over several CTAs (the runtime's split plan) and merges them; logits and the new cache rows must
+    match the oracle running the same two calls."""
+    cfg, w, om = tiny
+    V = cfg["vocab"]
+    T0, T1, cap = 1024, 64, 1100
+    ids = synth.make_ids(V, 1, T0 + T1, 11)
+    m = bd.Model(cfg, w, max_batch=1, capacity=cap, max_tokens=T0)
+    logits = torch.empty(1, V, dtype=torch.float32, device="cuda")
+    m.prefill(ids[:, :T0].cuda().contiguous(), logits)
+    m.prefill(ids[:, T0:].cuda().contiguous(), logits)
+    assert m.get_error() == 0
+    kc, vc = om.new_cache(1, cap)
+    om.forward(kc, vc, ids[:, :T0].numpy(), 0)
+    ref = om.forward(kc, vc, ids[:, T0:].numpy(), T0)
+    got = logits.cpu().numpy()
+    assert rel_l2(got, ref) <= 2e-2
+    k, v = m.kv_view(cfg["n_layers"] - 1)
+    assert rel_l2(widen(bits(k[0, :, T0:T0 + T1])), widen(kc[-1, 0, :, T0:T0 + T1])) <= 1e-2
+    m.close()

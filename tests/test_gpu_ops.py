@@ -220,6 +220,17 @@ def _attn_ref(q, kc, vc, len0, T):
                                                   (1, 1, 4, 4, 128, 300), (1, 700, 8, 2, 128, 0),
                                                   (1, 384, 4, 1, 64, 129), (3, 257, 8, 8, 128, 511)])
 def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
+    _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 0, 1)
+
+
+@pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0,split,chunks", [(1, 700, 8, 2, 128, 0, 1, 4), (1, 1024, 16, 8, 128, 0, 2, 4),
+                                                               (2, 257, 8, 8, 128, 511, 1, 3), (1, 384, 4, 1, 64, 129, 1, 2),
+                                                               (1, 300, 8, 4, 64, 70, 1, 8)])
+def test_attention_prefill_split_kv(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks):
+    _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks)
+
+
+def _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks):
     rng = np.random.default_rng(T * 31 + len0)
     cap = len0 + T + 5
     q = rand_bf16(rng, (Bq, Hq, T, dh))
@@ -230,9 +241,17 @@ def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
     out = torch.empty(Bq * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
     len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
     err = _err()
-    bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err)
+    work = None
+    if split:
+        work = torch.zeros(max(1, bd.attention_prefill_workspace(Bq, T, Hq, Hkv, dh, chunks) // 4),
+                           dtype=torch.float32, device="cuda")
+    for _ in range(2 if split else 1):  # twice: the merge tickets must be left at zero
+        bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err, kv_split=split, kv_chunks=chunks,
+                                work=work)
     torch.cuda.synchronize()
     assert err.item() == 0
+    if split:
+        assert not work[:64].view(torch.int32).any()
     ref = _attn_ref(q, kc, vc, len0, T)
     got = widen(bits(out))
     assert np.isfinite(got).all()
