@@ -189,6 +189,15 @@ QWEN3_API int qwen3_op_rmsnorm(const void* d_x, const void* d_gamma, int rows, i
 QWEN3_API int qwen3_op_gemm(const void* d_A, const void* d_B, int M, int N, int K, int epilogue, void* d_C,
                   int ldc, const void* d_R, int ldr, int* d_err, void* stream);
 
+/* Weight-streaming GEMM for a few rows (decode batches, 1 <= M <= 64): acc[b][n] = sum_k A[b][k] B[n][k]
+ * in fp32 on the tensor cores, with the weights B [N, K] as the 128-row MMA operand and the K range
+ * split over `splits` CTAs per 128 weight rows (qwen3_gemm_skinny_splits gives the runtime's choice).
+ * splits == 1: d_out [M, N] fp32 receives acc. splits > 1: d_slices receives split s's partial sums
+ * at [s][M][N] fp32 (splits * M * N floats); their sum is acc. K % 8 == 0. */
+QWEN3_API int qwen3_gemm_skinny_splits(int N, int K);
+QWEN3_API int qwen3_op_gemm_skinny(const void* d_A, const void* d_B, int M, int N, int K, int splits, float* d_slices,
+                                   float* d_out, int* d_err, void* stream);
+
 /* Pack gate [F, d] and up [F, d] into the [2F, d] layout QWEN3_EPI_SWIGLU expects: blocks of 128
  * gate rows followed by the matching 128 up rows. F % 128 == 0. */
 QWEN3_API int qwen3_op_pack_gate_up(const void* d_gate, const void* d_up, int F, int d, void* d_out, void* stream);

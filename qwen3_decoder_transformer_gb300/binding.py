@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
     L.qwen3_op_rmsnorm.argtypes = [_vp, _vp, i, i, i, i, ctypes.c_float, _vp, _vp]
     L.qwen3_op_gemm.argtypes = [_vp, _vp, i, i, i, i, _vp, i, _vp, i, _vp, _vp]
     L.qwen3_op_pack_gate_up.argtypes = [_vp, _vp, i, i, _vp, _vp]
+    L.qwen3_gemm_skinny_splits.argtypes = [i, i]
+    L.qwen3_op_gemm_skinny.argtypes = [_vp, _vp, i, i, i, i, _vp, _vp, _vp, _vp]
     L.qwen3_op_rope_table.argtypes = [ctypes.c_float, i, i, _vp, _vp]
     L.qwen3_op_qknorm_rope_append.argtypes = [_vp, i, i, i, i, i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                               _vp, i, _vp]
@@ -236,6 +238,16 @@ def op_gemm(A, B, epi, C, R=None, err=None, stream=None):
     N = B.shape[0]
     check(lib().qwen3_op_gemm(_p(A), _p(B), M, N, K, epi, _p(C), C.shape[1], _p(R),
                               R.shape[1] if R is not None else 0, _p(err), _stream(stream)))
+
+
+def gemm_skinny_splits(N, K) -> int:
+    return lib().qwen3_gemm_skinny_splits(N, K)
+
+
+def op_gemm_skinny(A, B, splits, slices=None, out=None, err=None, stream=None):
+    M, K = A.shape
+    N = B.shape[0]
+    check(lib().qwen3_op_gemm_skinny(_p(A), _p(B), M, N, K, splits, _p(slices), _p(out), _p(err), _stream(stream)))
 
 
 def op_pack_gate_up(gate, up, out, stream=None):

@@ -476,6 +476,131 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+
+// ------------------------------------------------------------------------------ skinny (decode)
+// Weight-streaming GEMM for decode batches. One CTA = 128 weight rows x one K chunk: warp 0 streams
+// 128x64 weight boxes and 64x64 activation boxes through an 8-stage ring, warp 1 issues
+// tcgen05.mma M=128 (weight rows) x N=MP (activation rows) x K=16 into MP TMEM columns, warps 2-5
+// read the accumulator (thread = weight row) and store it into this split's fp32 slice of the
+// workspace, or straight to the output when the K range is not split. With few rows the kernel is
+// bound by reading the weights once.
+constexpr int SK_STAGES = 8;
+constexpr int SK_W_BYTES = 128 * BK * 2;
+constexpr int SK_X_BYTES = kSkinnyRowsBox * BK * 2;
+constexpr int SK_STAGE_BYTES = SK_W_BYTES + SK_X_BYTES;
+constexpr int SK_SMEM = SK_STAGES * SK_STAGE_BYTES + 256 + 1024;
+
+template <int MP>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const SkinnyArgs args) {
+    constexpr uint32_t IDESC = idesc_bf16(128, MP);
+    constexpr uint32_t TCOLS = MP < 32 ? 32 : MP;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SK_STAGES * SK_STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + SK_STAGES;
+    uint64_t* acc_full = empty_bar + SK_STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * 128;
+    const int k_blocks = (args.K + BK - 1) / BK;
+    const int per = (k_blocks + args.splits - 1) / args.splits;
+    const int kb0 = blockIdx.y * per, kb1 = min(k_blocks, kb0 + per);
+    const int nkb = max(0, kb1 - kb0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SK_STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % SK_STAGES;
+            if (!mbar_wait(&empty_bar[s], ((i / SK_STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* st = smem + s * SK_STAGE_BYTES;
+            mbar_expect_tx(&full_bar[s], SK_STAGE_BYTES);
+            tma_load_2d(st, &tmW, &full_bar[s], (kb0 + i) * BK, n0);
+            tma_load_2d(st + SK_W_BYTES, &tmX, &full_bar[s], (kb0 + i) * BK, 0);
+        }
+    } else if (warp == 1 && lane == 0) {
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % SK_STAGES;
+            if (!mbar_wait(&full_bar[s], (i / SK_STAGES) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + s * SK_STAGE_BYTES);
+            const uint64_t wdesc = sdesc_kmajor_sw128(sa), xdesc = sdesc_kmajor_sw128(sa + SK_W_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) umma_bf16_ss(tmem, wdesc + 2 * k, xdesc + 2 * k, IDESC, (i | k) != 0);
+            umma_commit(&empty_bar[s]);
+        }
+        if (ok) umma_commit(acc_full);
+    } else if (warp >= 2) {
+        const int quarter = warp & 3;
+        const int n = n0 + quarter * 32 + lane;  // this thread's weight row = TMEM lane
+        const bool w = nkb == 0 || mbar_wait(acc_full, 0, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+        } else if (nkb > 0) {
+            tc_fence_after();
+            uint32_t v[MP];
+            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16);
+            if constexpr (MP == 16) {
+                tmem_ld_32x32b_x16(ta, v);
+            } else {
+#pragma unroll
+                for (int c = 0; c < MP / 32; ++c)
+                    tmem_ld_32x32b_x32(ta + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+            }
+            tmem_ld_wait();
+            if (n < args.N) {
+                if (args.splits == 1 && args.out) {
+#pragma unroll
+                    for (int b = 0; b < MP; ++b)
+                        if (b < args.M) args.out[(size_t)b * args.ldo + n] = __uint_as_float(v[b]);
+                } else {
+                    float* slice = args.ws + (size_t)blockIdx.y * args.M * args.ldw;
+#pragma unroll
+                    for (int b = 0; b < MP; ++b)
+                        if (b < args.M) slice[(size_t)b * args.ldw + n] = __uint_as_float(v[b]);
+                }
+            }
+        }
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        if (args.err) atomicOr(args.err, ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -526,6 +651,12 @@ cudaError_t gemm_prepare() {
     }
     for (const void* f : f128) {
         cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::SMEM_BYTES);
+        if (r != cudaSuccess) e = r;
+    }
+    const void* fsk[] = {(const void*)gemm_skinny_kernel<16>, (const void*)gemm_skinny_kernel<32>,
+                         (const void*)gemm_skinny_kernel<64>};
+    for (const void* f : fsk) {
+        cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM);
         if (r != cudaSuccess) e = r;
     }
     return e;
@@ -598,6 +729,29 @@ cudaError_t gemm_launch(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
         case EPI_QKV_ROPE: return narrow ? launch_epi<EPI_QKV_ROPE, 128>(m, a, st) : launch_epi<EPI_QKV_ROPE, 256>(m, a, st);
     }
     return cudaErrorInvalidValue;
+}
+
+bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_t K) {
+    return encode_tmap_bf16_2d(map, X, K, rows, K * 2, BK, kSkinnyRowsBox);
+}
+
+int skinny_splits(int N, int K) {
+    // enough CTAs for about two per SM, each with at least two 64-wide K blocks, at most 16 slices
+    const int tiles = (N + 127) / 128, k_blocks = (K + BK - 1) / BK;
+    int s = (2 * device_sm_count() + tiles - 1) / tiles;
+    s = std::min(std::min(s, 16), std::max(1, k_blocks / 2));
+    // no empty splits: every split must own at least one K block
+    const int per = (k_blocks + s - 1) / s;
+    return std::max(1, (k_blocks + per - 1) / per);
+}
+
+cudaError_t gemm_skinny_launch(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, cudaStream_t st) {
+    if (a.M <= 0 || a.N <= 0) return cudaSuccess;
+    if (a.M > kSkinnyRowsBox) return cudaErrorInvalidValue;
+    const dim3 grid((a.N + 127) / 128, a.splits);
+    if (a.M <= 16) return launch_pdl(gemm_skinny_kernel<16>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);
+    if (a.M <= 32) return launch_pdl(gemm_skinny_kernel<32>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);
+    return launch_pdl(gemm_skinny_kernel<64>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);
 }
 
 }  // namespace q3

@@ -78,6 +78,25 @@ struct GemmMaps {
 bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2);
 cudaError_t gemm_launch(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
 
+// ---------------------------------------------------------------- skinny GEMM (gemm.cu)
+// For a handful of activation rows (decode, M <= 64): acc[b][n] = sum_k X[b][k] W[n][k] with the
+// weights as the 128-row MMA operand and the rows as the N side (padded to 16/32/64), the K range
+// split over `splits` CTAs per 128 weight rows. splits == 1 with out != nullptr stores fp32 rows
+// directly (out[b * ldo + n]); otherwise split s stores its partial sums in its own slice,
+// ws[(s * M + b) * ldw + n], and a finalize kernel adds the slices in a fixed order (deterministic).
+struct SkinnyArgs {
+    int M, N, K, splits;
+    float* ws;
+    long long ldw;
+    float* out;
+    long long ldo;
+    int* err;
+};
+constexpr int kSkinnyRowsBox = 64;  // TMA box rows of the activation operand
+bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_t K);
+int skinny_splits(int N, int K);
+cudaError_t gemm_skinny_launch(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, cudaStream_t st);
+
 // ---------------------------------------------------------------- small kernels (kernels.cu)
 cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* ids, int M, __nv_bfloat16* out, int* err,
                          cudaStream_t st);
@@ -90,6 +109,17 @@ cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, in
                                       const __nv_bfloat16* qg, const __nv_bfloat16* kg, const __nv_bfloat16* table,
                                       const int* len0, float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc,
                                       __nv_bfloat16* vc, int cap, cudaStream_t st);
+// Decode finalize kernels: sum the `splits` fp32 slices of the skinny GEMM ([splits][M][ldw]) in order,
+// then apply the epilogue.
+cudaError_t finalize_residual_rmsnorm_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* x,
+                                             const __nv_bfloat16* g, int M, int n, float eps, __nv_bfloat16* y,
+                                             cudaStream_t st);
+cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* h, int M, int F,
+                                   cudaStream_t st);
+cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, int Hq, int Hkv, int dh, const __nv_bfloat16* qg,
+                                          const __nv_bfloat16* kg, const __nv_bfloat16* table, const int* len0,
+                                          float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap,
+                                          cudaStream_t st);
 // Length bookkeeping on the device: *len = value, or *len += delta.
 cudaError_t set_len_launch(int* len, int value, cudaStream_t st);
 cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);

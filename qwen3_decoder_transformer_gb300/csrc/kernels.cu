@@ -113,12 +113,14 @@ __global__ void rope_table_kernel(double theta, int dh, int n_pos, __nv_bfloat16
 // rotate-half pairing). One warp per (token, head) vector of DH values; lane l holds features
 // [l*E, l*E+E), so feature i < DH/2 and its rotation partner i + DH/2 sit in lanes l and l^16.
 // The rotation is evaluated as bf16(bf16(a*c) + bf16(-b*s)) and bf16(bf16(b*c) + bf16(a*s)).
-template <int DH>
-__global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int B, int T, int Hq, int Hkv,
-                                          const __nv_bfloat16* __restrict__ qg, const __nv_bfloat16* __restrict__ kg,
-                                          const __nv_bfloat16* __restrict__ table, const int* __restrict__ len0p,
-                                          float eps, __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ kc,
-                                          __nv_bfloat16* __restrict__ vc, int cap) {
+// F32_SRC: the projection is the sum of the fp32 split-K slices ([splits][B][H*DH], added in order)
+// instead of a bf16 qkv buffer; it is rounded to bf16 as the unsplit GEMM stores it.
+template <int DH, bool F32_SRC>
+__global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ ws, int splits, int B, int T,
+                                          int Hq, int Hkv, const __nv_bfloat16* __restrict__ qg,
+                                          const __nv_bfloat16* __restrict__ kg, const __nv_bfloat16* __restrict__ table,
+                                          const int* __restrict__ len0p, float eps, __nv_bfloat16* __restrict__ q_out,
+                                          __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, int cap) {
     pdl_wait();
     pdl_trigger();
     constexpr int E = DH / 32;  // 2 or 4 features per lane
@@ -131,15 +133,29 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
     const long long m = w / H;
     const int b = (int)(m / T), t = (int)(m % T);
     const int pos = *len0p + t;
-    const __nv_bfloat16* src = qkv + (size_t)m * H * DH + (size_t)hh * DH + lane * E;
 
     uint32_t raw[E / 2];
-    if constexpr (E == 4) {
-        uint2 v = *reinterpret_cast<const uint2*>(src);
-        raw[0] = v.x;
-        raw[1] = v.y;
+    if constexpr (F32_SRC) {
+        const size_t slice = (size_t)B * H * DH;
+        const float* src = ws + (size_t)m * H * DH + (size_t)hh * DH + lane * E;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
+        for (int sp = 0; sp < splits; ++sp)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] += src[sp * slice + e];
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) raw[e] = pack_bf16(acc[2 * e], acc[2 * e + 1]);
     } else {
-        raw[0] = *reinterpret_cast<const uint32_t*>(src);
+        const __nv_bfloat16* src = qkv + (size_t)m * H * DH + (size_t)hh * DH + lane * E;
+        if constexpr (E == 4) {
+            uint2 v = *reinterpret_cast<const uint2*>(src);
+            raw[0] = v.x;
+            raw[1] = v.y;
+        } else {
+            raw[0] = *reinterpret_cast<const uint32_t*>(src);
+        }
     }
     if (hh >= Hq + Hkv) {  // V: copied into the cache unchanged
         __nv_bfloat16* dst = vc + (((size_t)b * Hkv + (hh - Hq - Hkv)) * cap + pos) * DH + lane * E;
@@ -185,6 +201,95 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
     else dst = kc + (((size_t)b * Hkv + (hh - Hq)) * cap + pos) * DH + lane * E;
     if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
     else *reinterpret_cast<uint32_t*>(dst) = o[0];
+}
+
+
+// x = bf16(x + bf16(acc)) for the decode rows (acc = the sum of the split-K slices, added in order),
+// then y = RMSNorm(x) with gain g: the residual add of o_proj / down_proj fused with the RMSNorm that
+// follows it (post-attention norm, the next layer's input norm, or the final norm). One 256-thread
+// CTA per row; each thread owns 8-element groups of the row and issues all its slice loads at once.
+constexpr int FIN_THREADS = 256;
+__global__ void __launch_bounds__(FIN_THREADS)
+    finalize_residual_rmsnorm_kernel(const float* __restrict__ ws, int splits, long long ldw,
+                                     __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int M, int n,
+                                     float eps, __nv_bfloat16* __restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[FIN_THREADS / 32];
+    const int row = blockIdx.x;
+    constexpr int MAXG = 2;  // 8-element groups per thread: rows up to 256 * 8 * 2 = 4096 elements
+    uint4 keep[MAXG];
+    float ss = 0.f;
+    uint4* xr = reinterpret_cast<uint4*>(x + (size_t)row * n);
+    const size_t slice = (size_t)M * ldw;
+#pragma unroll
+    for (int i = 0; i < MAXG; ++i) {
+        const int v = threadIdx.x + FIN_THREADS * i;
+        if (v < n / 8) {
+            const uint4 xv = xr[v];
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float4* wr = reinterpret_cast<const float4*>(ws + (size_t)row * ldw) + 2 * v;
+#pragma unroll 4
+            for (int sp = 0; sp < splits; ++sp) {
+                const float4 a0 = wr[sp * (slice / 4)], a1 = wr[sp * (slice / 4) + 1];
+                acc[0] += a0.x, acc[1] += a0.y, acc[2] += a0.z, acc[3] += a0.w;
+                acc[4] += a1.x, acc[5] += a1.y, acc[6] += a1.z, acc[7] += a1.w;
+            }
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float lo = bf16_lo(xw[e]) + rbf(acc[2 * e]), hi = bf16_hi(xw[e]) + rbf(acc[2 * e + 1]);
+                o[e] = pack_bf16(lo, hi);
+                const float rl = bf16_lo(o[e]), rh = bf16_hi(o[e]);
+                ss = fmaf(rl, rl, ss);
+                ss = fmaf(rh, rh, ss);
+            }
+            keep[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            xr[v] = keep[i];
+        }
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < FIN_THREADS / 32; ++w) tot += red[w];
+    const float r = __frsqrt_rn(tot / (float)n + eps);
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * n);
+#pragma unroll
+    for (int i = 0; i < MAXG; ++i) {
+        const int v = threadIdx.x + FIN_THREADS * i;
+        if (v < n / 8) yr[v] = norm8(keep[i], __ldg(gr + v), r);
+    }
+}
+
+// h = bf16(bf16(silu(bf16(gate))) * bf16(up)) from the split-K slices of the packed gate/up GEMM
+// (128-column blocks: gate block j at columns 256j.., up block at 256j+128..).
+__global__ void finalize_swiglu_kernel(const float* __restrict__ ws, int splits, long long ldw,
+                                       __nv_bfloat16* __restrict__ h, int M, int F) {
+    pdl_wait();
+    pdl_trigger();
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // one thread per 4 outputs
+    if (idx >= (long long)M * F / 4) return;
+    const int row = (int)(idx / (F / 4)), j = (int)(idx % (F / 4)) * 4;
+    const size_t slice = (size_t)M * ldw, off = (size_t)row * ldw + (j / 128) * 256 + (j % 128);
+    float gg[4] = {0.f, 0.f, 0.f, 0.f}, uu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int sp = 0; sp < splits; ++sp) {
+        const float4 gv = *reinterpret_cast<const float4*>(ws + sp * slice + off);
+        const float4 uv = *reinterpret_cast<const float4*>(ws + sp * slice + off + 128);
+        gg[0] += gv.x, gg[1] += gv.y, gg[2] += gv.z, gg[3] += gv.w;
+        uu[0] += uv.x, uu[1] += uv.y, uu[2] += uv.z, uu[3] += uv.w;
+    }
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float g0 = rbf(gg[e]);
+        o[e] = rbf(__fdividef(g0, 1.0f + __expf(-g0))) * rbf(uu[e]);
+    }
+    *reinterpret_cast<uint2*>(h + (size_t)row * F + j) = make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]));
 }
 
 __global__ void set_len_kernel(int* len, int value) {
@@ -245,12 +350,13 @@ cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, in
     if (warps <= 0) return cudaSuccess;
     const int threads = 256, wpb = threads / 32;
     const unsigned blocks = (unsigned)((warps + wpb - 1) / wpb);
+    const float* nows = nullptr;
     if (dh == 128)
-        return launch_pdl(qknorm_rope_append_kernel<128>, dim3(blocks), dim3(threads), 0, st, qkv, B, T, Hq, Hkv, qg, kg,
-                          table, len0, eps, q_out, kc, vc, cap);
+        return launch_pdl(qknorm_rope_append_kernel<128, false>, dim3(blocks), dim3(threads), 0, st, qkv, nows, 1, B, T, Hq,
+                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
     if (dh == 64)
-        return launch_pdl(qknorm_rope_append_kernel<64>, dim3(blocks), dim3(threads), 0, st, qkv, B, T, Hq, Hkv, qg, kg,
-                          table, len0, eps, q_out, kc, vc, cap);
+        return launch_pdl(qknorm_rope_append_kernel<64, false>, dim3(blocks), dim3(threads), 0, st, qkv, nows, 1, B, T, Hq,
+                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
     return cudaErrorInvalidValue;
 }
 
@@ -260,6 +366,41 @@ cudaError_t set_len_launch(int* len, int value, cudaStream_t st) {
 
 cudaError_t add_len_launch(int* len, int delta, cudaStream_t st) {
     return launch_pdl(add_len_kernel, dim3(1), dim3(1), 0, st, len, delta);
+}
+
+cudaError_t finalize_residual_rmsnorm_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* x,
+                                             const __nv_bfloat16* g, int M, int n, float eps, __nv_bfloat16* y,
+                                             cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    if (n % 8 || n > 4096 || ldw % 4) return cudaErrorInvalidValue;
+    return launch_pdl(finalize_residual_rmsnorm_kernel, dim3(M), dim3(FIN_THREADS), 0, st, ws, splits, ldw, x, g, M, n,
+                      eps, y);
+}
+
+cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* h, int M, int F,
+                                   cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    const long long n = (long long)M * F / 4;
+    return launch_pdl(finalize_swiglu_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, ws, splits, ldw, h, M,
+                      F);
+}
+
+cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, int Hq, int Hkv, int dh,
+                                          const __nv_bfloat16* qg, const __nv_bfloat16* kg, const __nv_bfloat16* table,
+                                          const int* len0, float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc,
+                                          __nv_bfloat16* vc, int cap, cudaStream_t st) {
+    const long long warps = (long long)B * (Hq + 2 * Hkv);
+    if (warps <= 0) return cudaSuccess;
+    const int threads = 256, wpb = threads / 32;
+    const unsigned blocks = (unsigned)((warps + wpb - 1) / wpb);
+    const __nv_bfloat16* noq = nullptr;
+    if (dh == 128)
+        return launch_pdl(qknorm_rope_append_kernel<128, true>, dim3(blocks), dim3(threads), 0, st, noq, ws, splits, B, 1,
+                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+    if (dh == 64)
+        return launch_pdl(qknorm_rope_append_kernel<64, true>, dim3(blocks), dim3(threads), 0, st, noq, ws, splits, B, 1,
+                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace q3

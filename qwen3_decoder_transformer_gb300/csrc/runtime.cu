@@ -2,6 +2,7 @@
 // launch sequence of the forward pass ("A modern architecture: Qwen3", The whole model: embed,
 // L pre-norm blocks, final norm, LM head; positions continue from the cache length), CUDA-graph
 // replay of decode steps, per-kernel event timing, and the single-operation entry points.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -26,6 +27,7 @@ enum KernelClass : int {
     K_GEMM_LMHEAD,
     K_ATTN_DECODE,
     K_LENGTH,
+    K_FINALIZE,
     K_NUM_CLASSES
 };
 const char* kClassNames[K_NUM_CLASSES] = {"embed",
@@ -37,7 +39,8 @@ const char* kClassNames[K_NUM_CLASSES] = {"embed",
                                           "gemm_down_residual",
                                           "gemm_lmhead",
                                           "attn_decode",
-                                          "length_update"};
+                                          "length_update",
+                                          "decode_finalize"};
 
 struct TimedLaunch {
     int cls;
@@ -82,6 +85,9 @@ struct qwen3_ctx {
     bf16 *wqkv = nullptr, *wgu = nullptr, *kcache = nullptr, *vcache = nullptr, *rope = nullptr;
     bf16 *x = nullptr, *xn = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
     float* dec_work = nullptr;
+    float* skinny_ws = nullptr;  // decode split-K GEMM accumulator [64][max N] fp32, kept zero between uses
+    long long skinny_ld = 0;
+    CUtensorMap tX_xn, tX_attn, tX_h, tX_hn;  // decode activation maps (64-row boxes)
     float* attn_ws = nullptr;  // split prefill attention: tickets + partials (zeroed at init)
     size_t attn_ws_bytes = 0;
     int* d_len = nullptr;
@@ -164,10 +170,66 @@ int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, co
 bf16* layer_k(qwen3_ctx* c, int l) { return c->kcache + (size_t)l * c->layer_elems; }
 bf16* layer_v(qwen3_ctx* c, int l) { return c->vcache + (size_t)l * c->layer_elems; }
 
+int skinny(qwen3_ctx* c, int cls, const CUtensorMap& tw, const CUtensorMap& tx, int M, int N, int K, float* out,
+           int splits, cudaStream_t st) {
+    SkinnyArgs a{M, N, K, splits, c->skinny_ws, N, out, N, c->d_err};
+    return timed(c, cls, 1, st, [&] { return gemm_skinny_launch(tw, tx, a, st); });
+}
+
+// Decode step for B <= 64 sequences: weight-streaming split-K GEMMs into per-split fp32 slices, each
+// followed by a finalize kernel that adds the slices in order and applies the epilogue (q/k-norm +
+// RoPE + cache append, residual add fused with the next RMSNorm, SwiGLU).
+int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits, cudaStream_t st) {
+    const qwen3_config& g = c->cfg;
+    const int d = g.hidden, dh = g.head_dim, F = g.intermediate, L = g.n_layers;
+    const int s_qkv = skinny_splits(c->qkv_n, d), s_o = skinny_splits(d, c->q_width);
+    const int s_gu = skinny_splits(2 * F, d), s_dn = skinny_splits(d, F);
+    TRY(timed(c, K_EMBED, 1, st, [&] { return embed_launch(c->embed, g.vocab, d, ids, B, c->x, c->d_err, st); }));
+    TRY(timed(c, K_RMSNORM, 1, st, [&] { return rmsnorm_launch(c->x, c->in_norm[0], B, d, 1, 0, g.rms_eps, c->xn, st); }));
+    for (int l = 0; l < L; ++l) {
+        if (l == c->tap_layer && c->tap_in)
+            if (cudaMemcpyAsync(c->tap_in, c->x, (size_t)B * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return QWEN3_E_CUDA;
+        TRY(skinny(c, K_GEMM_QKV, c->tB_qkv[l], c->tX_xn, B, c->qkv_n, d, nullptr, s_qkv, st));
+        TRY(timed(c, K_FINALIZE, 1, st, [&] {
+            return qknorm_rope_append_f32_launch(c->skinny_ws, s_qkv, B, g.n_q_heads, g.n_kv_heads, dh, c->q_norm[l],
+                                                 c->k_norm[l], c->rope, c->d_len, g.rms_eps, c->q, layer_k(c, l),
+                                                 layer_v(c, l), c->capacity, st);
+        }));
+        TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
+            return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
+                                      c->capacity, c->d_len, c->dec_work, c->attn, st);
+        }));
+        TRY(skinny(c, K_GEMM_O, c->tB_o[l], c->tX_attn, B, d, c->q_width, nullptr, s_o, st));
+        TRY(timed(c, K_FINALIZE, 1, st, [&] {
+            return finalize_residual_rmsnorm_launch(c->skinny_ws, s_o, d, c->x, c->post_norm[l], B, d, g.rms_eps, c->xn,
+                                                    st);
+        }));
+        TRY(skinny(c, K_GEMM_GATEUP, c->tB_gu[l], c->tX_xn, B, 2 * F, d, nullptr, s_gu, st));
+        TRY(timed(c, K_FINALIZE, 1, st,
+                  [&] { return finalize_swiglu_launch(c->skinny_ws, s_gu, 2 * F, c->h, B, F, st); }));
+        TRY(skinny(c, K_GEMM_DOWN, c->tB_down[l], c->tX_h, B, d, F, nullptr, s_dn, st));
+        const bool last = l == L - 1;
+        TRY(timed(c, K_FINALIZE, 1, st, [&] {
+            return finalize_residual_rmsnorm_launch(c->skinny_ws, s_dn, d, c->x, last ? c->final_norm : c->in_norm[l + 1],
+                                                    B, d, g.rms_eps, last ? c->hn : c->xn, st);
+        }));
+        if (l == c->tap_layer && c->tap_out)
+            if (cudaMemcpyAsync(c->tap_out, c->x, (size_t)B * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return QWEN3_E_CUDA;
+    }
+    TRY(skinny(c, K_GEMM_LMHEAD, c->tB_head, c->tX_hn, B, g.vocab, d, logits, 1, st));
+    TRY(timed(c, K_LENGTH, 1, st, [&] { return add_len_launch(c->d_len, 1, st); }));
+    return QWEN3_OK;
+}
+
+bool use_skinny_decode(const qwen3_ctx* c, int B) { return B <= kSkinnyRowsBox && c->cfg.hidden <= 4096; }
+
 // One forward pass over M = B*T rows already gathered into c->x (T = 1 for decode).
 int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logits, int flags, bool decode,
                     cudaStream_t st) {
     const qwen3_config& g = c->cfg;
+    if (decode && use_skinny_decode(c, B)) return enqueue_decode_skinny(c, ids, B, logits, st);
     const int M = B * T, d = g.hidden, dh = g.head_dim, F = g.intermediate;
     TRY(timed(c, K_EMBED, 1, st, [&] { return embed_launch(c->embed, g.vocab, d, ids, M, c->x, c->d_err, st); }));
     // Q [B*Hq][T][dh] store map for the fused QKV epilogue (used when T is a multiple of 128)
@@ -261,7 +323,7 @@ void release(qwen3_ctx* c) {
     for (auto e : c->free_events) cudaEventDestroy(e);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
-                    c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->d_len,
+                    c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->skinny_ws, c->d_len,
                     c->d_err, c->d_ids_buf, c->d_logits_buf};
     for (void* p : bufs)
         if (p) cudaFree(p);
@@ -364,6 +426,14 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
                   cudaSuccess &&
               dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
               dmalloc(&c->d_ids_buf, rows) == cudaSuccess;
+    // decode split-K workspace: the largest [splits][64][N] fp32 set of slices over the four projections
+    if (ok) {
+        const long long need = std::max(
+            std::max((long long)skinny_splits(c->qkv_n, d) * c->qkv_n, (long long)skinny_splits(d, c->q_width) * d),
+            std::max((long long)skinny_splits(2 * F, d) * 2 * F, (long long)skinny_splits(d, F) * d));
+        c->skinny_ld = need;
+        ok = dmalloc(&c->skinny_ws, (size_t)kSkinnyRowsBox * need) == cudaSuccess;
+    }
     // split-attention workspace: sized for the largest split the planner can choose (work items up to
     // the SM count, up to 4 chunks each)
     if (ok) {
@@ -404,7 +474,9 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          encode_tmap_bf16_2d(&c->tA_h, c->h, F, arows, (uint64_t)F * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN) &&
-         encode_tmap_out(&c->tC_x, c->x, false, d, rows, d) && encode_tmap_out(&c->tC_h, c->h, false, F, arows, F);
+         encode_tmap_out(&c->tC_x, c->x, false, d, rows, d) && encode_tmap_out(&c->tC_h, c->h, false, F, arows, F) &&
+         encode_skinny_x_map(&c->tX_xn, c->xn, arows, d) && encode_skinny_x_map(&c->tX_attn, c->attn, arows, c->q_width) &&
+         encode_skinny_x_map(&c->tX_h, c->h, arows, F) && encode_skinny_x_map(&c->tX_hn, c->hn, arows, d);
     c->tK3.resize(L);
     c->tV3.resize(L);
     for (int l = 0; ok && l < L; ++l)
@@ -579,10 +651,10 @@ int qwen3_kernel_times(qwen3_ctx* c, double* total_ms, int64_t* launches, int* n
 const char* qwen3_kernel_class_name(int i) { return (i >= 0 && i < K_NUM_CLASSES) ? kClassNames[i] : nullptr; }
 
 int qwen3_launch_count(const qwen3_ctx* c, int B, int T, int flags, int decode) {
-    (void)B;
     (void)T;
     (void)flags;
     if (!c) return -1;
+    if (decode && use_skinny_decode(c, B)) return 2 + c->cfg.n_layers * (8 + attn_decode_kernel_count()) + 2;
     const int per_layer = 6 + (decode ? attn_decode_kernel_count() : 1);
     return 1 + c->cfg.n_layers * per_layer + 3;
 }
@@ -633,6 +705,24 @@ int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, vo
         return QWEN3_E_CUDA;
     GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
     return gemm_launch(m, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
+}
+
+int qwen3_gemm_skinny_splits(int N, int K) { return (N < 1 || K < 8) ? 1 : skinny_splits(N, K); }
+
+int qwen3_op_gemm_skinny(const void* A, const void* B, int M, int N, int K, int splits, float* slices, float* out,
+                         int* err, void* stream) {
+    if (!A || !B || M < 1 || M > kSkinnyRowsBox || N < 1 || K < 8 || K % 8 || splits < 1 || splits > 64) return QWEN3_E_ARG;
+    if ((splits == 1 && !out) || (splits > 1 && !slices)) return QWEN3_E_ARG;
+    if (!is_aligned(A, 16) || !is_aligned(B, 16)) return QWEN3_E_ARG;
+    const int k_blocks = (K + kGemmBK - 1) / kGemmBK;
+    if ((k_blocks + splits - 1) / splits * (splits - 1) >= k_blocks) return QWEN3_E_ARG;  // no empty split
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
+    CUtensorMap tw, tx;
+    if (!encode_tmap_bf16_2d(&tw, B, K, N, (uint64_t)K * 2, kGemmBK, kGemmBoxN) ||
+        !encode_skinny_x_map(&tx, A, (uint64_t)M, (uint64_t)K))
+        return QWEN3_E_CUDA;
+    SkinnyArgs a{M, N, K, splits, slices, N, splits == 1 ? out : nullptr, N, err};
+    return gemm_skinny_launch(tw, tx, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
 int qwen3_op_pack_gate_up(const void* gate, const void* up, int F, int d, void* out, void* stream) {

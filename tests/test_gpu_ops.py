@@ -203,6 +203,27 @@ def test_gemm_residual_in_place(bd, M, N, K):
     assert rel_l2(widen(bits(xd)), widen(ref)) <= 1e-3
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (16, 4096, 4096), (64, 1024, 2048), (5, 1000, 1024), (33, 3072, 512)])
+def test_gemm_skinny(bd, M, N, K):
+    """Decode GEMM: split-K slices (summed on the test side) and the unsplit direct store."""
+    rng = np.random.default_rng(M * 7 + N)
+    a = rand_bf16(rng, (M, K))
+    w = rand_bf16(rng, (N, K), 0.05)
+    ref = O.linear(a, w, f32_out=True)
+    splits = bd.gemm_skinny_splits(N, K)
+    err = _err()
+    if splits > 1:
+        sl = torch.full((splits, M, N), float("nan"), dtype=torch.float32, device="cuda")
+        bd.op_gemm_skinny(dev(a), dev(w), splits, slices=sl, err=err)
+        torch.cuda.synchronize()
+        assert rel_l2(sl.sum(0).double().cpu().numpy(), ref) <= 1e-5
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    bd.op_gemm_skinny(dev(a), dev(w), 1, out=out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert rel_l2(out.cpu().numpy(), ref) <= 1e-5
+
+
 # ------------------------------------------------------------------------------------- attention
 
 def _attn_ref(q, kc, vc, len0, T):
