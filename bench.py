@@ -456,7 +456,7 @@ def run_op(args, wl):
         fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out)
         work, unit, bound = 4.0 * B * hq * dh * T * (T + 1) / 2, "TFLOP/s", "tensor"
     elif args.op == "attn_decode":
-        Bd, ctx = wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
+        Bd, ctx = args.rows or wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
         q, kc, vc = rnd(Bd, hq, dh), rnd(Bd, hkv, ctx + 8, dh), rnd(Bd, hkv, ctx + 8, dh)
         len0.fill_(ctx - 1)
         ws = torch.empty(binding.attention_decode_workspace(Bd, hq, dh, ctx + 8) // 4, dtype=torch.float32,
@@ -534,7 +534,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=128, help="cap on timed decode steps")
     ap.add_argument("--op", default=None, help="time one kernel alone: attn_prefill, attn_decode, gemm_gateup, "
                                                 "gemm_qkv, gemm_o, gemm_down, qknorm_rope, rmsnorm")
-    ap.add_argument("--rows", type=int, default=0, help="row count for --op gemm_*/rmsnorm (default B*T)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="row count for --op gemm_*/rmsnorm (default B*T), batch for --op attn_decode")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
