@@ -21,6 +21,7 @@ _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 class OracleConfig(ctypes.Structure):
@@ -106,6 +107,13 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
                                  _u16p, _u16p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                  _i32p, ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int,
                                  _u16p, _u16p]
+    L.oracle_attention_masked_gqa_row_f64.restype = ctypes.c_int
+    L.oracle_attention_masked_gqa_row_f64.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, _u8p, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int, _f64p]
+    L.oracle_forward_masked.restype = ctypes.c_int
+    L.oracle_forward_masked.argtypes = [ctypes.POINTER(OracleConfig), ctypes.POINTER(OracleWeights),
+                                        _u16p, _u16p, ctypes.c_int, ctypes.c_int64, _i32p, ctypes.c_int,
+                                        _i32p, _i32p, _u8p, ctypes.c_int, _f32p, ctypes.c_int, _u16p, _u16p]
     return L
 
 
@@ -242,6 +250,20 @@ def attention_gqa_row_f64(q, kc, vc, n: int) -> np.ndarray:
     return out
 
 
+def attention_masked_gqa_row_f64(q, kc, vc, mask) -> np.ndarray:
+    """q [Hq, dh] against the slots of kc/vc [Hkv, cap, dh] that mask [cap] admits; [Hq, dh] fp64."""
+    q, kc, vc = _u16(q), _u16(kc), _u16(vc)
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    hq, dim = q.shape
+    hkv, cap, _ = kc.shape
+    out = np.empty((hq, dim), dtype=np.float64)
+    rc = lib().oracle_attention_masked_gqa_row_f64(_p(q, _u16p), _p(kc, _u16p), _p(vc, _u16p), cap,
+                                                   _p(mask, _u8p), hq, hkv, dim, _p(out, _f64p))
+    if rc != 0:
+        raise ValueError("the mask admits no key")
+    return out
+
+
 # ---------------------------------------------------------------- model
 
 def make_config(cfg: dict) -> OracleConfig:
@@ -313,6 +335,32 @@ class Model:
                                   _p(tout, _u16p) if tout is not None else null)
         if rc != 0:
             raise ValueError({-1: "token id out of range", -2: "cache capacity exceeded"}.get(rc, rc))
+        return (logits, tin, tout) if tap_layer >= 0 else logits
+
+    def forward_masked(self, kc, vc, ids, pos, slot, mask, all_rows: bool = False, tap_layer: int = -1):
+        """General forward: ids, pos, slot [B, T] int32; mask [B, T, cap] bool over cache slots.
+
+        Token (b, t) is rotated at pos[b, t], writes its K/V into slot[b, t] of sequence b and attends to
+        the slots mask[b, t] admits (after this call's writes). Returns logits like ``forward``."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        B, T = ids.shape
+        cap = kc.shape[3]
+        pos = np.ascontiguousarray(np.broadcast_to(pos, (B, T)), dtype=np.int32)
+        slot = np.ascontiguousarray(np.broadcast_to(slot, (B, T)), dtype=np.int32)
+        mask = np.ascontiguousarray(np.broadcast_to(mask, (B, T, cap)), dtype=np.uint8)
+        V, d = self.cfg["vocab"], self.cfg["hidden"]
+        logits = np.empty(((B * T) if all_rows else B, V), dtype=np.float32)
+        tin = np.empty((B * T, d), dtype=np.uint16) if tap_layer >= 0 else None
+        tout = np.empty((B * T, d), dtype=np.uint16) if tap_layer >= 0 else None
+        null = ctypes.cast(None, _u16p)
+        rc = lib().oracle_forward_masked(ctypes.byref(self.c), ctypes.byref(self.ow), _p(kc, _u16p),
+                                         _p(vc, _u16p), B, cap, _p(ids, _i32p), T, _p(pos, _i32p),
+                                         _p(slot, _i32p), _p(mask, _u8p), int(all_rows), _p(logits, _f32p),
+                                         tap_layer, _p(tin, _u16p) if tin is not None else null,
+                                         _p(tout, _u16p) if tout is not None else null)
+        if rc != 0:
+            raise ValueError({-1: "token id out of range", -2: "cache slot out of range",
+                              -3: "a row's mask admits no key"}.get(rc, rc))
         return (logits, tin, tout) if tap_layer >= 0 else logits
 
     def layer_qkv(self, layer: int, xin, pos):

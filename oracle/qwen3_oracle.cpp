@@ -19,6 +19,10 @@
 // value the pages print, a closed form, an invariant, or an independent library routine, except
 // oracle_forward as a whole, which is pinned only through its pinned parts plus invariants
 // (cached == uncached, causal prefix, batch independence) and an fp64 library re-statement.
+// The masked forms (oracle_attention_masked_gqa_row_f64, oracle_layer_out_masked,
+// oracle_forward_masked) are pinned by reduction to the equal-length forward pass and by the pairs
+// of routes the pages say must agree: a padded row equals the row alone, a shared prefix equals the
+// concatenated prompt, a banded mask equals a rolling buffer (tests/test_oracle_generation.py).
 
 #include "qwen3_oracle.h"
 
@@ -294,24 +298,15 @@ void oracle_layer_qkv(const oracle_config* c, const oracle_weights* w, int layer
     }
 }
 
-// a5-a9: causal GQA attention over the cache, o_proj + residual, post-attention RMSNorm,
-// SwiGLU MLP + residual.
-void oracle_layer_out(const oracle_config* c, const oracle_weights* w, int layer, const uint16_t* xin,
-                      const uint16_t* q, const int32_t* pos, int64_t n, const uint16_t* kc,
-                      const uint16_t* vc, const int32_t* kvset, int64_t cap, uint16_t* xout) {
+// a6-a9 for n rows, given their bf16 attention outputs att [n][Hq*dh]: o_proj + residual,
+// post-attention RMSNorm, SwiGLU MLP + residual.
+static void layer_tail(const oracle_config* c, const oracle_weights* w, int layer, const uint16_t* xin,
+                       const uint16_t* att, int64_t n, uint16_t* xout) {
     Dims D(c);
     int64_t qw = (int64_t)D.hq * D.dh;
-    std::vector<uint16_t> att((size_t)(n * qw)), o((size_t)(n * D.d)), x1((size_t)(n * D.d)),
-        xn((size_t)(n * D.d)), gt((size_t)(n * D.F)), up((size_t)(n * D.F)), a((size_t)(n * D.F)),
-        dn((size_t)(n * D.d));
-    std::vector<double> orow((size_t)qw);
-    for (int64_t r = 0; r < n; ++r) {
-        int64_t set_base = (int64_t)kvset[r] * D.hkv * cap * D.dh;
-        oracle_attention_gqa_row_f64(q + r * qw, kc + set_base, vc + set_base, (int64_t)pos[r] + 1,
-                                     D.hq, D.hkv, D.dh, cap, orow.data());
-        for (int64_t i = 0; i < qw; ++i) att[r * qw + i] = bf16_of_d(orow[i]);
-    }
-    oracle_linear(att.data(), w->o_proj[layer], n, D.d, qw, o.data());
+    std::vector<uint16_t> o((size_t)(n * D.d)), x1((size_t)(n * D.d)), xn((size_t)(n * D.d)),
+        gt((size_t)(n * D.F)), up((size_t)(n * D.F)), a((size_t)(n * D.F)), dn((size_t)(n * D.d));
+    oracle_linear(att, w->o_proj[layer], n, D.d, qw, o.data());
 #ifdef ORACLE_PLANT_DROP_ATTN_RESIDUAL
     for (int64_t i = 0; i < n * D.d; ++i) x1[i] = o[i];
 #else
@@ -323,6 +318,74 @@ void oracle_layer_out(const oracle_config* c, const oracle_weights* w, int layer
     oracle_swiglu(gt.data(), up.data(), n * D.F, a.data());
     oracle_linear(a.data(), w->down_proj[layer], n, D.d, D.F, dn.data());
     oracle_residual_add(x1.data(), dn.data(), n * D.d, xout);
+}
+
+// a5-a9: causal GQA attention over the cache, o_proj + residual, post-attention RMSNorm,
+// SwiGLU MLP + residual.
+void oracle_layer_out(const oracle_config* c, const oracle_weights* w, int layer, const uint16_t* xin,
+                      const uint16_t* q, const int32_t* pos, int64_t n, const uint16_t* kc,
+                      const uint16_t* vc, const int32_t* kvset, int64_t cap, uint16_t* xout) {
+    Dims D(c);
+    int64_t qw = (int64_t)D.hq * D.dh;
+    std::vector<uint16_t> att((size_t)(n * qw));
+    std::vector<double> orow((size_t)qw);
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t set_base = (int64_t)kvset[r] * D.hkv * cap * D.dh;
+        oracle_attention_gqa_row_f64(q + r * qw, kc + set_base, vc + set_base, (int64_t)pos[r] + 1,
+                                     D.hq, D.hkv, D.dh, cap, orow.data());
+        for (int64_t i = 0; i < qw; ++i) att[r * qw + i] = bf16_of_d(orow[i]);
+    }
+    layer_tail(c, w, layer, xin, att.data(), n, xout);
+}
+
+// Masked attention (the pages' boolean attention mask, True = may attend): the keys a row's mask
+// admits are gathered in slot order from one cache set kc/vc [Hkv][cap][dh] and handed to the
+// plain row attention. A row that admits no key has no defined output (softmax over nothing);
+// the function returns -3 for it.
+int oracle_attention_masked_gqa_row_f64(const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
+                                        int64_t cap, const uint8_t* mask, int hq, int hkv, int dim,
+                                        double* out) {
+    std::vector<int64_t> keep;
+    for (int64_t s = 0; s < cap; ++s) {
+#ifdef ORACLE_PLANT_MASK_CAUSAL_ONLY
+        // planted mistake: every slot up to the last admitted one, masked keys inside included
+        bool later = false;
+        for (int64_t u = s; u < cap; ++u) later = later || mask[u];
+        if (later) keep.push_back(s);
+#else
+        if (mask[s]) keep.push_back(s);
+#endif
+    }
+    if (keep.empty()) return -3;
+    int64_t n = (int64_t)keep.size();
+    std::vector<uint16_t> kg((size_t)(hkv * n * dim)), vg((size_t)(hkv * n * dim));
+    for (int j = 0; j < hkv; ++j)
+        for (int64_t i = 0; i < n; ++i) {
+            std::memcpy(&kg[(size_t)((j * n + i) * dim)], kc + ((int64_t)j * cap + keep[i]) * dim, (size_t)dim * 2);
+            std::memcpy(&vg[(size_t)((j * n + i) * dim)], vc + ((int64_t)j * cap + keep[i]) * dim, (size_t)dim * 2);
+        }
+    oracle_attention_gqa_row_f64(q, kg.data(), vg.data(), n, hq, hkv, dim, n, out);
+    return 0;
+}
+
+// a5-a9 with an explicit mask per row: row r reads the slots of kv set kvset[r] that
+// mask[r][0..cap) admits.
+int oracle_layer_out_masked(const oracle_config* c, const oracle_weights* w, int layer, const uint16_t* xin,
+                            const uint16_t* q, int64_t n, const uint16_t* kc, const uint16_t* vc,
+                            const int32_t* kvset, int64_t cap, const uint8_t* mask, uint16_t* xout) {
+    Dims D(c);
+    int64_t qw = (int64_t)D.hq * D.dh;
+    std::vector<uint16_t> att((size_t)(n * qw));
+    std::vector<double> orow((size_t)qw);
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t set_base = (int64_t)kvset[r] * D.hkv * cap * D.dh;
+        int rc = oracle_attention_masked_gqa_row_f64(q + r * qw, kc + set_base, vc + set_base, cap, mask + r * cap,
+                                                     D.hq, D.hkv, D.dh, orow.data());
+        if (rc != 0) return rc;
+        for (int64_t i = 0; i < qw; ++i) att[r * qw + i] = bf16_of_d(orow[i]);
+    }
+    layer_tail(c, w, layer, xin, att.data(), n, xout);
+    return 0;
 }
 
 // Final RMSNorm, then hidden @ W^T with W = lm_head, or the embedding matrix when tied.
@@ -364,6 +427,58 @@ int oracle_forward(const oracle_config* c, const oracle_weights* w, uint16_t* kc
                 std::memcpy(vl + slot, &v[(size_t)(m * kvw + (int64_t)j * D.dh)], (size_t)D.dh * 2);
             }
         oracle_layer_out(c, w, l, x.data(), q.data(), pos.data(), M, kl, vl, set.data(), cap, y.data());
+        x.swap(y);
+        if (l == tap_layer && tap_out) std::memcpy(tap_out, x.data(), x.size() * 2);
+    }
+    if (all_rows) {
+        oracle_head(c, w, x.data(), M, logits);
+    } else {
+        std::vector<uint16_t> last((size_t)B * D.d);
+        for (int b = 0; b < B; ++b)
+            std::memcpy(&last[(size_t)b * D.d], &x[(size_t)(((int64_t)b * T + T - 1) * D.d)], (size_t)D.d * 2);
+        oracle_head(c, w, last.data(), B, logits);
+    }
+    return 0;
+}
+
+// The general form of the forward pass ("A modern architecture: Qwen3", section The whole model,
+// hidden(ids, positions, mask, caches), as its batched generation section drives it): token
+// r = b*T + t is rotated at position pos[r], writes its key and value into slot slot[r] of
+// sequence b's cache, and then attends to the slots of sequence b that mask[r][0..cap) admits.
+// Left padding, a shared prefix, a banded (sliding-window) mask and a rolling buffer are all
+// choices of pos, slot and mask; this function only carries them out.
+// Returns 0, -1 on a bad token id, -2 on a slot outside [0, cap), -3 on a row admitting no key.
+int oracle_forward_masked(const oracle_config* c, const oracle_weights* w, uint16_t* kc, uint16_t* vc,
+                          int B, int64_t cap, const int32_t* ids, int T, const int32_t* pos,
+                          const int32_t* slot, const uint8_t* mask, int all_rows, float* logits,
+                          int tap_layer, uint16_t* tap_in, uint16_t* tap_out) {
+    Dims D(c);
+    int64_t M = (int64_t)B * T;
+    int64_t kvw = (int64_t)D.hkv * D.dh;
+    std::vector<uint16_t> x((size_t)(M * D.d)), y((size_t)(M * D.d)), q((size_t)(M * D.hq * D.dh)),
+        k((size_t)(M * kvw)), v((size_t)(M * kvw));
+    std::vector<int32_t> set((size_t)M);
+    for (int64_t m = 0; m < M; ++m) {
+        int32_t id = ids[m];
+        if (id < 0 || id >= D.V) return -1;
+        if (slot[m] < 0 || slot[m] >= cap) return -2;
+        std::memcpy(&x[(size_t)(m * D.d)], w->embed + (int64_t)id * D.d, (size_t)D.d * 2);
+        set[m] = (int32_t)(m / T);
+    }
+    int64_t layer_elems = (int64_t)B * D.hkv * cap * D.dh;
+    for (int l = 0; l < D.L; ++l) {
+        if (l == tap_layer && tap_in) std::memcpy(tap_in, x.data(), x.size() * 2);
+        oracle_layer_qkv(c, w, l, x.data(), pos, M, q.data(), k.data(), v.data());
+        uint16_t* kl = kc + l * layer_elems;
+        uint16_t* vl = vc + l * layer_elems;
+        for (int64_t m = 0; m < M; ++m)
+            for (int j = 0; j < D.hkv; ++j) {
+                int64_t at = (((int64_t)set[m] * D.hkv + j) * cap + slot[m]) * D.dh;
+                std::memcpy(kl + at, &k[(size_t)(m * kvw + (int64_t)j * D.dh)], (size_t)D.dh * 2);
+                std::memcpy(vl + at, &v[(size_t)(m * kvw + (int64_t)j * D.dh)], (size_t)D.dh * 2);
+            }
+        int rc = oracle_layer_out_masked(c, w, l, x.data(), q.data(), M, kl, vl, set.data(), cap, mask, y.data());
+        if (rc != 0) return rc;
         x.swap(y);
         if (l == tap_layer && tap_out) std::memcpy(tap_out, x.data(), x.size() * 2);
     }

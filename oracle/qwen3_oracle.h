@@ -117,6 +117,28 @@ int oracle_forward(const oracle_config* c, const oracle_weights* w, uint16_t* kc
                    int B, int64_t cap, int64_t len0, const int32_t* ids, int T, int all_rows,
                    float* logits, int tap_layer, uint16_t* tap_in, uint16_t* tap_out);
 
+/* Masked attention of one row: q [Hq][dh] against the slots of kc/vc [Hkv][cap][dh] that
+   mask[0..cap) admits (nonzero), in slot order. Returns -3 when the mask admits nothing. */
+int oracle_attention_masked_gqa_row_f64(const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
+                                        int64_t cap, const uint8_t* mask, int hq, int hkv, int dim,
+                                        double* out);
+
+/* Steps a5-a9 with an explicit mask: row r reads the slots of kv set kvset[r] that mask[r][cap]
+   admits. Returns 0 or -3 (a row admitting no key). */
+int oracle_layer_out_masked(const oracle_config* c, const oracle_weights* w, int layer, const uint16_t* xin,
+                            const uint16_t* q, int64_t n, const uint16_t* kc, const uint16_t* vc,
+                            const int32_t* kvset, int64_t cap, const uint8_t* mask, uint16_t* xout);
+
+/* General forward pass: token r = b*T + t is rotated at position pos[r], writes its K/V into slot
+   slot[r] of sequence b's cache kc/vc ([L][B][Hkv][cap][dh]) and attends to the slots that
+   mask[r][cap] admits. Left padding, a shared prefix, a sliding window and a rolling buffer are
+   choices of pos, slot and mask made by the caller. Returns 0, -1 (bad token id), -2 (slot out
+   of range) or -3 (a row admitting no key). */
+int oracle_forward_masked(const oracle_config* c, const oracle_weights* w, uint16_t* kc, uint16_t* vc,
+                          int B, int64_t cap, const int32_t* ids, int T, const int32_t* pos,
+                          const int32_t* slot, const uint8_t* mask, int all_rows, float* logits,
+                          int tap_layer, uint16_t* tap_in, uint16_t* tap_out);
+
 #ifdef __cplusplus
 }
 #endif

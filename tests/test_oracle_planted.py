@@ -5,12 +5,14 @@ import pytest
 
 import oracle as O
 from qwen3_decoder_transformer_gb300 import TINY, synth
+from tests import test_oracle_generation as TG
 from tests import test_oracle_model as TM
 from tests import test_oracle_pins as TP
 
 PLANTS = ["ORACLE_PLANT_GAMMA_BEFORE_CAST", "ORACLE_PLANT_LINEAR_DROP_LAST_K", "ORACLE_PLANT_SILU_SIGN",
           "ORACLE_PLANT_ROPE_ADJACENT", "ORACLE_PLANT_ROPE_SIGN", "ORACLE_PLANT_SCALE_BY_DIM",
-          "ORACLE_PLANT_GQA_MODULO", "ORACLE_PLANT_NO_QNORM", "ORACLE_PLANT_DROP_ATTN_RESIDUAL"]
+          "ORACLE_PLANT_GQA_MODULO", "ORACLE_PLANT_NO_QNORM", "ORACLE_PLANT_DROP_ATTN_RESIDUAL",
+          "ORACLE_PLANT_MASK_CAUSAL_ONLY"]
 
 
 def _run_all_checks():
@@ -26,6 +28,11 @@ def _run_all_checks():
         TM.check_matches_f64_statement(w, m)
     except AssertionError:
         failed.append("check_matches_f64_statement")
+    for chk in TG.ALL_CHECKS:
+        try:
+            chk(m)
+        except AssertionError:
+            failed.append(chk.__name__)
     return failed
 
 
