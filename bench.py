@@ -265,11 +265,13 @@ def run_ours(args, wl):
     ids = synth.make_ids(V, B, T, wl["seed"], device=dev)
     m = binding.Model(cfg, w, max_batch=B, capacity=T, max_tokens=B * T)
     logits = torch.empty(B, V, dtype=torch.float32, device=dev)
+    next_ids = torch.empty(B, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step():  # prefill, then the greedy next token of every sequence
         m.set_length(0, 0)
         m.prefill(ids, logits)
+        binding.op_greedy(logits, next_ids)
 
     for _ in range(args.warmup):
         step()
@@ -347,7 +349,7 @@ def run_ours(args, wl):
             "peak_source": f"{peak_src} ({'sustained' if (bound == 'tensor' and long_region) else 'burst'})",
             "algorithmic_per_launch": units, "avg_launch_ms": avg_ms}
     step_tf = step_flops(cfg, B, T)
-    launches = m.launch_count(B, T) + 1  # + the length reset before each step
+    launches = m.launch_count(B, T) + 2  # + the length reset before each step and the greedy kernel
     if rank != 0:
         return
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -395,17 +397,21 @@ def measure_decode(binding, synth, torch, cfg, wl, w, dev, steps_cap: int):
         k[:, :, :ctx].copy_(synth.make_kv_normal(shape, wl["seed"], layer, "k", device=dev))
         v[:, :, :ctx].copy_(synth.make_kv_normal(shape, wl["seed"], layer, "v", device=dev))
     ids = synth.make_ids(V, Bd, 1, wl["seed"] + 100, device=dev).reshape(Bd)
+    first = ids.clone()
     logits = torch.empty(Bd, V, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(3):  # warm-up (the first call captures the graph)
         m.set_length(ctx, Bd)
         m.decode_step(ids, logits)
+        binding.op_greedy(logits, ids)
     torch.cuda.synchronize()
     m.set_length(ctx, Bd)
+    ids.copy_(first)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
+    for _ in range(steps):  # greedy generation: each step's argmax is the next step's input
         m.decode_step(ids, logits)
+        binding.op_greedy(logits, ids)
     b.record(stream)
     torch.cuda.synchronize()
     if m.get_error() != 0:
@@ -453,7 +459,10 @@ def run_op(args, wl):
     if args.op == "attn_prefill":
         q, kc, vc = rnd(B, hq, T, dh), rnd(B, hkv, T, dh), rnd(B, hkv, T, dh)
         out = torch.empty(M, hq * dh, dtype=torch.bfloat16, device="cuda")
-        fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out)
+        split, chunks = args.kv_split, max(1, args.kv_chunks)
+        ws = torch.zeros(max(1, binding.attention_prefill_workspace(B, T, hq, hkv, dh, chunks) // 4),
+                         dtype=torch.float32, device="cuda")
+        fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out, kv_split=split, kv_chunks=chunks, work=ws)
         work, unit, bound = 4.0 * B * hq * dh * T * (T + 1) / 2, "TFLOP/s", "tensor"
     elif args.op == "attn_decode":
         Bd, ctx = args.rows or wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
@@ -512,6 +521,201 @@ def run_op(args, wl):
                       "algorithmic_per_launch": work, "peak_source": src + " (burst)"}), flush=True)
 
 
+# ----------------------------------------------------------------------------- generation features
+
+def _timed(torch, fn, steps: int, warmup: int) -> float:
+    """Mean ms of fn() over `steps` calls after `warmup` calls, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def _kernel_split(m, fn, steps: int) -> dict:
+    m.set_timing(True)
+    m.kernel_times()
+    for _ in range(steps):
+        fn()
+    kt = m.kernel_times()
+    m.set_timing(False)
+    return {k: round(v[0] / steps, 4) for k, v in kt.items() if v[1]}
+
+
+def run_feature(args):
+    """Time one generation feature on its own synthetic workload (one GPU; prints one JSON line):
+
+    padded  left-padded batch ("A modern architecture: Qwen3", generation with a batch of prompts):
+            Qwen3-0.6B shape, 32 prompts of 512..2048 tokens padded to 2048; prefill + greedy token,
+            then 64 greedy decode steps (each step's argmax fed back).
+    prefix  shared prefix (section 8): a 2048-token start shared by 32 prompts of 64..256 tokens;
+            prefill of the start once + share + padded prefill of the prompts, against one padded
+            prefill of the 32 concatenated prompts.
+    window  sliding window (section 7): Qwen3-8B shape with a 4096-token window; decode of 16 sequences
+            at position 32768 from a rolling buffer, and a banded 1 x 32768 prefill over a full cache.
+    """
+    import torch
+
+    from qwen3_decoder_transformer_gb300 import binding, build, configs, synth
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks, src = load_peaks()
+    K, Wm = args.steps, args.warmup
+    line = {"feature": args.feature, "data": "synthetic (random-init bf16 weights, uniform token ids)",
+            "peak_source": src}
+    with ClockSampler(0) as clk:
+        if args.feature in ("padded", "prefix"):
+            cfg = configs.QWEN3_0P6B
+            V = cfg["vocab"]
+            seed = 5 if args.feature == "padded" else 6
+            w = synth.make_weights(cfg, seed, device=dev)
+            rng = np.random.default_rng(seed)
+            pad_id = 151643 % V
+        if args.feature == "padded":
+            B, T, D = 32, 2048, 64
+            real = rng.integers(512, T + 1, size=B)
+            ids = synth.make_ids(V, B, T, seed, device=dev)
+            for b in range(B):
+                ids[b, :T - int(real[b])] = pad_id
+            m = binding.Model(cfg, w, max_batch=B, capacity=T + D + 8, max_tokens=B * T)
+            logits = torch.empty(B, V, dtype=torch.float32, device=dev)
+            nxt = torch.empty(B, dtype=torch.int32, device=dev)
+
+            def prefill():
+                m.set_length(0, 0)
+                m.prefill_padded(ids, real, logits)
+                binding.op_greedy(logits, nxt)
+
+            ms = _timed(torch, prefill, K, Wm)
+            kern = _kernel_split(m, prefill, max(1, K // 4))
+            work = kernel_work(cfg, B, T)
+            att_ms = kern.get("attn_prefill", 0) / cfg["n_layers"]
+            line.update({"batch": B, "width": T, "real_tokens": int(real.sum()), "prefill_ms": ms,
+                         "real_tokens_per_s": float(real.sum()) / (ms / 1e3), "padded_tokens_per_s": B * T / (ms / 1e3),
+                         "prefill_kernels_ms": kern,
+                         "attn_prefill_frac_of_peak": work["attn_prefill"][1] / (att_ms / 1e3) / 1e12
+                         / peaks["bf16_tflops"] if att_ms else None})
+            prefill()
+
+            def decode():
+                m.decode_step(nxt, logits)
+                binding.op_greedy(logits, nxt)
+
+            line.update({"decode_steps": D, "decode_ms_per_step": _timed(torch, decode, D, 3)})
+            assert m.get_error() == 0
+            m.close()
+        elif args.feature == "prefix":
+            B, P, lo, hi = 32, 2048, 64, 256
+            lens = rng.integers(lo, hi + 1, size=B)
+            Tp = int(lens.max())
+            pre = synth.make_ids(V, 1, P, seed, device=dev)
+            body = synth.make_ids(V, B, Tp, seed + 1, device=dev)
+            for b in range(B):
+                body[b, :Tp - int(lens[b])] = pad_id
+            full = torch.cat([pre.expand(B, P), body], dim=1).contiguous()
+            for b in range(B):  # concatenated prompts, left-padded as a whole
+                n = P + int(lens[b])
+                full[b] = torch.cat([torch.full((P + Tp - n,), pad_id, dtype=torch.int32, device=dev),
+                                     pre[0], body[b, Tp - int(lens[b]):]])
+            m = binding.Model(cfg, w, max_batch=B, capacity=P + Tp + 8, max_tokens=B * (P + Tp))
+            l1 = torch.empty(1, V, dtype=torch.float32, device=dev)
+            la = torch.empty(B, V, dtype=torch.float32, device=dev)
+            lb = torch.empty(B, V, dtype=torch.float32, device=dev)
+            na = torch.empty(B, dtype=torch.int32, device=dev)
+            nb = torch.empty(B, dtype=torch.int32, device=dev)
+
+            def shared():
+                m.set_length(0, 0)
+                m.prefill(pre, l1)
+                m.share_prefix(B)
+                m.prefill_padded(body, lens, la)
+                binding.op_greedy(la, na)
+
+            def recompute():
+                m.set_length(0, 0)
+                m.prefill_padded(full, lens + P, lb)
+                binding.op_greedy(lb, nb)
+
+            ms_a = _timed(torch, shared, K, Wm)
+            ms_b = _timed(torch, recompute, K, Wm)
+            shared()
+            recompute()
+            torch.cuda.synchronize()
+            agree = float((na == nb).float().mean().item())
+            line.update({"batch": B, "prefix": P, "prompt_tokens": int(lens.sum()), "shared_ms": ms_a,
+                         "recompute_ms": ms_b, "speedup": ms_b / ms_a, "first_token_agreement": agree,
+                         "logits_rel_l2": float((la - lb).norm() / lb.norm())})
+            assert m.get_error() == 0
+            m.close()
+        elif args.feature == "window":
+            W = 4096
+            cfg = dict(configs.QWEN3_8B, sliding_window=W, rolling_cache=1)
+            V, L, Hkv, dh = cfg["vocab"], cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
+            seed = 7
+            w = synth.make_weights(cfg, seed, device=dev)
+            Bd, ctx, D = 16, 32768, 64
+            m = binding.Model(cfg, w, max_batch=Bd, capacity=ctx + D + 8, max_tokens=128)
+            k0, _ = m.kv_view(0)
+            R = k0.shape[2]
+            for layer in range(L):
+                k, v = m.kv_view(layer)
+                shape = (Bd, Hkv, R, dh)
+                k.copy_(synth.make_kv_normal(shape, seed, layer, "k", device=dev))
+                v.copy_(synth.make_kv_normal(shape, seed, layer, "v", device=dev))
+            nxt = synth.make_ids(V, Bd, 1, seed, device=dev).reshape(Bd)
+            logits = torch.empty(Bd, V, dtype=torch.float32, device=dev)
+            m.set_length(ctx, Bd)
+
+            def decode():
+                m.decode_step(nxt, logits)
+                binding.op_greedy(logits, nxt)
+
+            dms = _timed(torch, decode, D - 3, 3)
+            m.set_length(ctx, Bd)
+            kern = _kernel_split(m, lambda: m.decode_step(nxt, logits), 8)
+            att_bytes = 2.0 * Bd * Hkv * W * dh * 2
+            att_ms = kern.get("attn_decode", 0) / L
+            full_cache = 2.0 * L * Bd * Hkv * (ctx + D + 8) * dh * 2
+            line.update({"window": W, "decode_batch": Bd, "context": ctx, "ring_slots": R,
+                         "decode_ms_per_step": dms, "decode_kernels_ms": kern,
+                         "attn_decode_gbs": att_bytes / (att_ms / 1e3) / 1e9 if att_ms else None,
+                         "attn_decode_frac_of_hbm": att_bytes / (att_ms / 1e3) / 1e9 / peaks["hbm_gbs"] if att_ms else None,
+                         "cache_gb": 2.0 * L * Bd * Hkv * R * dh * 2 / 1e9, "full_cache_gb": full_cache / 1e9})
+            assert m.get_error() == 0
+            m.close()
+            # banded prefill of one long sequence over a full cache
+            cfgb = dict(configs.QWEN3_8B, sliding_window=W, rolling_cache=0)
+            T = 32768
+            mb = binding.Model(cfgb, w, max_batch=1, capacity=T, max_tokens=T)
+            ids = synth.make_ids(V, 1, T, seed, device=dev)
+            lg = torch.empty(1, V, dtype=torch.float32, device=dev)
+
+            def prefill():
+                mb.set_length(0, 0)
+                mb.prefill(ids, lg)
+
+            pms = _timed(torch, prefill, max(1, K // 4), 3)
+            kern = _kernel_split(mb, prefill, 1)
+            pairs = W * (W + 1) / 2 + (T - W) * W
+            att_flops = 4.0 * cfgb["n_q_heads"] * dh * pairs
+            line.update({"banded_prefill_tokens": T, "banded_prefill_ms": pms,
+                         "banded_prefill_tokens_per_s": T / (pms / 1e3), "banded_prefill_kernels_ms": kern,
+                         "banded_attn_tflops": att_flops * L / (kern["attn_prefill"] / 1e3) / 1e12})
+            assert mb.get_error() == 0
+            mb.close()
+        else:
+            raise SystemExit(f"unknown feature {args.feature}")
+    line["clocks"] = clk.summary()
+    print(json.dumps(line), flush=True)
+
+
+
 def _flat(w):
     for k, v in w.items():
         if isinstance(v, list):
@@ -534,13 +738,19 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=128, help="cap on timed decode steps")
     ap.add_argument("--op", default=None, help="time one kernel alone: attn_prefill, attn_decode, gemm_gateup, "
                                                 "gemm_qkv, gemm_o, gemm_down, qknorm_rope, rmsnorm")
+    ap.add_argument("--feature", default=None, choices=["padded", "prefix", "window"],
+                    help="time a generation feature on its own workload instead of the step")
+    ap.add_argument("--kv-split", type=int, default=0, help="--op attn_prefill: minimum tiles per KV chunk")
+    ap.add_argument("--kv-chunks", type=int, default=1, help="--op attn_prefill: maximum KV chunks per query tile")
     ap.add_argument("--rows", type=int, default=0,
                     help="row count for --op gemm_*/rmsnorm (default B*T), batch for --op attn_decode")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = configs.WORKLOADS[args.workload]
-    if args.op:
+    if args.feature:
+        run_feature(args)
+    elif args.op:
         run_op(args, wl)
     elif args.impl == "reference":
         run_reference(args, wl)

@@ -61,6 +61,15 @@ typedef struct qwen3_config {
     int32_t max_positions;  /* max_position_embeddings: upper bound for the cache capacity */
     float rope_theta;       /* RoPE base theta (1e6 for Qwen3) */
     float rms_eps;          /* RMSNorm epsilon (1e-6 for Qwen3) */
+    /* Sliding-window attention ("A modern architecture: Qwen3", section 7): 0 = full causal
+     * attention (Qwen3); W > 0 = in every layer the token in slot i sees slots j with i - W < j <= i. */
+    int32_t sliding_window;
+    /* With a window: 0 = the cache keeps every slot (the banded mask over a full cache); 1 = a
+     * rolling buffer that stores slot s at s mod R, R = W + min(ceil(max_tokens / max_batch),
+     * capacity) - 1 rounded up to 256, so the cache holds R slots per sequence and head however long
+     * the sequence grows.
+     * Prefill calls then take at most R - W + 1 tokens per sequence (E_BATCH beyond). */
+    int32_t rolling_cache;
 } qwen3_config;
 
 /* Device pointers to bf16 weights, BORROWED: they must stay valid until qwen3_free(). Linear
@@ -122,15 +131,49 @@ QWEN3_API int qwen3_decode_step(qwen3_ctx* ctx, const int32_t* d_ids, int B, flo
 QWEN3_API int qwen3_prefill_host(qwen3_ctx* ctx, const int32_t* h_ids, int B, int T, float* h_logits,
                        int flags, void* stream);
 
+/* Left-padded batch prefill ("A modern architecture: Qwen3", generation with a batch of prompts):
+ * row b of d_ids [B*T] holds h_real[b] real tokens (1..T, HOST array) at its end, after T - h_real[b]
+ * padding tokens. Padding gets no attention from any other token, each padding token attends to
+ * itself (and to every earlier real slot), and positions count real tokens: the k-th real token of
+ * a row is at position length + k, padding at max(length - 1, 0). Later prefill and decode calls keep
+ * the layout (each row's next position is its own count of real tokens). Allowed once per fill of
+ * the cache (qwen3_set_length clears the layout); rows without padding are ordinary prefill.
+ * Errors as qwen3_prefill, plus E_ARG (h_real out of range, a second padded block, or a context with
+ * a sliding window). */
+QWEN3_API int qwen3_prefill_padded(qwen3_ctx* ctx, const int32_t* d_ids, const int32_t* h_real, int B, int T,
+                                   float* d_logits, int flags, void* stream);
+
+/* Prefix caching ("A modern architecture: Qwen3", section 8): after a one-sequence prefill of a shared
+ * start of P tokens, make it the start of B sequences without recomputing it. Whole 128-slot tiles
+ * of the start are read in place from sequence 0's cache by every sequence; the remaining P mod 128
+ * slots are copied into sequences 1..B-1. The batch becomes B at length P; the next call continues all
+ * B sequences (qwen3_prefill_padded for prompts of different lengths). Errors: E_BATCH (B out of
+ * range), E_ARG (the cache does not hold exactly one unpadded sequence, a prefix is already shared,
+ * or the context has a sliding window), E_CUDA. */
+QWEN3_API int qwen3_share_prefix(qwen3_ctx* ctx, int B, void* stream);
+
+/* Greedy generation, the pages' generate loop: prefill of d_ids (left-padded by h_real when h_real
+ * is not NULL, else equal-length), then up to max_new tokens per row chosen by argmax of each step's
+ * logits (lowest index on ties), each fed back through qwen3_decode_step. With stop_id >= 0 a row that
+ * emits stop_id is finished and emits stop_id from then on, and the loop ends when every row has
+ * finished (the host reads a device counter after each step; this synchronises `stream`). Token k of
+ * row b goes to d_out[b * max_new + k]; *h_steps receives the number of columns written, later columns
+ * are left untouched. Errors as qwen3_prefill_padded / qwen3_decode_step, and E_OVERFLOW when the
+ * cache cannot hold T + max_new - 1 more tokens. */
+QWEN3_API int qwen3_generate(qwen3_ctx* ctx, const int32_t* d_ids, const int32_t* h_real, int B, int T, int max_new,
+                             int stop_id, int32_t* d_out, int* h_steps, void* stream);
+
 /* Current cache length (tokens per sequence) and batch held in the cache. */
 QWEN3_API int qwen3_length(const qwen3_ctx* ctx, int* length, int* batch);
 
 /* Set the cache length and batch, e.g. after filling the cache through qwen3_kv_view. Enqueues a
- * device update on `stream`. Errors: E_ARG, E_OVERFLOW (length > capacity), E_BATCH. */
+ * device update on `stream`. The cache then holds plain equal-length sequences: any padding layout
+ * or shared prefix is cleared. Errors: E_ARG, E_OVERFLOW (length > capacity), E_BATCH. */
 QWEN3_API int qwen3_set_length(qwen3_ctx* ctx, int length, int batch, void* stream);
 
-/* Device pointers to layer `layer`'s K and V cache, each [max_batch][Hkv][capacity][dh] bf16,
- * dims[0..3] = {max_batch, Hkv, capacity, dh}. The memory stays owned by the context. */
+/* Device pointers to layer `layer`'s K and V cache, each [max_batch][Hkv][slots][dh] bf16,
+ * dims[0..3] = {max_batch, Hkv, slots, dh}; slots = capacity, or the ring size of a rolling buffer.
+ * The memory stays owned by the context. */
 QWEN3_API int qwen3_kv_view(qwen3_ctx* ctx, int layer, void** d_k, void** d_v, int64_t dims[4]);
 
 /* Debug tap: on later prefill/decode calls, copy layer `layer`'s input and output hidden states
@@ -217,8 +260,13 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
                                 const int* d_len0, float eps, void* d_q_out, void* d_k_cache,
                                 void* d_v_cache, int cap, void* stream);
 
-/* Causal GQA attention for prefill: for query row t of sequence b (position len0 + t) and query
+/* Causal GQA attention for prefill: for query row t of sequence b (cache slot len0 + t) and query
  * head h, out = softmax(q k^T * dh^-0.5 over cache slots 0..len0+t of kv head h / (Hq/Hkv)) V.
+ * d_seq_meta (may be NULL) gives a padding layout and shared prefix as qwen3_prefill_padded and
+ * qwen3_share_prefix build it: ints [ps, psh, pad_0 .. pad_{B-1}]; slots [ps, ps + pad_b) of sequence b
+ * are seen only by themselves, slots below psh (a multiple of 128) are read from sequence 0.
+ * window > 0 restricts slot i to keys j > i - window; ring > 0 (= cap, a multiple of 256, with a
+ * window) reads slot s from cache row s mod ring.
  * q [B, Hq, T, dh]; caches [B, Hkv, cap, dh] with len0 + T <= cap; out [B*T, Hq*dh] bf16
  * (token-major, the o_proj input). kv_split > 0 cuts each 128-row query tile's key range into at most
  * kv_chunks chunks of at least kv_split 128-key tiles, computed by separate CTAs and merged by
@@ -227,22 +275,33 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
  * per query tile, d_work unused. d_err (may be NULL) receives bit 2 if a bounded wait gave up. */
 QWEN3_API size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int kv_chunks);
 QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
-                               int T, int Hq, int Hkv, int dh, int cap, const int* d_len0, int kv_split,
-                               int kv_chunks, void* d_work, void* d_out, int* d_err, void* stream);
+                               int T, int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
+                               int window, int ring, int kv_split, int kv_chunks, void* d_work, void* d_out,
+                               int* d_err, void* stream);
 
 /* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.
- * d_work is caller scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap) bytes. */
-QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap);
+ * d_seq_meta, window and ring as for qwen3_op_attention_prefill (padding slots are skipped, a window
+ * keeps the last `window` slots, a ring wraps). d_work is caller scratch of
+ * qwen3_attention_decode_workspace(B, Hq, dh, cap, window) bytes. */
+QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window);
 QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
-                              int Hq, int Hkv, int dh, int cap, const int* d_len0, void* d_work,
-                              void* d_out, void* stream);
+                              int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
+                              int window, int ring, void* d_work, void* d_out, void* stream);
+
+/* Greedy next token ("A modern architecture: Qwen3", generation): next[b] = the index of the largest
+ * of the V fp32 logits in row b (row stride ld floats; the lowest index on ties, a NaN counting as the
+ * largest, as torch.argmax). With stop_id >= 0 and d_done (int [B], device): a row with done[b] != 0
+ * emits stop_id, and done[b] becomes 1 once the row emits stop_id. V % 4 == 0, ld % 4 == 0, logits
+ * 16-byte aligned. */
+QWEN3_API int qwen3_op_greedy(const float* d_logits, int64_t ld, int B, int V, int stop_id, int32_t* d_done,
+                              int32_t* d_next, void* stream);
 
 /* Allocation-free variant of qwen3_op_attention_decode, for callers that cannot call cudaMalloc:
  * code whose device memory belongs to another allocator (for example a framework's caching pool),
  * code that must not trigger the device-wide synchronisation an allocation can cause, and code that
  * may not allocate once it has started. Same arguments and result as qwen3_op_attention_decode,
- * minus the workspace: the split partials go to a fixed array compiled into this library,
+ * minus the workspace and the sequence layout (plain causal sequences only): the split partials go to a fixed array compiled into this library,
  * QWEN3_DECODE_NOALLOC_MAX_BYTES (16 MiB) large, which every GPU that loads the library holds until
  * the process exits. A call whose workspace (qwen3_attention_decode_workspace) is larger returns
  * QWEN3_E_ARG and launches nothing. The call allocates nothing itself. Its first call on each device

@@ -74,16 +74,18 @@ def greedy(logits, done, stop_id: int):
 
 
 def generate(model, prompts, max_new: int, stop_id: int, prefix=None, capacity: int | None = None,
-             forced=None, keep=False):
+             forced=None, keep=False, pad_id: int | None = None):
     """Greedy generation for a batch of prompts of different lengths.
 
     Returns (rows, steps): rows = each row's generated ids cut at its first stop id; steps = list of
     dicts per forward call with the logits [B, V], the ids fed, the positions and the cache column.
     ``forced`` (list of [B] arrays) replaces the fed ids of decode step k (teacher forcing) without
-    changing the recorded greedy choices. With ``keep`` the final cache is returned in steps[-1]."""
+    changing the recorded greedy choices. With ``keep`` the final cache is returned in steps[-1].
+    Padding uses the stop id, as the pages do, unless ``pad_id`` is given (needed when stop_id < 0
+    means "no stop id")."""
     B = len(prompts)
     start = 0 if prefix is None else prefix["length"]
-    ids, real, positions, mask = left_pad(prompts, stop_id, start)
+    ids, real, positions, mask = left_pad(prompts, stop_id if pad_id is None else pad_id, start)
     width = ids.shape[1]
     cap = capacity or (start + width + max_new)
     kc, vc = model.new_cache(B, cap)

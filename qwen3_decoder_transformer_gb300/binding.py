@@ -29,13 +29,15 @@ class Qwen3Error(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "vocab",
-        "tie_embeddings", "max_positions")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+        "tie_embeddings", "max_positions")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                                               ("sliding_window", ctypes.c_int32), ("rolling_cache", ctypes.c_int32)]
 
     @classmethod
     def from_dict(cls, c: dict) -> "Config":
         return cls(c["n_layers"], c["hidden"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"],
                    c["intermediate"], c["vocab"], int(c["tie_embeddings"]), c.get("max_positions", 40960),
-                   float(c["rope_theta"]), float(c["rms_eps"]))
+                   float(c["rope_theta"]), float(c["rms_eps"]), int(c.get("sliding_window", 0)),
+                   int(c.get("rolling_cache", 0)))
 
 
 _LAYER = ("in_norm", "q_proj", "k_proj", "v_proj", "o_proj", "q_norm", "k_norm", "post_norm", "gate_proj",
@@ -85,12 +87,17 @@ def lib() -> ctypes.CDLL:
     L.qwen3_op_rope_table.argtypes = [ctypes.c_float, i, i, _vp, _vp]
     L.qwen3_op_qknorm_rope_append.argtypes = [_vp, i, i, i, i, i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                               _vp, i, _vp]
-    L.qwen3_op_attention_prefill.argtypes = [_vp, _vp, _vp, i, i, i, i, i, i, _vp, i, i, _vp, _vp, _vp, _vp]
+    L.qwen3_op_attention_prefill.argtypes = [_vp, _vp, _vp, i, i, i, i, i, i, _vp, _vp, i, i, i, i, _vp, _vp, _vp,
+                                             _vp]
     L.qwen3_attention_prefill_workspace.restype = sz
     L.qwen3_attention_prefill_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_attention_decode_workspace.restype = sz
-    L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i]
-    L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp, _vp]
+    L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i, i]
+    L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, i, i, _vp, _vp, _vp]
+    L.qwen3_op_greedy.argtypes = [_vp, ctypes.c_int64, i, i, i, _vp, _vp, _vp]
+    L.qwen3_prefill_padded.argtypes = [_vp, _vp, _i32p, i, i, _vp, i, _vp]
+    L.qwen3_share_prefix.argtypes = [_vp, i, _vp]
+    L.qwen3_generate.argtypes = [_vp, _vp, _i32p, i, i, i, i, _vp, _i32p, _vp]
     _lib = L
     return L
 
@@ -176,6 +183,25 @@ class Model:
         B, T = ids.shape
         check(lib().qwen3_prefill(self.ctx, _p(ids), B, T, _p(logits), ALL_ROWS if all_rows else 0,
                                   _stream(stream)))
+
+    def prefill_padded(self, ids: torch.Tensor, real, logits: torch.Tensor, all_rows: bool = False, stream=None):
+        """ids [B, T] left-padded; real[b] = number of real tokens at the end of row b."""
+        B, T = ids.shape
+        r = (ctypes.c_int32 * B)(*[int(x) for x in real])
+        check(lib().qwen3_prefill_padded(self.ctx, _p(ids), r, B, T, _p(logits), ALL_ROWS if all_rows else 0,
+                                         _stream(stream)))
+
+    def share_prefix(self, batch: int, stream=None):
+        check(lib().qwen3_share_prefix(self.ctx, batch, _stream(stream)))
+
+    def generate(self, ids: torch.Tensor, real, max_new: int, stop_id: int, out: torch.Tensor, stream=None) -> int:
+        """Greedy generation; out [B, max_new] int32 receives the tokens. Returns the columns written."""
+        B, T = ids.shape
+        r = (ctypes.c_int32 * B)(*[int(x) for x in real]) if real is not None else None
+        steps = ctypes.c_int32()
+        check(lib().qwen3_generate(self.ctx, _p(ids), r, B, T, max_new, stop_id, _p(out), ctypes.byref(steps),
+                                   _stream(stream)))
+        return steps.value
 
     def decode_step(self, ids: torch.Tensor, logits: torch.Tensor, stream=None):
         check(lib().qwen3_decode_step(self.ctx, _p(ids), ids.shape[0], _p(logits), _stream(stream)))
@@ -271,19 +297,27 @@ def attention_prefill_workspace(B, T, Hq, Hkv, dh, kv_chunks) -> int:
     return lib().qwen3_attention_prefill_workspace(B, T, Hq, Hkv, dh, kv_chunks)
 
 
-def op_attention_prefill(q, k_cache, v_cache, len0, out, err=None, kv_split=0, kv_chunks=1, work=None, stream=None):
+def op_attention_prefill(q, k_cache, v_cache, len0, out, err=None, kv_split=0, kv_chunks=1, work=None,
+                         seq_meta=None, window=0, ring=0, stream=None):
     B, Hq, T, dh = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
     check(lib().qwen3_op_attention_prefill(_p(q), _p(k_cache), _p(v_cache), B, T, Hq, Hkv, dh, cap, _p(len0),
-                                           kv_split, kv_chunks, _p(work), _p(out), _p(err), _stream(stream)))
+                                           _p(seq_meta), window, ring, kv_split, kv_chunks, _p(work), _p(out), _p(err),
+                                           _stream(stream)))
 
 
-def attention_decode_workspace(B, Hq, dh, cap) -> int:
-    return lib().qwen3_attention_decode_workspace(B, Hq, dh, cap)
+def attention_decode_workspace(B, Hq, dh, cap, window=0) -> int:
+    return lib().qwen3_attention_decode_workspace(B, Hq, dh, cap, window)
 
 
-def op_attention_decode(q, k_cache, v_cache, len0, work, out, stream=None):
+def op_attention_decode(q, k_cache, v_cache, len0, work, out, seq_meta=None, window=0, ring=0, stream=None):
     B, Hq, dh = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
     check(lib().qwen3_op_attention_decode(_p(q), _p(k_cache), _p(v_cache), B, Hq, Hkv, dh, cap, _p(len0),
-                                          _p(work), _p(out), _stream(stream)))
+                                          _p(seq_meta), window, ring, _p(work), _p(out), _stream(stream)))
+
+
+def op_greedy(logits, next_ids, stop_id=-1, done=None, stream=None):
+    B, V = logits.shape
+    check(lib().qwen3_op_greedy(_p(logits), logits.stride(0), B, V, stop_id, _p(done), _p(next_ids),
+                                _stream(stream)))

@@ -56,8 +56,9 @@ template <int DH, int NH>
 __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv,
-                           const int* __restrict__ len0p, __nv_bfloat16* __restrict__ out, int* err, int split,
-                           int max_chunks, float* __restrict__ ws, int* __restrict__ tickets) {
+                           const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
+                           __nv_bfloat16* __restrict__ out, int* err, int split, int max_chunks,
+                           float* __restrict__ ws, int* __restrict__ tickets) {
     using Ly = TcLayout<DH, NH>;
     constexpr int NCH = Ly::NCH;
     constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
@@ -117,14 +118,25 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     pdl_wait();  // Q and the cache come from the previous kernel
     pdl_trigger();
     const int len0 = *len0p;
+    // sequence layout: padding slots [ps, pe) of this sequence, slots below psh read from sequence 0
+    int ps = 0, pe = 0, psh = 0;
+    if (meta) {
+        ps = meta[0];
+        psh = meta[1];
+        pe = ps + meta[kSeqMetaHead + b];
+    }
     const int n_valid = len0 + q_end;
-    const int n_tiles = (n_valid + TC_BN - 1) / TC_BN;
+    const int n_end = (n_valid + TC_BN - 1) / TC_BN;
+    // a sliding window starts at the tile holding the first query's oldest visible key
+    const int j_lo = window > 0 ? max(0, len0 + q0 - window + 1) / TC_BN : 0;
+    const int n_tiles = n_end - j_lo;
     // KV range of this CTA: the whole causal range, or one chunk of it (split > 0: chunks of at least
     // `split` tiles, at most max_chunks of them, merged by the last CTA of the query tile to finish)
     const int chunk_tiles = split > 0 ? max(split, (n_tiles + max_chunks - 1) / max_chunks) : n_tiles;
     const int n_chunks = (n_tiles + chunk_tiles - 1) / chunk_tiles;
-    const int j0 = chunk * chunk_tiles;
-    const int nt = chunk < n_chunks ? min(n_tiles, j0 + chunk_tiles) - j0 : 0;  // tiles of this CTA
+    const int jc = chunk * chunk_tiles;  // first tile of this chunk, relative to j_lo
+    const int j0 = j_lo + jc;
+    const int nt = chunk < n_chunks ? min(n_tiles, jc + chunk_tiles) - jc : 0;  // tiles of this CTA
 
     if (warp == 0) {
         if (lane == 0 && nt > 0) {
@@ -136,14 +148,16 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             for (int i = 0; i < nt; ++i) {
                 const int s = i & 1, j = j0 + i;
                 if (!mbar_wait(&kv_empty[s], ((i >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                // cache row of the tile (a rolling buffer wraps) and its sequence (a shared prefix
+                // lives in sequence 0)
+                const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
+                const int z = (j * TC_BN < psh ? 0 : b) * Hkv + jkv;
                 mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmK, &k_full[s], c * 64,
-                                j * TC_BN, b * Hkv + jkv);
+                    tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmK, &k_full[s], c * 64, y, z);
                 mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmV, &v_full[s], c * 64,
-                                j * TC_BN, b * Hkv + jkv);
+                    tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmV, &v_full[s], c * 64, y, z);
             }
         }
     } else if (warp == 1 && nt > 0) {
@@ -228,11 +242,20 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             tmem_ld_wait();
             const int k0 = j * TC_BN;
             float mx = -INFINITY;
-            if (k0 + TC_BN - 1 > len0 + q0) {  // tile crosses the diagonal: mask keys past pos
+            // keys to mask in this tile (decided for the whole CTA): past the diagonal, padding of
+            // this sequence, or older than some row's window
+            const bool diag = k0 + TC_BN - 1 > len0 + q0;
+            const bool pads = k0 < pe && k0 + TC_BN > ps;
+            const bool old = window > 0 && k0 < len0 + q_end - window;
+            if (diag || pads || old) {
+                // key i is visible iff (i <= lim, not padding, inside the window) or it is the query itself
                 const int lim = pos - k0;
+                const int lo = window > 0 ? lim - window + 1 : -TC_BN;
+                const int pl = ps - k0, ph = pe - k0;
 #pragma unroll
                 for (int i = 0; i < TC_BN; ++i) {
-                    const float v = i <= lim ? __uint_as_float(sr[i]) : -INFINITY;
+                    const bool vis = (i <= lim && i >= lo && (i < pl || i >= ph)) || i == lim;
+                    const float v = vis ? __uint_as_float(sr[i]) : -INFINITY;
                     sr[i] = __float_as_uint(v);
                     mx = fmaxf(mx, v);
                 }
@@ -398,7 +421,8 @@ template <int DH, int G>
 __global__ void __launch_bounds__(DEC_THREADS)
     attn_decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                              const __nv_bfloat16* __restrict__ vc, int Hq, int Hkv, int cap,
-                             const int* __restrict__ len0p, float* __restrict__ work) {
+                             const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
+                             float* __restrict__ work) {
     constexpr int LPK = DH / 8;   // lanes per key row (16-byte pieces)
     constexpr int KPW = 32 / LPK;  // keys per warp per step
     constexpr int KPS = KPW * (DEC_THREADS / 32);  // keys per block step
@@ -412,7 +436,9 @@ __global__ void __launch_bounds__(DEC_THREADS)
     const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int nsplit = gridDim.x;
     const int n = *len0p + 1;
-    const int s0 = split * DEC_CHUNK, s1 = min(n, s0 + DEC_CHUNK);
+    // keys [lo, n): a sliding window keeps the last `window`; chunks are aligned to DEC_CHUNK slots
+    const int lo = window > 0 ? max(0, n - window) : 0;
+    const int s0 = lo / DEC_CHUNK * DEC_CHUNK + split * DEC_CHUNK, s1 = min(n, s0 + DEC_CHUNK);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPK, li = lane % LPK;
     float* wb = work + (((size_t)b * Hq + (size_t)j * G) * nsplit + split) * REC;
@@ -423,7 +449,17 @@ __global__ void __launch_bounds__(DEC_THREADS)
         }
         return;
     }
-    const size_t kvbase = (((size_t)b * Hkv + j) * cap) * DH;
+    // padding slots [ps, pe) of this sequence; slots below psh live in sequence 0; a rolling buffer
+    // stores slot s at s mod ring (ring a multiple of DEC_CHUNK, so a chunk stays contiguous)
+    int ps = 0, pe = 0, psh = 0;
+    if (meta) {
+        ps = meta[0];
+        psh = meta[1];
+        pe = ps + meta[kSeqMetaHead + b];
+    }
+    const ptrdiff_t shift = ring ? (ptrdiff_t)(s0 % ring) - s0 : 0;
+    const ptrdiff_t kv_own = (ptrdiff_t)(((size_t)b * Hkv + j) * cap) * DH + shift * DH;
+    const ptrdiff_t kv_shared = (ptrdiff_t)((size_t)j * cap) * DH + shift * DH;
     const float sl2 = kLog2e / sqrtf((float)DH);
     float qv[G][8];
 #pragma unroll
@@ -442,7 +478,8 @@ __global__ void __launch_bounds__(DEC_THREADS)
 #pragma unroll
         for (int u = 0; u < DEC_UNROLL; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
-            kv[u] = s < s1 ? *reinterpret_cast<const uint4*>(kc + kvbase + (size_t)s * DH + li * 8)
+            kv[u] = s < s1 ? *reinterpret_cast<const uint4*>(kc + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH +
+                                                              li * 8)
                            : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -463,8 +500,9 @@ __global__ void __launch_bounds__(DEC_THREADS)
                 d[h] = acc;
             }
             if (li == 0 && s < s1) {
+                const bool vis = s >= lo && (s < ps || s >= pe);  // outside the window, or padding
 #pragma unroll
-                for (int h = 0; h < G; ++h) sc[h][s - s0] = d[h];
+                for (int h = 0; h < G; ++h) sc[h][s - s0] = vis ? d[h] : -INFINITY;
             }
         }
     }
@@ -478,7 +516,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float sum = 0.f;
         for (int i = lane; i < cnt; i += 32) {
-            const float e = exp2f(sc[h][i] - mx);
+            const float e = mx == -INFINITY ? 0.f : exp2f(sc[h][i] - mx);  // a chunk with no visible key
             sc[h][i] = e;
             sum += e;
         }
@@ -501,7 +539,8 @@ __global__ void __launch_bounds__(DEC_THREADS)
 #pragma unroll
         for (int u = 0; u < DEC_UNROLL; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
-            vv[u] = s < s1 ? *reinterpret_cast<const uint4*>(vc + kvbase + (size_t)s * DH + li * 8)
+            vv[u] = s < s1 ? *reinterpret_cast<const uint4*>(vc + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH +
+                                                              li * 8)
                            : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -573,24 +612,32 @@ __global__ void attn_decode_combine_kernel(const float* __restrict__ work, int H
     out[((size_t)b * Hq + h) * DH + d] = __float2bfloat16_rn(acc / L);
 }
 
+// Chunks per (sequence, kv head): enough to cover every slot, or a window's keys at any alignment.
+int decode_nsplit(int cap, int window) {
+    const int all = (cap + DEC_CHUNK - 1) / DEC_CHUNK;
+    return window > 0 ? std::min(all, (window + DEC_CHUNK - 1) / DEC_CHUNK + 1) : all;
+}
+
 template <int DH, int G>
 cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                            int Hkv, int cap, const int* len0, float* work, __nv_bfloat16* out, cudaStream_t st) {
-    const int nsplit = (cap + DEC_CHUNK - 1) / DEC_CHUNK;
+                            int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
+                            cudaStream_t st) {
+    const int nsplit = decode_nsplit(cap, sm.window);
     cudaError_t e = launch_pdl(attn_decode_split_kernel<DH, G>, dim3(nsplit, Hkv, B), dim3(DEC_THREADS), 0, st, q, kc, vc,
-                               Hq, Hkv, cap, len0, work);
+                               Hq, Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, out);
 }
 
 template <int DH>
 cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                             int Hkv, int cap, const int* len0, float* work, __nv_bfloat16* out, cudaStream_t st) {
+                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
+                             cudaStream_t st) {
     switch (Hq / Hkv) {
-        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
-        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
-        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
-        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
+        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -604,21 +651,21 @@ size_t attn_tickets_floats(int B, int T, int Hq, int Hkv) {
 
 template <int DH, int NH>
 cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int B, int T, int Hq,
-                              int Hkv, const int* len0, __nv_bfloat16* out, int* err, int split, int max_chunks,
-                              float* ws, cudaStream_t st) {
+                              int Hkv, const int* len0, SeqMap sm, __nv_bfloat16* out, int* err, int split,
+                              int max_chunks, float* ws, cudaStream_t st) {
     using Ly = TcLayout<DH, NH>;
     const int n_qt = (T + TC_BM - 1) / TC_BM;
     dim3 grid(n_qt * max_chunks, Hq / NH, B);
     int* tickets = reinterpret_cast<int*>(ws);
     float* parts = ws ? ws + attn_tickets_floats(B, T, Hq, Hkv) : nullptr;
     return launch_pdl(attn_prefill_tc_kernel<DH, NH>, grid, dim3(Ly::THREADS), Ly::SMEM, st, tq, tk, tv, T, Hq, Hkv, len0,
-                      out, err, split, max_chunks, parts, tickets);
+                      sm.meta, sm.window, sm.ring, out, err, split, max_chunks, parts, tickets);
 }
 
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                              int Hq, int Hkv, int cap, const int* len0, __nv_bfloat16* out, int* err, int split,
-                              int max_chunks, float* ws, cudaStream_t st) {
+                              int Hq, int Hkv, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out, int* err,
+                              int split, int max_chunks, float* ws, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
@@ -630,19 +677,21 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
     // Two heads per CTA share each K/V tile (measured faster than one head per CTA even when the
     // grid is smaller than the SM count).
     if ((Hq / Hkv) % 2 == 0)
-        return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, split, max_chunks, ws, st);
-    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, out, err, split, max_chunks, ws, st);
+        return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
+    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
 }
 
 }  // namespace
 
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
-                                int split, int max_chunks, float* ws, cudaStream_t st) {
+                                int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
+                                int* err, int split, int max_chunks, float* ws, cudaStream_t st) {
     if (B <= 0 || T <= 0) return cudaSuccess;
+    if (sm.ring && (sm.ring % 256 || sm.ring != cap)) return cudaErrorInvalidValue;
     if (dh == 128)
-        return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, split, max_chunks, ws, st);
-    if (dh == 64) return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, out, err, split, max_chunks, ws, st);
+        return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, st);
+    if (dh == 64)
+        return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, st);
     return cudaErrorInvalidValue;
 }
 
@@ -672,17 +721,18 @@ void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* spl
     }
 }
 
-size_t attn_decode_workspace(int B, int Hq, int dh, int cap) {
-    const size_t nsplit = (size_t)(cap + DEC_CHUNK - 1) / DEC_CHUNK;
+size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window) {
+    const size_t nsplit = (size_t)decode_nsplit(cap, window);
     return (size_t)B * Hq * nsplit * (dh + 2) * sizeof(float);
 }
 
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                               int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,
+                               int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                                cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
-    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
-    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, work, out, st);
+    if (sm.ring && (sm.ring % DEC_CHUNK || sm.ring != cap)) return cudaErrorInvalidValue;
+    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
     return cudaErrorInvalidValue;
 }
 

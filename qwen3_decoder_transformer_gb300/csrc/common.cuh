@@ -249,4 +249,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Position of cache slot s in a sequence whose left padding occupies slots [ps, ps + pad): the
+// count of real tokens before it (the padding sits at the position of the last token before it).
+__device__ __forceinline__ int slot_position(int s, int ps, int pad) {
+    return s < ps ? s : (s < ps + pad ? max(ps - 1, 0) : s - pad);
+}
+
 }  // namespace q3

@@ -233,7 +233,9 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
     const QkvRopeArgs& q = a.qkv;
     const int row = m0 + r;
     const bool row_ok = row < a.M;
-    const bool staged = (q.T % BM) == 0;
+    const int len0 = *q.len0;
+    // whole 128-row blocks go out by TMA, unless a rolling buffer could wrap inside the block
+    const bool staged = (q.T % BM) == 0 && (!q.rolling || len0 % BM == 0);
     const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
     constexpr int HALF = DH / 2;
     constexpr int NHEAD = BN / DH;
@@ -246,8 +248,9 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
         }
         tc_fence_after();
     }
-    const int len0 = *q.len0;
-    const int pos = len0 + t;
+    const int slot = len0 + t;
+    const int pos = q.meta ? slot_position(slot, q.meta[0], q.meta[kSeqMetaHead + b]) : slot;
+    const int phys = q.rolling ? slot % q.cap : slot;
 #pragma unroll 1
     for (int lh = 0; lh < NHEAD; ++lh) {
         const int hg = n0 / DH + lh;
@@ -309,7 +312,7 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
             if (threadIdx.x == EPI_LEADER) {
                 const int bt = m0 / q.T, t0 = m0 % q.T;
                 const CUtensorMap* map = kind == 0 ? tmQ : (kind == 1 ? tmK : tmV);
-                const int y = kind == 0 ? t0 : len0 + t0;
+                const int y = kind == 0 ? t0 : (q.rolling ? (len0 + t0) % q.cap : len0 + t0);
                 const int z = kind == 0 ? bt * q.Hq + hg : bt * q.Hkv + (kind == 1 ? hg - q.Hq : hg - q.Hq - q.Hkv);
 #pragma unroll
                 for (int c = 0; c < DH / 64; ++c) tma_store_3d(map, stg + c * 16384, c * 64, y, z);
@@ -317,8 +320,8 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
             }
         } else if (row_ok) {
             __nv_bfloat16* dst = kind == 0 ? q.q_out + (((size_t)b * q.Hq + hg) * q.T + t) * DH
-                               : kind == 1 ? q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + pos) * DH
-                                           : q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + pos) * DH;
+                               : kind == 1 ? q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + phys) * DH
+                                           : q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + phys) * DH;
 #pragma unroll
             for (int u = 0; u < DH / 8; ++u)
                 reinterpret_cast<uint4*>(dst)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);

@@ -45,12 +45,28 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
 // Extra operands of EPI_QKV_ROPE: the accumulator row of a QKV tile is one token's q/k/v head
 // vectors; the epilogue applies q_norm/k_norm and RoPE and writes Q [B, Hq, T, dh] and the cache.
 struct QkvRopeArgs {
-    const __nv_bfloat16 *q_gamma, *k_gamma, *table;  // table [cap][dh]: cos then sin per position
-    const int* len0;                                  // device cache length (first position)
+    const __nv_bfloat16 *q_gamma, *k_gamma, *table;  // table [positions][dh]: cos then sin per position
+    const int* len0;                                  // device cache length (first new slot)
     __nv_bfloat16 *q_out, *k_cache, *v_cache;        // caches [B][Hkv][cap][dh]
-    int T, Hq, Hkv, dh, cap;
+    int T, Hq, Hkv, dh, cap;                          // cap: physical slots per (sequence, kv head)
     float eps;
+    const int* meta;  // sequence layout (SeqMap::meta), or null
+    int rolling;      // nonzero: slot s is stored at s mod cap (cap a multiple of 256)
 };
+// Layout of each sequence's cache, read by the kernels that place or read keys:
+//   meta (device ints, null for plain equal-length sequences): meta[0] = ps, the first padding slot;
+//   meta[1] = psh, slots below it are read from sequence 0's cache (a multiple of 128, shared
+//   prefix); meta[2 + b] = the number of padding slots of sequence b, [ps, ps + pad_b).
+//   Slot s of sequence b holds position s below ps, max(ps - 1, 0) in the padding, s - pad_b after it.
+//   A query in slot q sees key slot k iff (k <= q, k is not padding and, with a window W > 0,
+//   q - k < W) or k == q.
+//   ring: 0 = slot s is stored at s; otherwise at s mod ring (rolling buffer).
+struct SeqMap {
+    const int* meta;
+    int window;
+    int ring;
+};
+constexpr int kSeqMetaHead = 2;
 struct GemmArgs {
     int M, N, K;
     int epi;
@@ -119,8 +135,14 @@ cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, _
 cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, int Hq, int Hkv, int dh, const __nv_bfloat16* qg,
                                           const __nv_bfloat16* kg, const __nv_bfloat16* table, const int* len0,
                                           float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap,
-                                          cudaStream_t st);
+                                          const int* meta, int rolling, cudaStream_t st);
 // Length bookkeeping on the device: *len = value, or *len += delta.
+// Greedy next tokens of B rows of logits (row stride ld floats); see greedy_kernel. done/next/out/alive
+// may be null (done null: no stop handling).
+cudaError_t greedy_launch(const float* logits, long long ld, int B, int V, int stop_id, int* done, int* next, int* out,
+                          long long out_ld, int out_col, int* alive, cudaStream_t st);
+cudaError_t copy_prefix_slots_launch(__nv_bfloat16* kc, __nv_bfloat16* vc, size_t layer_elems, int L, int nb, int Hkv,
+                                     int cap, int dh, int s0, int s1, cudaStream_t st);
 cudaError_t set_len_launch(int* len, int value, cudaStream_t st);
 cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 
@@ -128,14 +150,15 @@ cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 // split > 0: cut each query tile's KV range into at most max_chunks chunks of >= split tiles, merged by
 // the last CTA to finish; ws then holds attn_prefill_workspace() bytes whose leading ticket counters
 // are zero on entry (each launch leaves them zero).
+// cap: physical slots per (sequence, kv head); sm: sequence layout (SeqMap{} for plain sequences).
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
-                                int Hq, int Hkv, int dh, int cap, const int* len0, __nv_bfloat16* out, int* err,
-                                int split, int max_chunks, float* ws, cudaStream_t st);
+                                int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
+                                int* err, int split, int max_chunks, float* ws, cudaStream_t st);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
-size_t attn_decode_workspace(int B, int Hq, int dh, int cap);
+size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window);
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                               int Hkv, int dh, int cap, const int* len0, float* work, __nv_bfloat16* out,
+                               int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                                cudaStream_t st);
 int attn_decode_kernel_count();
 // Allocation-free decode attention: size of the library's fixed scratch, and its device address on

@@ -120,7 +120,8 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
                                           int Hq, int Hkv, const __nv_bfloat16* __restrict__ qg,
                                           const __nv_bfloat16* __restrict__ kg, const __nv_bfloat16* __restrict__ table,
                                           const int* __restrict__ len0p, float eps, __nv_bfloat16* __restrict__ q_out,
-                                          __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, int cap) {
+                                          __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, int cap,
+                                          const int* __restrict__ meta, int rolling) {
     pdl_wait();
     pdl_trigger();
     constexpr int E = DH / 32;  // 2 or 4 features per lane
@@ -132,7 +133,9 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
     const int hh = (int)(w % H);
     const long long m = w / H;
     const int b = (int)(m / T), t = (int)(m % T);
-    const int pos = *len0p + t;
+    const int slot = *len0p + t;
+    const int pos = meta ? slot_position(slot, meta[0], meta[kSeqMetaHead + b]) : slot;
+    const int phys = rolling ? slot % cap : slot;  // cache slot: a rolling buffer wraps
 
     uint32_t raw[E / 2];
     if constexpr (F32_SRC) {
@@ -158,7 +161,7 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
         }
     }
     if (hh >= Hq + Hkv) {  // V: copied into the cache unchanged
-        __nv_bfloat16* dst = vc + (((size_t)b * Hkv + (hh - Hq - Hkv)) * cap + pos) * DH + lane * E;
+        __nv_bfloat16* dst = vc + (((size_t)b * Hkv + (hh - Hq - Hkv)) * cap + phys) * DH + lane * E;
         if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(raw[0], raw[1]);
         else *reinterpret_cast<uint32_t*>(dst) = raw[0];
         return;
@@ -198,7 +201,7 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
     }
     __nv_bfloat16* dst;
     if (is_q) dst = q_out + (((size_t)b * Hq + hh) * T + t) * DH + lane * E;
-    else dst = kc + (((size_t)b * Hkv + (hh - Hq)) * cap + pos) * DH + lane * E;
+    else dst = kc + (((size_t)b * Hkv + (hh - Hq)) * cap + phys) * DH + lane * E;
     if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
     else *reinterpret_cast<uint32_t*>(dst) = o[0];
 }
@@ -303,6 +306,86 @@ __global__ void add_len_kernel(int* len, int delta) {
     *len += delta;
 }
 
+// Greedy next token ("A modern architecture: Qwen3", generation: argmax of the last row's logits):
+// one CTA per row finds the largest logit, the lowest index on ties, a NaN counting as the largest
+// (torch.argmax's rule). With stop_id >= 0 a finished row emits stop_id, and a row that emits it is
+// finished; `alive` counts the rows still running after this step.
+constexpr int GREEDY_THREADS = 512;
+__device__ __forceinline__ bool greedy_better(float v, int i, float bv, int bi) {
+    const bool nv = v != v, nb = bv != bv;
+    if (nv != nb) return nv;
+    if (nv) return i < bi;
+    return v > bv || (v == bv && i < bi);
+}
+__global__ void __launch_bounds__(GREEDY_THREADS)
+    greedy_kernel(const float* __restrict__ logits, long long ld, int V, int stop_id, int* __restrict__ done,
+                  int* __restrict__ next, int* __restrict__ out, long long out_ld, int out_col, int* __restrict__ alive) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x;
+    const float* row = logits + (size_t)b * ld;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = threadIdx.x * 4; i < V; i += GREEDY_THREADS * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(row + i);
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (greedy_better(e[k], i + k, bv, bi)) {
+                bv = e[k];
+                bi = i + k;
+            }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (greedy_better(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+        }
+    }
+    __shared__ float sv[GREEDY_THREADS / 32];
+    __shared__ int si[GREEDY_THREADS / 32];
+    if ((threadIdx.x & 31) == 0) {
+        sv[threadIdx.x >> 5] = bv;
+        si[threadIdx.x >> 5] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < GREEDY_THREADS / 32; ++w)
+            if (greedy_better(sv[w], si[w], bv, bi)) {
+                bv = sv[w];
+                bi = si[w];
+            }
+        if (bi >= V) bi = 0;  // every logit was -inf: the first index, as argmax returns
+        int tok = bi;
+        if (stop_id >= 0 && done) {
+            const int was = done[b];
+            if (was) tok = stop_id;
+            const int fin = was || tok == stop_id;
+            done[b] = fin;
+            if (alive && !fin) atomicAdd(alive, 1);
+        }
+        if (next) next[b] = tok;
+        if (out) out[(size_t)b * out_ld + out_col] = tok;
+    }
+}
+
+// Shared prefix: copy cache slots [s0, s1) of sequence 0 into sequences 1..nb-1, every layer and kv
+// head, K and V (the part of a shared prefix that does not fill a whole 128-slot tile).
+__global__ void copy_prefix_slots_kernel(__nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
+                                         size_t layer_elems, int Hkv, int cap, int dh, int s0, int s1) {
+    const int j = blockIdx.x, bdst = blockIdx.y + 1, l = blockIdx.z;
+    const size_t src = (size_t)l * layer_elems + ((size_t)j * cap + s0) * dh;
+    const size_t dst = (size_t)l * layer_elems + (((size_t)bdst * Hkv + j) * cap + s0) * dh;
+    const int n = (s1 - s0) * dh / 8;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        reinterpret_cast<uint4*>(kc + dst)[i] = reinterpret_cast<const uint4*>(kc + src)[i];
+        reinterpret_cast<uint4*>(vc + dst)[i] = reinterpret_cast<const uint4*>(vc + src)[i];
+    }
+}
+
 }  // namespace
 
 cudaError_t embed_launch(const __nv_bfloat16* E, int V, int d, const int32_t* ids, int M, __nv_bfloat16* out, int* err,
@@ -351,12 +434,13 @@ cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, in
     const int threads = 256, wpb = threads / 32;
     const unsigned blocks = (unsigned)((warps + wpb - 1) / wpb);
     const float* nows = nullptr;
+    const int* nometa = nullptr;
     if (dh == 128)
         return launch_pdl(qknorm_rope_append_kernel<128, false>, dim3(blocks), dim3(threads), 0, st, qkv, nows, 1, B, T, Hq,
-                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap, nometa, 0);
     if (dh == 64)
         return launch_pdl(qknorm_rope_append_kernel<64, false>, dim3(blocks), dim3(threads), 0, st, qkv, nows, 1, B, T, Hq,
-                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+                          Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap, nometa, 0);
     return cudaErrorInvalidValue;
 }
 
@@ -388,7 +472,7 @@ cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, _
 cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, int Hq, int Hkv, int dh,
                                           const __nv_bfloat16* qg, const __nv_bfloat16* kg, const __nv_bfloat16* table,
                                           const int* len0, float eps, __nv_bfloat16* q_out, __nv_bfloat16* kc,
-                                          __nv_bfloat16* vc, int cap, cudaStream_t st) {
+                                          __nv_bfloat16* vc, int cap, const int* meta, int rolling, cudaStream_t st) {
     const long long warps = (long long)B * (Hq + 2 * Hkv);
     if (warps <= 0) return cudaSuccess;
     const int threads = 256, wpb = threads / 32;
@@ -396,11 +480,26 @@ cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, in
     const __nv_bfloat16* noq = nullptr;
     if (dh == 128)
         return launch_pdl(qknorm_rope_append_kernel<128, true>, dim3(blocks), dim3(threads), 0, st, noq, ws, splits, B, 1,
-                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap, meta, rolling);
     if (dh == 64)
         return launch_pdl(qknorm_rope_append_kernel<64, true>, dim3(blocks), dim3(threads), 0, st, noq, ws, splits, B, 1,
-                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap);
+                          Hq, Hkv, qg, kg, table, len0, eps, q_out, kc, vc, cap, meta, rolling);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t greedy_launch(const float* logits, long long ld, int B, int V, int stop_id, int* done, int* next, int* out,
+                          long long out_ld, int out_col, int* alive, cudaStream_t st) {
+    if (B <= 0) return cudaSuccess;
+    if (V < 1 || V % 4 || ld % 4) return cudaErrorInvalidValue;
+    return launch_pdl(greedy_kernel, dim3(B), dim3(GREEDY_THREADS), 0, st, logits, ld, V, stop_id, done, next, out,
+                      out_ld, out_col, alive);
+}
+
+cudaError_t copy_prefix_slots_launch(__nv_bfloat16* kc, __nv_bfloat16* vc, size_t layer_elems, int L, int nb, int Hkv,
+                                     int cap, int dh, int s0, int s1, cudaStream_t st) {
+    if (nb <= 1 || s1 <= s0) return cudaSuccess;
+    copy_prefix_slots_kernel<<<dim3(Hkv, nb - 1, L), 256, 0, st>>>(kc, vc, layer_elems, Hkv, cap, dh, s0, s1);
+    return cudaGetLastError();
 }
 
 }  // namespace q3

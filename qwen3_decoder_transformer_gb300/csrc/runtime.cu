@@ -77,6 +77,8 @@ cudaError_t prepare_kernels() {
 struct qwen3_ctx {
     qwen3_config cfg;
     int max_batch = 0, capacity = 0, max_tokens = 0;
+    // physical cache slots per (sequence, kv head): capacity, or the rolling buffer's ring
+    int slots = 0, window = 0, ring = 0;
     int qkv_n = 0, q_width = 0;
     // borrowed weights
     const bf16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
@@ -92,6 +94,14 @@ struct qwen3_ctx {
     size_t attn_ws_bytes = 0;
     int* d_len = nullptr;
     int* d_err = nullptr;
+    // sequence layout (SeqMap::meta): [ps, psh, pad[0..max_batch)], with its host mirror
+    int* d_seq = nullptr;
+    std::vector<int> h_seq;
+    bool padded = false;
+    // greedy generation state: logits of the last rows, finished flags, next ids, running count
+    float* gen_logits = nullptr;
+    int *gen_done = nullptr, *gen_next = nullptr, *gen_alive = nullptr;
+    int* h_alive = nullptr;  // pinned
     int32_t* d_ids_buf = nullptr;
     float* d_logits_buf = nullptr;
     size_t logits_buf_elems = 0;
@@ -168,6 +178,7 @@ int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, co
 }
 
 bf16* layer_k(qwen3_ctx* c, int l) { return c->kcache + (size_t)l * c->layer_elems; }
+SeqMap seq_map(const qwen3_ctx* c) { return SeqMap{c->d_seq, c->window, c->ring}; }
 bf16* layer_v(qwen3_ctx* c, int l) { return c->vcache + (size_t)l * c->layer_elems; }
 
 int skinny(qwen3_ctx* c, int cls, const CUtensorMap& tw, const CUtensorMap& tx, int M, int N, int K, float* out,
@@ -194,11 +205,11 @@ int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
             return qknorm_rope_append_f32_launch(c->skinny_ws, s_qkv, B, g.n_q_heads, g.n_kv_heads, dh, c->q_norm[l],
                                                  c->k_norm[l], c->rope, c->d_len, g.rms_eps, c->q, layer_k(c, l),
-                                                 layer_v(c, l), c->capacity, st);
+                                                 layer_v(c, l), c->slots, c->d_seq, c->ring != 0, st);
         }));
         TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
             return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                      c->capacity, c->d_len, c->dec_work, c->attn, st);
+                                      c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, st);
         }));
         TRY(skinny(c, K_GEMM_O, c->tB_o[l], c->tX_attn, B, d, c->q_width, nullptr, s_o, st));
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
@@ -245,7 +256,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             // fused: Q/K/V projection, q_norm/k_norm, RoPE, Q to attention layout, K/V into the cache
             GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, nullptr, 0, nullptr, 0, c->d_err,
                        QkvRopeArgs{c->q_norm[l], c->k_norm[l], c->rope, c->d_len, c->q, layer_k(c, l), layer_v(c, l), T,
-                                   g.n_q_heads, g.n_kv_heads, dh, c->capacity, g.rms_eps}};
+                                   g.n_q_heads, g.n_kv_heads, dh, c->slots, g.rms_eps, c->d_seq, c->ring != 0}};
             GemmMaps m;
             std::memset(&m, 0, sizeof(m));
             m.a = c->tA_xn;
@@ -258,7 +269,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         if (decode) {
             TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
                 return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                          c->capacity, c->d_len, c->dec_work, c->attn, st);
+                                          c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, st);
             }));
         } else {
             int split = 0, chunks = 1;
@@ -269,7 +280,8 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             }
             TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
                 return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
-                                           c->capacity, c->d_len, c->attn, c->d_err, split, chunks, c->attn_ws, st);
+                                           c->slots, c->d_len, seq_map(c), c->attn, c->d_err, split, chunks,
+                                           c->attn_ws, st);
             }));
         }
         TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
@@ -303,6 +315,8 @@ int check_call(qwen3_ctx* c, int B, int T) {
     if (B > c->max_batch || (long long)B * T > c->max_tokens) return QWEN3_E_BATCH;
     if (c->len > 0 && B != c->batch) return QWEN3_E_BATCH;
     if ((long long)c->len + T > c->capacity) return QWEN3_E_OVERFLOW;
+    // a rolling buffer holds the window plus one call's tokens
+    if (c->ring && T > c->ring - c->window + 1) return QWEN3_E_BATCH;
     return QWEN3_OK;
 }
 
@@ -324,10 +338,34 @@ void release(qwen3_ctx* c) {
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
                     c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->skinny_ws, c->d_len,
-                    c->d_err, c->d_ids_buf, c->d_logits_buf};
+                    c->d_err, c->d_ids_buf, c->d_logits_buf, c->d_seq, c->gen_logits, c->gen_done, c->gen_next,
+                    c->gen_alive};
     for (void* p : bufs)
         if (p) cudaFree(p);
+    if (c->h_alive) cudaFreeHost(c->h_alive);
     delete c;
+}
+
+// Replace the device copy of the sequence layout (from pageable host memory: the copy is staged
+// before cudaMemcpyAsync returns, so `v` may go away at once).
+int write_seq(qwen3_ctx* c, const std::vector<int>& v, cudaStream_t st) {
+    if (cudaMemcpyAsync(c->d_seq, v.data(), v.size() * sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return QWEN3_E_CUDA;
+    c->h_seq = v;
+    return QWEN3_OK;
+}
+
+// Buffers of the greedy generation loop, allocated on first use.
+int ensure_generation_buffers(qwen3_ctx* c) {
+    if (c->gen_logits) return QWEN3_OK;
+    const size_t mb = (size_t)c->max_batch;
+    if (dmalloc(&c->gen_logits, mb * c->cfg.vocab) != cudaSuccess || dmalloc(&c->gen_done, mb) != cudaSuccess ||
+        dmalloc(&c->gen_next, mb) != cudaSuccess || dmalloc(&c->gen_alive, 1) != cudaSuccess ||
+        cudaMallocHost(reinterpret_cast<void**>(&c->h_alive), sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
 }
 
 }  // namespace
@@ -361,6 +399,8 @@ int qwen3_validate_config(const qwen3_config* g) {
     if (g->head_dim != 64 && g->head_dim != 128) return QWEN3_E_CONFIG;
     if (g->hidden % 64 || g->intermediate % 128 || g->vocab % 8 || g->hidden > 8192) return QWEN3_E_CONFIG;
     if (!(g->rms_eps > 0.f) || !(g->rope_theta > 1.f)) return QWEN3_E_CONFIG;
+    if (g->sliding_window < 0 || (g->rolling_cache != 0 && g->rolling_cache != 1)) return QWEN3_E_CONFIG;
+    if (g->rolling_cache && g->sliding_window < 1) return QWEN3_E_CONFIG;
     return QWEN3_OK;
 }
 
@@ -394,6 +434,17 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
         return QWEN3_E_ARG;
     }
     c->max_tokens = (int)mt;
+    c->window = g->sliding_window;
+    if (g->rolling_cache) {
+        // ring of W + (one sequence's share of a call) - 1 slots, a multiple of 256: no token of a call
+        // overwrites a key that another token of the same call still sees (longer calls are refused)
+        const long long chunk = std::min<long long>((mt + max_batch - 1) / max_batch, capacity);
+        const long long need = (long long)g->sliding_window + chunk - 1;
+        c->ring = (int)((need + 255) / 256 * 256);
+        c->slots = c->ring;
+    } else {
+        c->slots = capacity;
+    }
     const int L = g->n_layers, d = g->hidden, dh = g->head_dim, F = g->intermediate, V = g->vocab;
     c->q_width = g->n_q_heads * dh;
     c->qkv_n = (g->n_q_heads + 2 * g->n_kv_heads) * dh;
@@ -409,7 +460,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
         c->o_proj.push_back(static_cast<const bf16*>(w->o_proj[l]));
         c->down_proj.push_back(static_cast<const bf16*>(w->down_proj[l]));
     }
-    c->layer_elems = (size_t)max_batch * g->n_kv_heads * capacity * dh;
+    c->layer_elems = (size_t)max_batch * g->n_kv_heads * c->slots * dh;
     const size_t rows = (size_t)c->max_tokens;
     // The A-operand buffers get at least one full 128-row tile so TMA boxes stay inside them.
     const size_t arows = rows < 128 ? 128 : rows;
@@ -422,8 +473,9 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
               dmalloc(&c->q, rows * c->q_width) == cudaSuccess &&
               dmalloc(&c->attn, arows * c->q_width) == cudaSuccess && dmalloc(&c->h, arows * F) == cudaSuccess &&
               dmalloc(&c->hn, arows * d) == cudaSuccess &&
-              dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, capacity) / 4) ==
+              dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, c->slots, c->window) / 4) ==
                   cudaSuccess &&
+              dmalloc(&c->d_seq, (size_t)kSeqMetaHead + max_batch) == cudaSuccess &&
               dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
               dmalloc(&c->d_ids_buf, rows) == cudaSuccess;
     // decode split-K workspace: the largest [splits][64][N] fp32 set of slices over the four projections
@@ -455,6 +507,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          cudaMemsetAsync(c->h, 0, arows * F * 2, st) == cudaSuccess &&
          cudaMemsetAsync(c->hn, 0, arows * d * 2, st) == cudaSuccess &&
          cudaMemsetAsync(c->d_len, 0, sizeof(int), st) == cudaSuccess &&
+         cudaMemsetAsync(c->d_seq, 0, ((size_t)kSeqMetaHead + max_batch) * sizeof(int), st) == cudaSuccess &&
          cudaMemsetAsync(c->d_err, 0, sizeof(int), st) == cudaSuccess;
     for (int l = 0; ok && l < L; ++l) {
         bf16* dst = c->wqkv + (size_t)l * c->qkv_n * d;
@@ -480,9 +533,9 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
     c->tK3.resize(L);
     c->tV3.resize(L);
     for (int l = 0; ok && l < L; ++l)
-        ok = encode_tmap_bf16_3d(&c->tK3[l], c->kcache + (size_t)l * c->layer_elems, dh, capacity,
+        ok = encode_tmap_bf16_3d(&c->tK3[l], c->kcache + (size_t)l * c->layer_elems, dh, c->slots,
                                  (uint64_t)max_batch * g->n_kv_heads) &&
-             encode_tmap_bf16_3d(&c->tV3[l], c->vcache + (size_t)l * c->layer_elems, dh, capacity,
+             encode_tmap_bf16_3d(&c->tV3[l], c->vcache + (size_t)l * c->layer_elems, dh, c->slots,
                                  (uint64_t)max_batch * g->n_kv_heads);
     c->tB_qkv.resize(L);
     c->tB_o.resize(L);
@@ -503,6 +556,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
         release(c);
         return QWEN3_E_CUDA;
     }
+    c->h_seq.assign((size_t)kSeqMetaHead + max_batch, 0);
     *out = c;
     return QWEN3_OK;
 }
@@ -548,6 +602,91 @@ int qwen3_decode_step(qwen3_ctx* c, const int32_t* d_ids, int B, float* d_logits
     return QWEN3_OK;
 }
 
+int qwen3_prefill_padded(qwen3_ctx* c, const int32_t* d_ids, const int32_t* h_real, int B, int T, float* d_logits,
+                         int flags, void* stream) {
+    if (!c || !d_ids || !h_real || !d_logits) return QWEN3_E_ARG;
+    TRY(check_call(c, B, T));
+    if (c->window > 0) return QWEN3_E_ARG;  // padding and sliding windows are not combined
+    std::vector<int> v = c->h_seq;
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        if (h_real[b] < 1 || h_real[b] > T) return QWEN3_E_ARG;
+        any |= T - h_real[b];
+    }
+    if (any && c->padded) return QWEN3_E_ARG;  // one padded block per fill of the cache
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (any) {
+        v[0] = c->len;
+        for (int b = 0; b < c->max_batch; ++b) v[kSeqMetaHead + b] = b < B ? T - h_real[b] : 0;
+        TRY(write_seq(c, v, st));
+        c->padded = true;
+    }
+    TRY(enqueue_forward(c, d_ids, B, T, d_logits, flags, false, st));
+    c->len += T;
+    c->batch = B;
+    return QWEN3_OK;
+}
+
+int qwen3_share_prefix(qwen3_ctx* c, int B, void* stream) {
+    if (!c) return QWEN3_E_ARG;
+    if (B < 1 || B > c->max_batch) return QWEN3_E_BATCH;
+    if (c->batch != 1 || c->len < 1 || c->padded || c->window > 0 || c->h_seq[1] > 0) return QWEN3_E_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int psh = c->len / 128 * 128;  // whole 128-slot tiles are read from sequence 0 in place
+    if (copy_prefix_slots_launch(c->kcache, c->vcache, c->layer_elems, c->cfg.n_layers, B, c->cfg.n_kv_heads, c->slots,
+                                 c->cfg.head_dim, psh, c->len, st) != cudaSuccess)
+        return QWEN3_E_CUDA;
+    std::vector<int> v = c->h_seq;
+    v[1] = psh;
+    TRY(write_seq(c, v, st));
+    c->batch = B;
+    return QWEN3_OK;
+}
+
+int qwen3_generate(qwen3_ctx* c, const int32_t* d_ids, const int32_t* h_real, int B, int T, int max_new, int stop_id,
+                   int32_t* d_out, int* h_steps, void* stream) {
+    if (!c || !d_ids || !d_out || max_new < 1) return QWEN3_E_ARG;
+    if (stop_id >= c->cfg.vocab) return QWEN3_E_ARG;
+    if (c->len + T + max_new - 1 > c->capacity) return QWEN3_E_OVERFLOW;
+    TRY(ensure_generation_buffers(c));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int V = c->cfg.vocab;
+    if (h_real) {
+        TRY(qwen3_prefill_padded(c, d_ids, h_real, B, T, c->gen_logits, 0, stream));
+    } else {
+        TRY(qwen3_prefill(c, d_ids, B, T, c->gen_logits, 0, stream));
+    }
+    if (cudaMemsetAsync(c->gen_done, 0, (size_t)B * sizeof(int), st) != cudaSuccess) return QWEN3_E_CUDA;
+    int steps = 0;
+    for (;;) {
+        if (cudaMemsetAsync(c->gen_alive, 0, sizeof(int), st) != cudaSuccess) return QWEN3_E_CUDA;
+        if (greedy_launch(c->gen_logits, V, B, V, stop_id, stop_id >= 0 ? c->gen_done : nullptr, c->gen_next, d_out,
+                          max_new, steps, c->gen_alive, st) != cudaSuccess)
+            return QWEN3_E_CUDA;
+        ++steps;
+        if (steps == max_new) break;
+        if (stop_id >= 0) {  // stop once every row has finished
+            if (cudaMemcpyAsync(c->h_alive, c->gen_alive, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+                cudaStreamSynchronize(st) != cudaSuccess)
+                return QWEN3_E_CUDA;
+            if (*c->h_alive == 0) break;
+        }
+        TRY(qwen3_decode_step(c, c->gen_next, B, c->gen_logits, stream));
+    }
+    if (h_steps) *h_steps = steps;
+    return QWEN3_OK;
+}
+
+int qwen3_op_greedy(const float* logits, int64_t ld, int B, int V, int stop_id, int32_t* done, int32_t* next,
+                    void* stream) {
+    if (!logits || !next || B < 0 || V < 4 || V % 4 || ld < V || ld % 4 || !is_aligned(logits, 16)) return QWEN3_E_ARG;
+    if (stop_id >= V) return QWEN3_E_ARG;
+    return greedy_launch(logits, ld, B, V, stop_id, stop_id >= 0 ? done : nullptr, next, nullptr, 0, 0, nullptr,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QWEN3_OK
+               : QWEN3_E_CUDA;
+}
+
 int qwen3_prefill_host(qwen3_ctx* c, const int32_t* h_ids, int B, int T, float* h_logits, int flags, void* stream) {
     if (!c || !h_ids || !h_logits) return QWEN3_E_ARG;
     TRY(check_call(c, B, T));
@@ -583,6 +722,9 @@ int qwen3_set_length(qwen3_ctx* c, int length, int batch, void* stream) {
     if (set_len_launch(c->d_len, length, static_cast<cudaStream_t>(stream)) != cudaSuccess) return QWEN3_E_CUDA;
     c->len = length;
     c->batch = batch;
+    // the cache now holds plain equal-length sequences: no padding, no shared prefix
+    TRY(write_seq(c, std::vector<int>(c->h_seq.size(), 0), static_cast<cudaStream_t>(stream)));
+    c->padded = false;
     return QWEN3_OK;
 }
 
@@ -593,7 +735,7 @@ int qwen3_kv_view(qwen3_ctx* c, int layer, void** d_k, void** d_v, int64_t dims[
     if (dims) {
         dims[0] = c->max_batch;
         dims[1] = c->cfg.n_kv_heads;
-        dims[2] = c->capacity;
+        dims[2] = c->slots;
         dims[3] = c->cfg.head_dim;
     }
     return QWEN3_OK;
@@ -760,31 +902,39 @@ size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, 
 }
 
 int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, int B, int T, int Hq, int Hkv, int dh,
-                               int cap, const int* len0, int kv_split, int kv_chunks, void* work, void* out, int* err,
-                               void* stream) {
+                               int cap, const int* len0, const int* seq_meta, int window, int ring, int kv_split,
+                               int kv_chunks, void* work, void* out, int* err, void* stream) {
     if (!q || !kc || !vc || !len0 || !out || B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (dh != 64 && dh != 128) || cap < 1 || kv_split < 0 || kv_chunks > 64 || (kv_split > 0 && !work))
         return QWEN3_E_ARG;
+    if (window < 0 || (ring && (ring != cap || ring % 256 || window < 1))) return QWEN3_E_ARG;
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
-                               B, T, Hq, Hkv, dh, cap, len0, static_cast<bf16*>(out), err, kv_split,
+                               B, T, Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<bf16*>(out),
+                               err, kv_split,
                                kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work),
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
 }
 
-size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap) { return attn_decode_workspace(B, Hq, dh, cap); }
+size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window) {
+    if (B < 1 || Hq < 1 || cap < 1 || window < 0) return 0;
+    return attn_decode_workspace(B, Hq, dh, cap, window);
+}
 
 int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh, int cap,
-                              const int* len0, void* work, void* out, void* stream) {
+                              const int* len0, const int* seq_meta, int window, int ring, void* work, void* out,
+                              void* stream) {
     if (!q || !kc || !vc || !len0 || !work || !out || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (dh != 64 && dh != 128) || cap < 1)
         return QWEN3_E_ARG;
+    if (window < 0 || (ring && (ring != cap || ring % 256 || window < 1))) return QWEN3_E_ARG;
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
-                              Hq, Hkv, dh, cap, len0, static_cast<float*>(work), static_cast<bf16*>(out),
+                              Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<float*>(work),
+                              static_cast<bf16*>(out),
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
@@ -797,11 +947,11 @@ int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void*
         return QWEN3_E_ARG;
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
-    if (attn_decode_workspace(B, Hq, dh, cap) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
+    if (attn_decode_workspace(B, Hq, dh, cap, 0) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
     float* scratch = nullptr;
     if (attn_decode_noalloc_scratch(&scratch) != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
-                              Hq, Hkv, dh, cap, len0, scratch, static_cast<bf16*>(out),
+                              Hq, Hkv, dh, cap, len0, SeqMap{}, scratch, static_cast<bf16*>(out),
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
