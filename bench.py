@@ -457,13 +457,17 @@ def run_op(args, wl):
     len0 = torch.zeros(1, dtype=torch.int32, device="cuda")
     M = B * T
     if args.op == "attn_prefill":
-        q, kc, vc = rnd(B, hq, T, dh), rnd(B, hkv, T, dh), rnd(B, hkv, T, dh)
+        if args.rows:  # a prefill chunk of `rows` tokens after `len0` cached ones
+            T, M = args.rows, B * args.rows
+        len0.fill_(args.len0)
+        q, kc, vc = rnd(B, hq, T, dh), rnd(B, hkv, T + args.len0, dh), rnd(B, hkv, T + args.len0, dh)
         out = torch.empty(M, hq * dh, dtype=torch.bfloat16, device="cuda")
         split, chunks = args.kv_split, max(1, args.kv_chunks)
         ws = torch.zeros(max(1, binding.attention_prefill_workspace(B, T, hq, hkv, dh, chunks) // 4),
                          dtype=torch.float32, device="cuda")
-        fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out, kv_split=split, kv_chunks=chunks, work=ws)
-        work, unit, bound = 4.0 * B * hq * dh * T * (T + 1) / 2, "TFLOP/s", "tensor"
+        fn = lambda: binding.op_attention_prefill(q, kc, vc, len0, out, kv_split=split, kv_chunks=chunks, work=ws,
+                                                  heads_per_cta=args.heads)
+        work, unit, bound = 4.0 * B * hq * dh * (T * (T + 1) / 2 + T * args.len0), "TFLOP/s", "tensor"
     elif args.op == "attn_decode":
         Bd, ctx = args.rows or wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
         q, kc, vc = rnd(Bd, hq, dh), rnd(Bd, hkv, ctx + 8, dh), rnd(Bd, hkv, ctx + 8, dh)
@@ -742,6 +746,8 @@ def main():
                     help="time a generation feature on its own workload instead of the step")
     ap.add_argument("--kv-split", type=int, default=0, help="--op attn_prefill: minimum tiles per KV chunk")
     ap.add_argument("--kv-chunks", type=int, default=1, help="--op attn_prefill: maximum KV chunks per query tile")
+    ap.add_argument("--heads", type=int, default=0, help="--op attn_prefill: query heads per CTA (0 = automatic)")
+    ap.add_argument("--len0", type=int, default=0, help="--op attn_prefill: cached tokens before the chunk")
     ap.add_argument("--rows", type=int, default=0,
                     help="row count for --op gemm_*/rmsnorm (default B*T), batch for --op attn_decode")
     args = ap.parse_args()

@@ -266,7 +266,8 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
  * qwen3_share_prefix build it: ints [ps, psh, pad_0 .. pad_{B-1}]; slots [ps, ps + pad_b) of sequence b
  * are seen only by themselves, slots below psh (a multiple of 128) are read from sequence 0.
  * window > 0 restricts slot i to keys j > i - window; ring > 0 (= cap, a multiple of 256, with a
- * window) reads slot s from cache row s mod ring.
+ * window) reads slot s from cache row s mod ring. heads_per_cta: query heads of one kv group per CTA (1 or 2,
+ * 2 needs an even group size; 0 = the forward pass's choice).
  * q [B, Hq, T, dh]; caches [B, Hkv, cap, dh] with len0 + T <= cap; out [B*T, Hq*dh] bf16
  * (token-major, the o_proj input). kv_split > 0 cuts each 128-row query tile's key range into at most
  * kv_chunks chunks of at least kv_split 128-key tiles, computed by separate CTAs and merged by
@@ -276,8 +277,8 @@ QWEN3_API int qwen3_op_qknorm_rope_append(const void* d_qkv, int B, int T, int H
 QWEN3_API size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int kv_chunks);
 QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                                int T, int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
-                               int window, int ring, int kv_split, int kv_chunks, void* d_work, void* d_out,
-                               int* d_err, void* stream);
+                               int window, int ring, int heads_per_cta, int kv_split, int kv_chunks, void* d_work,
+                               void* d_out, int* d_err, void* stream);
 
 /* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.

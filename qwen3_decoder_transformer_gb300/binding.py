@@ -87,8 +87,8 @@ def lib() -> ctypes.CDLL:
     L.qwen3_op_rope_table.argtypes = [ctypes.c_float, i, i, _vp, _vp]
     L.qwen3_op_qknorm_rope_append.argtypes = [_vp, i, i, i, i, i, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                               _vp, i, _vp]
-    L.qwen3_op_attention_prefill.argtypes = [_vp, _vp, _vp, i, i, i, i, i, i, _vp, _vp, i, i, i, i, _vp, _vp, _vp,
-                                             _vp]
+    L.qwen3_op_attention_prefill.argtypes = [_vp, _vp, _vp, i, i, i, i, i, i, _vp, _vp, i, i, i, i, i, _vp, _vp,
+                                             _vp, _vp]
     L.qwen3_attention_prefill_workspace.restype = sz
     L.qwen3_attention_prefill_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_attention_decode_workspace.restype = sz
@@ -298,12 +298,12 @@ def attention_prefill_workspace(B, T, Hq, Hkv, dh, kv_chunks) -> int:
 
 
 def op_attention_prefill(q, k_cache, v_cache, len0, out, err=None, kv_split=0, kv_chunks=1, work=None,
-                         seq_meta=None, window=0, ring=0, stream=None):
+                         seq_meta=None, window=0, ring=0, heads_per_cta=0, stream=None):
     B, Hq, T, dh = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
     check(lib().qwen3_op_attention_prefill(_p(q), _p(k_cache), _p(v_cache), B, T, Hq, Hkv, dh, cap, _p(len0),
-                                           _p(seq_meta), window, ring, kv_split, kv_chunks, _p(work), _p(out), _p(err),
-                                           _stream(stream)))
+                                           _p(seq_meta), window, ring, heads_per_cta, kv_split, kv_chunks, _p(work),
+                                           _p(out), _p(err), _stream(stream)))
 
 
 def attention_decode_workspace(B, Hq, dh, cap, window=0) -> int:

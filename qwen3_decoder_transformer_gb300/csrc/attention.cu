@@ -22,15 +22,19 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // --------------------------------------------------------------------------- prefill (tcgen05)
-// One CTA = 128 query rows of NH query heads that share one kv head (NH = 2 when the group size
-// allows), so every K/V tile is loaded once for both heads. Warps:
-//   warp 0          TMA: the NH Q tiles once, then K_j / V_j tiles (128 keys) into a 2-stage ring.
-//   warp 1          TMEM owner and MMA issuer. Per head h: S_h = Q_h K_j^T into 128 fp32 TMEM
-//                   columns; softmax overwrites the first 64 of them with P_h as packed bf16; then
-//                   O_h += P_h V_j reads P_h straight from TMEM (A operand in tensor memory) and V_j as
-//                   an MN-major shared-memory operand. Order per tile: PV_0, S_0(next), PV_1, S_1(next),
-//                   so one head's scores are computed while the other head's softmax runs. The MMA
-//                   pipe executes in issue order, which makes S_h(next) overwriting P_h safe.
+// One CTA = 128 query rows of NH query heads that share one kv head. Tensor memory holds two
+// 128-column score regions and NH 128-column output accumulators. Warps:
+//   warp 0          TMA: the NH Q tiles once, then K_j / V_j tiles (128 keys) into 2-stage rings; a K
+//                   stage is refilled as soon as its scores are done, a V stage once its PV is done.
+//   warp 1          TMEM owner and MMA issuer. S = Q_h K_j^T into a score region (128 fp32 columns);
+//                   softmax overwrites its first 64 columns with P as packed bf16; then O_h += P V_j
+//                   reads P straight from TMEM (A operand in tensor memory) and V_j as an MN-major
+//                   shared-memory operand. The MMA pipe executes in issue order, which makes a later
+//                   S overwriting an earlier P safe.
+//                   NH = 2: one region per head; order per tile PV_0, S_0(next), PV_1, S_1(next), so
+//                   one head's scores are computed while the other head's softmax runs.
+//                   NH = 1: the two regions alternate between tiles, and the scores of tile j+1 are
+//                   computed while the softmax of tile j runs (S_{j+2} is issued right after PV_j).
 //   warps 2..2+4NH  softmax, four warps per head; thread r owns query row r (TMEM lane r). Online
 //                   softmax in base 2 with lazy rescaling: O and l are rescaled only when the running
 //                   max grows by more than 8 (so P <= 256). At the end each thread normalises its row.
@@ -71,12 +75,13 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;    // [2]
     uint64_t* v_full = bars + 3;    // [2]
-    uint64_t* kv_empty = bars + 5;  // [2]
-    uint64_t* s_full = bars + 7;    // [NH]
-    uint64_t* p_full = bars + 9;    // [NH]
-    uint64_t* o_done = bars + 11;   // [NH]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+    uint64_t* k_empty = bars + 5;   // [2]
+    uint64_t* v_empty = bars + 7;   // [2]
+    uint64_t* s_full = bars + 9;    // [2] per score region
+    uint64_t* p_full = bars + 11;   // [2] per score region
+    uint64_t* o_done = bars + 13;   // [NH]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
     volatile int* merge_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,13 +98,12 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
         }
-        for (int hh = 0; hh < NH; ++hh) {
-            mbar_init(&s_full[hh], 1);
-            mbar_init(&p_full[hh], 128);
-            mbar_init(&o_done[hh], 1);
-        }
+        for (int hh = 0; hh < NH; ++hh) mbar_init(&o_done[hh], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -129,13 +133,21 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     const int n_end = (n_valid + TC_BN - 1) / TC_BN;
     // a sliding window starts at the tile holding the first query's oldest visible key
     const int j_lo = window > 0 ? max(0, len0 + q0 - window + 1) / TC_BN : 0;
-    const int n_tiles = n_end - j_lo;
+    // tiles [ja, jb) lie wholly inside this sequence's padding and below every query of the block:
+    // no row sees any of their keys, so they are skipped
+    const int ja = max(j_lo, (ps + TC_BN - 1) / TC_BN);
+    const int jb = max(ja, min(pe / TC_BN, (len0 + q0) / TC_BN));
+    const int n_tiles = n_end - j_lo - (jb - ja);
+    // absolute KV tile of the i-th live tile (counted from j_lo)
+    auto tile_of_live = [&](int i) { return j_lo + i < ja ? j_lo + i : j_lo + i + (jb - ja); };
+    // score region of head hh at this CTA's tile i, and how many earlier tiles used it (barrier phase)
+    auto s_region = [](int hh, int i) { return NH == 2 ? hh : (i & 1); };
+    auto s_use = [](int i) { return NH == 2 ? i : (i >> 1); };
     // KV range of this CTA: the whole causal range, or one chunk of it (split > 0: chunks of at least
     // `split` tiles, at most max_chunks of them, merged by the last CTA of the query tile to finish)
     const int chunk_tiles = split > 0 ? max(split, (n_tiles + max_chunks - 1) / max_chunks) : n_tiles;
     const int n_chunks = (n_tiles + chunk_tiles - 1) / chunk_tiles;
-    const int jc = chunk * chunk_tiles;  // first tile of this chunk, relative to j_lo
-    const int j0 = j_lo + jc;
+    const int jc = chunk * chunk_tiles;  // first live tile of this chunk
     const int nt = chunk < n_chunks ? min(n_tiles, jc + chunk_tiles) - jc : 0;  // tiles of this CTA
 
     if (warp == 0) {
@@ -146,15 +158,17 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                     tma_load_3d(smem + Ly::Q_OFF + hh * Ly::Q_BYTES + c * TC_BM * 128, &tmQ, q_full, c * 64, q0,
                                 b * Hq + h0 + hh);
             for (int i = 0; i < nt; ++i) {
-                const int s = i & 1, j = j0 + i;
-                if (!mbar_wait(&kv_empty[s], ((i >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const int s = i & 1, j = tile_of_live(jc + i);
+                const uint32_t free_ph = ((i >> 1) & 1) ^ 1;
                 // cache row of the tile (a rolling buffer wraps) and its sequence (a shared prefix
                 // lives in sequence 0)
                 const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
                 const int z = (j * TC_BN < psh ? 0 : b) * Hkv + jkv;
+                if (!mbar_wait(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
                 mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmK, &k_full[s], c * 64, y, z);
+                if (!mbar_wait(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
                 mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + c * TC_BN * 128, &tmV, &v_full[s], c * 64, y, z);
@@ -162,7 +176,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
         }
     } else if (warp == 1 && nt > 0) {
         // all lanes walk the schedule (so the warp can zero V tails together); lane 0 issues.
-        // i counts this CTA's tiles (barrier phases); j = j0 + i is the absolute KV tile.
+        // i counts this CTA's tiles (barrier phases); j = tile_of_live(jc + i) is the absolute KV tile.
         auto issue_s = [&](int hh, int i) -> bool {
             const int s = i & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (i >> 1) & 1, abort_flag))) return false;
@@ -170,21 +184,25 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             if (lane == 0) {
                 const uint32_t sq = smem_u32(smem + Ly::Q_OFF + hh * Ly::Q_BYTES);
                 const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
+                const int r = s_region(hh, i);
 #pragma unroll
                 for (int kk = 0; kk < DH / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
-                    umma_bf16_ss(tmem + hh * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), IDESC_S,
+                    umma_bf16_ss(tmem + r * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off), IDESC_S,
                                  kk > 0);
                 }
-                umma_commit(&s_full[hh]);
+                umma_commit(&s_full[r]);
+                if (hh == NH - 1) umma_commit(&k_empty[s]);  // K_i is no longer needed
             }
             __syncwarp();
             return true;
         };
         ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+        // scores run ahead: tile 0 of both heads (NH = 2), or tiles 0 and 1 (NH = 1)
         for (int hh = 0; ok && hh < NH; ++hh) ok = issue_s(hh, 0);
+        if (NH == 1 && ok && nt > 1) ok = issue_s(0, 1);
         for (int i = 0; ok && i < nt; ++i) {
-            const int s = i & 1, j = j0 + i;
+            const int s = i & 1, j = tile_of_live(jc + i);
             if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (i >> 1) & 1, abort_flag))) { ok = false; break; }
             uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
             const int r0 = n_valid - j * TC_BN;  // first stale key row of this tile
@@ -198,20 +216,22 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             }
             __syncwarp();
             for (int hh = 0; ok && hh < NH; ++hh) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[hh], i & 1, abort_flag))) { ok = false; break; }
+                const int r = s_region(hh, i);
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[r], s_use(i) & 1, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t svv = smem_u32(sv);
 #pragma unroll
                     for (int kk = 0; kk < TC_BN / 16; ++kk) {
                         const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
-                        umma_bf16_ts(tmem + TM_O + hh * 128, tmem + hh * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
+                        umma_bf16_ts(tmem + TM_O + hh * 128, tmem + r * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
                     }
                     umma_commit(&o_done[hh]);
-                    if (hh == NH - 1) umma_commit(&kv_empty[s]);
+                    if (hh == NH - 1) umma_commit(&v_empty[s]);  // V_i is no longer needed
                 }
                 __syncwarp();
-                if (i + 1 < nt) ok = issue_s(hh, i + 1);
+                const int nxt = NH == 2 ? i + 1 : i + 2;  // the next tile whose scores go to region r
+                if (nxt < nt) ok = issue_s(hh, nxt);
             }
         }
     } else if (warp >= 2 && nt > 0) {
@@ -220,7 +240,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
         const int quarter = warp & 3, row = quarter * 32 + lane;
         const int t = q0 + row, pos = len0 + t;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tm_s = tmem + lane_off + hh * TC_BN, tm_o = tmem + lane_off + TM_O + hh * 128;
+        const uint32_t tm_o = tmem + lane_off + TM_O + hh * 128;
         const float sl2 = kLog2e / sqrtf((float)DH);
         float m_used = -INFINITY, l = 0.f;  // m_used in scaled (log2) units
         int pv_seen = 0;                    // PV completions confirmed so far
@@ -232,8 +252,10 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             return true;
         };
         for (int i = 0; i < nt; ++i) {
-            const int j = j0 + i;
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[hh], i & 1, abort_flag))) { ok = false; break; }
+            const int j = tile_of_live(jc + i);
+            const int r = s_region(hh, i);
+            const uint32_t tm_s = tmem + lane_off + r * TC_BN;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[r], s_use(i) & 1, abort_flag))) { ok = false; break; }
             tc_fence_after();
             uint32_t sr[TC_BN];
 #pragma unroll
@@ -241,28 +263,44 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 tmem_ld_32x32b_x32(tm_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_ld_wait();
             const int k0 = j * TC_BN;
-            float mx = -INFINITY;
+            // row max over 8 independent partial maxima (short dependency chains)
+            float mx8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
             // keys to mask in this tile (decided for the whole CTA): past the diagonal, padding of
             // this sequence, or older than some row's window
             const bool diag = k0 + TC_BN - 1 > len0 + q0;
             const bool pads = k0 < pe && k0 + TC_BN > ps;
             const bool old = window > 0 && k0 < len0 + q_end - window;
-            if (diag || pads || old) {
-                // key i is visible iff (i <= lim, not padding, inside the window) or it is the query itself
+            if (pads || old) {
+                // key i is visible iff (i <= lim, not padding, inside the window) or it is the query
+                // itself: two intervals, before and after the padding, plus the query's own slot.
+                // Branch-free (unsigned range tests): a short-circuit form diverges per element.
                 const int lim = pos - k0;
                 const int lo = window > 0 ? lim - window + 1 : -TC_BN;
-                const int pl = ps - k0, ph = pe - k0;
+                const int a1 = max(lo, 0), n1 = max(0, min(lim, ps - k0 - 1) - a1 + 1);
+                const int a2 = max(lo, pe - k0), n2 = max(0, lim - a2 + 1);
 #pragma unroll
                 for (int i = 0; i < TC_BN; ++i) {
-                    const bool vis = (i <= lim && i >= lo && (i < pl || i >= ph)) || i == lim;
+                    const bool vis = ((unsigned)(i - a1) < (unsigned)n1) | ((unsigned)(i - a2) < (unsigned)n2) | (i == lim);
                     const float v = vis ? __uint_as_float(sr[i]) : -INFINITY;
                     sr[i] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
+                    mx8[i & 7] = fmaxf(mx8[i & 7], v);
+                }
+            } else if (diag) {  // only the causal diagonal: keys past the query's slot
+                const int lim = pos - k0;
+#pragma unroll
+                for (int i = 0; i < TC_BN; ++i) {
+                    const float v = i <= lim ? __uint_as_float(sr[i]) : -INFINITY;
+                    sr[i] = __float_as_uint(v);
+                    mx8[i & 7] = fmaxf(mx8[i & 7], v);
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < TC_BN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+                for (int i = 0; i < TC_BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
             }
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= sl2;
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
@@ -289,7 +327,9 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region (a row
             // with no visible key yet keeps m = -inf and gets P = 0)
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            float rs = 0.f;
+            float rs8[8];  // row sum over 8 independent partial sums
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
@@ -297,13 +337,14 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 for (int e = 0; e < 32; ++e) {
                     const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
                     const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
-                    rs += p0 + p1;
+                    rs8[(2 * e) & 7] += p0;
+                    rs8[(2 * e + 1) & 7] += p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
                 tmem_st_32x32b_x32(tm_s + half * 32, pk);
             }
             tmem_st_wait();
-            l += rs;
+            l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             // Observe the previous P V completion before releasing this P: o_done is then never more
             // than one phase ahead of this thread, so its parity waits stay unambiguous.
             if (i > 0) {
@@ -311,7 +352,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
             tc_fence_before();
-            mbar_arrive(&p_full[hh]);
+            mbar_arrive(&p_full[r]);
         }
         // epilogue
         if (ok) ok = confirm_pv(nt);
@@ -442,13 +483,6 @@ __global__ void __launch_bounds__(DEC_THREADS)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPK, li = lane % LPK;
     float* wb = work + (((size_t)b * Hq + (size_t)j * G) * nsplit + split) * REC;
-    if (s0 >= n) {
-        if (threadIdx.x < G) {
-            wb[(size_t)threadIdx.x * nsplit * REC + 0] = -INFINITY;
-            wb[(size_t)threadIdx.x * nsplit * REC + 1] = 0.f;
-        }
-        return;
-    }
     // padding slots [ps, pe) of this sequence; slots below psh live in sequence 0; a rolling buffer
     // stores slot s at s mod ring (ring a multiple of DEC_CHUNK, so a chunk stays contiguous)
     int ps = 0, pe = 0, psh = 0;
@@ -456,6 +490,13 @@ __global__ void __launch_bounds__(DEC_THREADS)
         ps = meta[0];
         psh = meta[1];
         pe = ps + meta[kSeqMetaHead + b];
+    }
+    if (s0 >= n || (s0 >= ps && s1 <= pe)) {  // nothing to read, or only padding
+        if (threadIdx.x < G) {
+            wb[(size_t)threadIdx.x * nsplit * REC + 0] = -INFINITY;
+            wb[(size_t)threadIdx.x * nsplit * REC + 1] = 0.f;
+        }
+        return;
     }
     const ptrdiff_t shift = ring ? (ptrdiff_t)(s0 % ring) - s0 : 0;
     const ptrdiff_t kv_own = (ptrdiff_t)(((size_t)b * Hkv + j) * cap) * DH + shift * DH;
@@ -642,7 +683,6 @@ cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, co
     return cudaErrorInvalidValue;
 }
 
-int attn_heads_per_cta(int Hq, int Hkv) { return (Hq / Hkv) % 2 == 0 ? 2 : 1; }
 // Ticket counters (one int per work item), padded to 256 bytes, at the start of the workspace.
 size_t attn_tickets_floats(int B, int T, int Hq, int Hkv) {
     const size_t items = (size_t)((T + TC_BM - 1) / TC_BM) * (Hq / attn_heads_per_cta(Hq, Hkv)) * B;
@@ -665,7 +705,7 @@ cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, cons
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                               int Hq, int Hkv, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out, int* err,
-                              int split, int max_chunks, float* ws, cudaStream_t st) {
+                              int split, int max_chunks, float* ws, int heads, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
@@ -674,24 +714,28 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         split = 0;
         max_chunks = 1;
     }
-    // Two heads per CTA share each K/V tile (measured faster than one head per CTA even when the
-    // grid is smaller than the SM count).
-    if ((Hq / Hkv) % 2 == 0)
+    if (heads == 0) heads = attn_heads_per_cta(Hq, Hkv);
+    if (heads == 2 && (Hq / Hkv) % 2 == 0)
         return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
     return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
 }
 
 }  // namespace
 
+// Two heads of one kv group per CTA share every K/V tile load.
+int attn_heads_per_cta(int Hq, int Hkv) { return (Hq / Hkv) % 2 == 0 ? 2 : 1; }
+
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
-                                int* err, int split, int max_chunks, float* ws, cudaStream_t st) {
+                                int* err, int split, int max_chunks, float* ws, int heads, cudaStream_t st) {
     if (B <= 0 || T <= 0) return cudaSuccess;
     if (sm.ring && (sm.ring % 256 || sm.ring != cap)) return cudaErrorInvalidValue;
+    if (heads < 0 || heads > 2) return cudaErrorInvalidValue;
     if (dh == 128)
-        return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, st);
+        return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, heads,
+                                      st);
     if (dh == 64)
-        return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, st);
+        return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, heads, st);
     return cudaErrorInvalidValue;
 }
 

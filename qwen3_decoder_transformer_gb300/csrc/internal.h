@@ -67,6 +67,8 @@ struct SeqMap {
     int ring;
 };
 constexpr int kSeqMetaHead = 2;
+constexpr int kSeqChunk = 1000;  // ints per set_seq launch (carried as a kernel parameter)
+cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st);
 struct GemmArgs {
     int M, N, K;
     int epi;
@@ -153,7 +155,9 @@ cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 // cap: physical slots per (sequence, kv head); sm: sequence layout (SeqMap{} for plain sequences).
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
-                                int* err, int split, int max_chunks, float* ws, cudaStream_t st);
+                                int* err, int split, int max_chunks, float* ws, int heads, cudaStream_t st);
+// heads: query heads per CTA (1 or 2; 0 = attn_heads_per_cta).
+int attn_heads_per_cta(int Hq, int Hkv);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window);

@@ -1,3 +1,4 @@
+#include <algorithm>
 // Memory-bound kernels of the Qwen3 block: embedding gather, RMSNorm, the RoPE table, and the
 // fused q_norm/k_norm + RoPE + KV-cache append. Each reads and writes its rows once with 8- or
 // 16-byte vector accesses; one warp owns one row or one head vector.
@@ -372,6 +373,17 @@ __global__ void __launch_bounds__(GREEDY_THREADS)
     }
 }
 
+// Sequence layout update: writes n ints carried in the launch itself (no host buffer to keep alive,
+// stream-ordered like every other launch).
+struct SeqChunk {
+    int v[kSeqChunk];
+};
+__global__ void set_seq_kernel(int* __restrict__ dst, SeqChunk c, int n) {
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = c.v[i];
+}
+
 // Shared prefix: copy cache slots [s0, s1) of sequence 0 into sequences 1..nb-1, every layer and kv
 // head, K and V (the part of a shared prefix that does not fill a whole 128-slot tile).
 __global__ void copy_prefix_slots_kernel(__nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
@@ -493,6 +505,17 @@ cudaError_t greedy_launch(const float* logits, long long ld, int B, int V, int s
     if (V < 1 || V % 4 || ld % 4) return cudaErrorInvalidValue;
     return launch_pdl(greedy_kernel, dim3(B), dim3(GREEDY_THREADS), 0, st, logits, ld, V, stop_id, done, next, out,
                       out_ld, out_col, alive);
+}
+
+cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st) {
+    for (int i = 0; i < n; i += kSeqChunk) {
+        SeqChunk c;
+        const int k = std::min(kSeqChunk, n - i);
+        for (int j = 0; j < k; ++j) c.v[j] = vals[i + j];
+        cudaError_t e = launch_pdl(set_seq_kernel, dim3(1), dim3(256), 0, st, dst + i, c, k);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t copy_prefix_slots_launch(__nv_bfloat16* kc, __nv_bfloat16* vc, size_t layer_elems, int L, int nb, int Hkv,

@@ -121,7 +121,8 @@ struct qwen3_ctx {
     bool timing = false;
     std::vector<TimedLaunch> timed;
     std::vector<cudaEvent_t> free_events;
-    cudaStream_t last_timed = nullptr;
+    cudaStream_t last_timed = nullptr;  // may be the legacy default stream (null handle)
+    bool have_timed = false;
     // debug tap
     int tap_layer = -1;
     void *tap_in = nullptr, *tap_out = nullptr;
@@ -154,6 +155,7 @@ int timed(qwen3_ctx* c, int cls, int launches, cudaStream_t st, F&& fn) {
         cudaEventRecord(b, st);
         c->timed.push_back({cls, launches, a, b});
         c->last_timed = st;
+        c->have_timed = true;
     }
     return e == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
@@ -281,7 +283,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
                 return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
                                            c->slots, c->d_len, seq_map(c), c->attn, c->d_err, split, chunks,
-                                           c->attn_ws, st);
+                                           c->attn_ws, 0, st);
             }));
         }
         TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
@@ -346,11 +348,11 @@ void release(qwen3_ctx* c) {
     delete c;
 }
 
-// Replace the device copy of the sequence layout (from pageable host memory: the copy is staged
-// before cudaMemcpyAsync returns, so `v` may go away at once).
+// Replace the device copy of the sequence layout (values travel inside the update launches; nothing
+// is enqueued when the layout does not change).
 int write_seq(qwen3_ctx* c, const std::vector<int>& v, cudaStream_t st) {
-    if (cudaMemcpyAsync(c->d_seq, v.data(), v.size() * sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return QWEN3_E_CUDA;
+    if (v == c->h_seq) return QWEN3_OK;
+    if (set_seq_launch(c->d_seq, v.data(), (int)v.size(), st) != cudaSuccess) return QWEN3_E_CUDA;
     c->h_seq = v;
     return QWEN3_OK;
 }
@@ -775,10 +777,12 @@ int qwen3_kernel_times(qwen3_ctx* c, double* total_ms, int64_t* launches, int* n
         if (total_ms) total_ms[i] = 0;
         if (launches) launches[i] = 0;
     }
-    if (c->last_timed && cudaStreamSynchronize(c->last_timed) != cudaSuccess) return QWEN3_E_CUDA;
+    if (c->have_timed && cudaStreamSynchronize(c->last_timed) != cudaSuccess) return QWEN3_E_CUDA;
+    c->have_timed = false;
+    bool bad = false;
     for (auto& t : c->timed) {
         float ms = 0.f;
-        cudaEventElapsedTime(&ms, t.start, t.stop);
+        bad = bad || cudaEventElapsedTime(&ms, t.start, t.stop) != cudaSuccess;
         if (t.cls < cap) {
             if (total_ms) total_ms[t.cls] += ms;
             if (launches) launches[t.cls] += t.launches;
@@ -787,7 +791,7 @@ int qwen3_kernel_times(qwen3_ctx* c, double* total_ms, int64_t* launches, int* n
         c->free_events.push_back(t.stop);
     }
     c->timed.clear();
-    return QWEN3_OK;
+    return bad ? QWEN3_E_CUDA : QWEN3_OK;
 }
 
 const char* qwen3_kernel_class_name(int i) { return (i >= 0 && i < K_NUM_CLASSES) ? kClassNames[i] : nullptr; }
@@ -902,17 +906,18 @@ size_t qwen3_attention_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, 
 }
 
 int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, int B, int T, int Hq, int Hkv, int dh,
-                               int cap, const int* len0, const int* seq_meta, int window, int ring, int kv_split,
-                               int kv_chunks, void* work, void* out, int* err, void* stream) {
+                               int cap, const int* len0, const int* seq_meta, int window, int ring, int heads_per_cta,
+                               int kv_split, int kv_chunks, void* work, void* out, int* err, void* stream) {
     if (!q || !kc || !vc || !len0 || !out || B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (dh != 64 && dh != 128) || cap < 1 || kv_split < 0 || kv_chunks > 64 || (kv_split > 0 && !work))
         return QWEN3_E_ARG;
     if (window < 0 || (ring && (ring != cap || ring % 256 || window < 1))) return QWEN3_E_ARG;
+    if (heads_per_cta < 0 || heads_per_cta > 2 || (heads_per_cta == 2 && (Hq / Hkv) % 2)) return QWEN3_E_ARG;
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
                                B, T, Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<bf16*>(out),
                                err, kv_split,
-                               kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work),
+                               kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work), heads_per_cta,
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

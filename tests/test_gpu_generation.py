@@ -100,7 +100,8 @@ def _run_padded(bd, w, prompts, steps_o, cap, prefix_ids=None):
     return m, got
 
 
-@pytest.mark.parametrize("lengths", [[5, 64, 37, 100], [128, 77, 1]], ids=["width100", "width128"])
+@pytest.mark.parametrize("lengths", [[5, 64, 37, 100], [128, 77, 1], [300, 40, 129], [512, 3, 260]],
+                         ids=["width100", "width128", "width300", "width512"])
 def test_padded_prefill_and_decode(bd, tiny, lengths):
     w, om = tiny
     prompts = _prompts(lengths, 40 + len(lengths))

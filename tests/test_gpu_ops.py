@@ -244,6 +244,15 @@ def test_attention_prefill(bd, Bq, T, Hq, Hkv, dh, len0):
     _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 0, 1)
 
 
+@pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0", [(1, 64, 8, 4, 64, 0), (2, 130, 8, 2, 64, 0), (1, 700, 8, 2, 128, 0),
+                                                  (2, 77, 16, 8, 128, 70), (3, 257, 8, 8, 128, 511)])
+def test_attention_prefill_one_head_per_cta(bd, Bq, T, Hq, Hkv, dh, len0):
+    """The one-head-per-CTA variant (score regions alternate between tiles)."""
+    _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 0, 1, heads=1)
+    if Hkv < Hq:
+        _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 1, 3, heads=1)
+
+
 @pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0,split,chunks", [(1, 700, 8, 2, 128, 0, 1, 4), (1, 1024, 16, 8, 128, 0, 2, 4),
                                                                (2, 257, 8, 8, 128, 511, 1, 3), (1, 384, 4, 1, 64, 129, 1, 2),
                                                                (1, 300, 8, 4, 64, 70, 1, 8)])
@@ -251,7 +260,7 @@ def test_attention_prefill_split_kv(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks)
     _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks)
 
 
-def _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks):
+def _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks, heads=0):
     rng = np.random.default_rng(T * 31 + len0)
     cap = len0 + T + 5
     q = rand_bf16(rng, (Bq, Hq, T, dh))
@@ -268,7 +277,7 @@ def _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, split, chunks):
                            dtype=torch.float32, device="cuda")
     for _ in range(2 if split else 1):  # twice: the merge tickets must be left at zero
         bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err, kv_split=split, kv_chunks=chunks,
-                                work=work)
+                                work=work, heads_per_cta=heads)
     torch.cuda.synchronize()
     assert err.item() == 0
     if split:
