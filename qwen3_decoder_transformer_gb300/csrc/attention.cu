@@ -453,6 +453,356 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
     }
 }
 
+// Persistent form of the one-head-per-CTA kernel: grid = min(work items, SMs). Work items are
+// (query tile, sequence, query head) triples, longest causal range first; CTA c takes items
+// c, 2G-1-c, 2G+c, ... (a snake over the sorted list, so every CTA gets a similar total). Tensor
+// memory, barriers and the TMA/MMA pipeline stay alive across items: the next item's Q and first
+// scores load while the softmax warps finish the current item, whose output accumulator is then
+// handed back to the MMA warp (o_free) before the next item's first PV overwrites it. Tiles are
+// counted across items (g), so ring stages, score regions and barrier phases simply continue.
+constexpr int PS_THREADS = 64 + 128;
+
+template <int DH>
+__global__ void __launch_bounds__(PS_THREADS, 1)
+    attn_prefill_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                                   const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv, int B,
+                                   const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
+                                   __nv_bfloat16* __restrict__ out, int* err) {
+    using Ly = TcLayout<DH, 1>;
+    constexpr int NCH = Ly::NCH;
+    constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
+    constexpr uint32_t IDESC_O = idesc_bf16(TC_BM, DH, true);
+    constexpr uint32_t TM_O = 2 * TC_BN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR_OFF);
+    uint64_t* q_full = bars;
+    uint64_t* q_empty = bars + 1;
+    uint64_t* k_full = bars + 2;   // [2]
+    uint64_t* v_full = bars + 4;   // [2]
+    uint64_t* k_empty = bars + 6;  // [2]
+    uint64_t* v_empty = bars + 8;  // [2]
+    uint64_t* s_full = bars + 10;  // [2] per score region
+    uint64_t* p_full = bars + 12;  // [2] per score region
+    uint64_t* o_done = bars + 14;
+    uint64_t* o_free = bars + 15;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_qt = (T + TC_BM - 1) / TC_BM;
+    const int per_qt = B * Hq;
+    const int n_items = n_qt * per_qt;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(o_free, 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    pdl_wait();  // Q and the cache come from the previous kernel
+    pdl_trigger();
+    const int len0 = *len0p;
+    int ps_meta = 0, psh = 0;
+    if (meta) {
+        ps_meta = meta[0];
+        psh = meta[1];
+    }
+
+    // The parameters of this CTA's round-th item (n_tiles = 0 when it has none left).
+    struct Item {
+        int b, h, q0, q_end, n_valid, j_lo, ja, jb, n_tiles, ps, pe;
+    };
+    auto item_of = [&](int round) -> Item {
+        Item it{};
+        const int k = round * G + ((round & 1) ? G - 1 - c : c);
+        if (k >= n_items) return it;
+        const int qt = n_qt - 1 - k / per_qt, rem = k % per_qt;
+        it.b = rem / Hq;
+        it.h = rem % Hq;
+        it.q0 = qt * TC_BM;
+        it.q_end = min(T, it.q0 + TC_BM);
+        it.ps = ps_meta;
+        it.pe = meta ? ps_meta + meta[kSeqMetaHead + it.b] : 0;
+        it.n_valid = len0 + it.q_end;
+        const int n_end = (it.n_valid + TC_BN - 1) / TC_BN;
+        it.j_lo = window > 0 ? max(0, len0 + it.q0 - window + 1) / TC_BN : 0;
+        it.ja = max(it.j_lo, (it.ps + TC_BN - 1) / TC_BN);
+        it.jb = max(it.ja, min(it.pe / TC_BN, (len0 + it.q0) / TC_BN));
+        it.n_tiles = n_end - it.j_lo - (it.jb - it.ja);
+        return it;
+    };
+    auto tile_j = [](const Item& it, int i) { return it.j_lo + i < it.ja ? it.j_lo + i : it.j_lo + i + (it.jb - it.ja); };
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            int g = 0;
+            for (int round = 0; ok; ++round) {
+                const Item it = item_of(round);
+                if (it.n_tiles == 0) break;
+                const int jkv = it.h / (Hq / Hkv);
+                if (!mbar_wait(q_empty, (round & 1) ^ 1, abort_flag)) { ok = false; break; }
+                mbar_expect_tx(q_full, Ly::Q_BYTES);
+                for (int cc = 0; cc < NCH; ++cc)
+                    tma_load_3d(smem + Ly::Q_OFF + cc * TC_BM * 128, &tmQ, q_full, cc * 64, it.q0, it.b * Hq + it.h);
+                for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                    const int s = g & 1, j = tile_j(it, i);
+                    const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
+                    const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
+                    const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
+                    if (!mbar_wait(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
+                    for (int cc = 0; cc < NCH; ++cc)
+                        tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmK, &k_full[s], cc * 64, y, z);
+                    if (!mbar_wait(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
+                    for (int cc = 0; cc < NCH; ++cc)
+                        tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmV, &v_full[s], cc * 64, y, z);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (all lanes walk the schedule; lane 0 issues)
+        int g = 0;  // tiles of earlier items
+        for (int round = 0; ok; ++round) {
+            const Item it = item_of(round);
+            const int nt = it.n_tiles;
+            if (nt == 0) break;
+            // scores of local tile i into region (g + i) & 1; the item's last score releases Q
+            auto issue_s = [&](int i) -> bool {
+                const int gi = g + i, s = gi & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (gi >> 1) & 1, abort_flag))) return false;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sq = smem_u32(smem + Ly::Q_OFF);
+                    const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < DH / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
+                        umma_bf16_ss(tmem + s * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off),
+                                     IDESC_S, kk > 0);
+                    }
+                    umma_commit(&s_full[s]);
+                    umma_commit(&k_empty[s]);
+                    if (i == nt - 1) umma_commit(q_empty);
+                }
+                __syncwarp();
+                return true;
+            };
+            ok = __all_sync(0xffffffffu, mbar_wait(q_full, round & 1, abort_flag));
+            if (ok) ok = issue_s(0);
+            if (ok && nt > 1) ok = issue_s(1);
+            for (int i = 0; ok && i < nt; ++i) {
+                const int gi = g + i, s = gi & 1;
+                const int j = tile_j(it, i);
+                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
+                const int r0 = it.n_valid - j * TC_BN;  // first stale key row of this tile
+                if (r0 < TC_BN) {
+                    for (int e = lane; e < (TC_BN - r0) * 8 * NCH; e += 32) {
+                        const int cc = e / ((TC_BN - r0) * 8), rem = e % ((TC_BN - r0) * 8);
+                        reinterpret_cast<uint4*>(sv + cc * TC_BN * 128 + (r0 + rem / 8) * 128)[rem % 8] =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (i == 0 && !__all_sync(0xffffffffu, mbar_wait(o_free, (round & 1) ^ 1, abort_flag))) {
+                    ok = false;  // the previous item's output is still being read
+                    break;
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t svv = smem_u32(sv);
+#pragma unroll
+                    for (int kk = 0; kk < TC_BN / 16; ++kk) {
+                        const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
+                        umma_bf16_ts(tmem + TM_O, tmem + s * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
+                    }
+                    umma_commit(o_done);
+                    umma_commit(&v_empty[s]);
+                }
+                __syncwarp();
+                if (i + 2 < nt) ok = issue_s(i + 2);
+            }
+            g += nt;
+        }
+    } else {
+        // ---------------- softmax warps: thread <-> query row (TMEM lane)
+        const int quarter = warp & 3, row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tm_o = tmem + lane_off + TM_O;
+        const float sl2 = kLog2e / sqrtf((float)DH);
+        int pv_seen = 0;  // PV completions confirmed so far, across items
+        auto confirm_pv = [&](int upto) -> bool {
+            while (pv_seen < upto) {
+                if (!mbar_wait(o_done, pv_seen & 1, abort_flag)) return false;
+                ++pv_seen;
+            }
+            return true;
+        };
+        int g = 0;
+        for (int round = 0; ok; ++round) {
+            const Item it = item_of(round);
+            const int nt = it.n_tiles;
+            if (nt == 0) break;
+            const int t = it.q0 + row, pos = len0 + t;
+            float m_used = -INFINITY, l = 0.f;
+            for (int i = 0; i < nt; ++i) {
+                const int gi = g + i, r = gi & 1;
+                const int j = tile_j(it, i);
+                const uint32_t tm_s = tmem + lane_off + r * TC_BN;
+                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[r], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[TC_BN];
+#pragma unroll
+                for (int cc = 0; cc < TC_BN / 32; ++cc)
+                    tmem_ld_32x32b_x32(tm_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+                tmem_ld_wait();
+                const int k0 = j * TC_BN;
+                float mx = -INFINITY;
+                const bool diag = k0 + TC_BN - 1 > len0 + it.q0;
+                const bool pads = k0 < it.pe && k0 + TC_BN > it.ps;
+                const bool old = window > 0 && k0 < len0 + it.q_end - window;
+                if (pads || old) {
+                    // visible: (i <= lim, not padding, inside the window) or the query itself; branch-free
+                    const int lim = pos - k0;
+                    const int lo = window > 0 ? lim - window + 1 : -TC_BN;
+                    const int a1 = max(lo, 0), n1 = max(0, min(lim, it.ps - k0 - 1) - a1 + 1);
+                    const int a2 = max(lo, it.pe - k0), n2 = max(0, lim - a2 + 1);
+#pragma unroll
+                    for (int e = 0; e < TC_BN; ++e) {
+                        const bool vis =
+                            ((unsigned)(e - a1) < (unsigned)n1) | ((unsigned)(e - a2) < (unsigned)n2) | (e == lim);
+                        const float v = vis ? __uint_as_float(sr[e]) : -INFINITY;
+                        sr[e] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+                } else if (diag) {
+                    const int lim = pos - k0;
+#pragma unroll
+                    for (int e = 0; e < TC_BN; ++e) {
+                        const float v = e <= lim ? __uint_as_float(sr[e]) : -INFINITY;
+                        sr[e] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < TC_BN; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]));
+                }
+                mx *= sl2;
+                const bool grow = mx > m_used + 8.0f;
+                const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
+                if (i > 0 && __any_sync(0xffffffffu, grow)) {
+                    const bool w = confirm_pv(gi);  // O must hold P V of the previous tile before it is scaled
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < DH / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(tm_o + cc * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st_32x32b_x32(tm_o + cc * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                if (grow) {
+                    l *= alpha;
+                    m_used = mx;
+                }
+                const float nm = m_used == -INFINITY ? 0.f : -m_used;
+                float rs = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
+                        rs += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st_32x32b_x32(tm_s + half * 32, pk);
+                }
+                tmem_st_wait();
+                l += rs;
+                // observe the previous PV completion before releasing this P (keeps o_done parity waits
+                // unambiguous: never more than one phase ahead of this thread)
+                if (i > 0) {
+                    const bool w = confirm_pv(gi);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                tc_fence_before();
+                mbar_arrive(&p_full[r]);
+            }
+            if (ok) ok = confirm_pv(g + nt);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            // O / l to the output, then hand the accumulator back to the MMA warp
+            tc_fence_after();
+            __nv_bfloat16* orow = out + (((size_t)it.b * T + t) * Hq + it.h) * DH;
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int cc = 0; cc < DH / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tm_o + cc * 32, o);
+                tmem_ld_wait();
+                if (t < T) {
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        reinterpret_cast<uint4*>(orow + cc * 32)[v] =
+                            make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(o_free);
+            g += nt;
+        }
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        if (err) atomicOr(err, ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 
 // ------------------------------------------------------------------------------------- decode
 constexpr int DEC_CHUNK = 256, DEC_THREADS = 128, DEC_UNROLL = 8;
@@ -714,10 +1064,20 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         split = 0;
         max_chunks = 1;
     }
-    if (heads == 0) heads = attn_heads_per_cta(Hq, Hkv);
+    if (heads == 0) {
+        // Two heads per CTA share each K/V tile and have the best per-tile throughput on long grids;
+        // below ~16 waves of those CTAs the persistent one-head kernel wins on load balance.
+        const long long ctas2 = (long long)((T + TC_BM - 1) / TC_BM) * (Hq / 2) * B;
+        heads = (Hq / Hkv) % 2 == 0 && (split > 0 || ctas2 >= 16LL * device_sm_count()) ? 2 : 1;
+    }
     if (heads == 2 && (Hq / Hkv) % 2 == 0)
         return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
-    return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
+    if (split > 0)
+        return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
+    const long long items = (long long)((T + TC_BM - 1) / TC_BM) * Hq * B;
+    const unsigned grid = (unsigned)std::min<long long>(items, device_sm_count());
+    return launch_pdl(attn_prefill_persistent_kernel<DH>, dim3(grid), dim3(PS_THREADS), TcLayout<DH, 1>::SMEM, st, tq, tk,
+                      tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
 }
 
 }  // namespace
@@ -784,9 +1144,11 @@ int attn_decode_kernel_count() { return 2; }
 
 cudaError_t attention_prepare() {
     const void* fns[] = {(const void*)attn_prefill_tc_kernel<128, 1>, (const void*)attn_prefill_tc_kernel<128, 2>,
-                         (const void*)attn_prefill_tc_kernel<64, 1>, (const void*)attn_prefill_tc_kernel<64, 2>};
-    const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM};
-    for (int i = 0; i < 4; ++i) {
+                         (const void*)attn_prefill_tc_kernel<64, 1>,  (const void*)attn_prefill_tc_kernel<64, 2>,
+                         (const void*)attn_prefill_persistent_kernel<128>, (const void*)attn_prefill_persistent_kernel<64>};
+    const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM,
+                        TcLayout<128, 1>::SMEM, TcLayout<64, 1>::SMEM};
+    for (int i = 0; i < 6; ++i) {
         cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
     }
