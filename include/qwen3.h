@@ -283,9 +283,9 @@ QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache,
 /* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.
  * d_seq_meta, window and ring as for qwen3_op_attention_prefill (padding slots are skipped, a window
- * keeps the last `window` slots, a ring wraps). d_work is caller scratch of
- * qwen3_attention_decode_workspace(B, Hq, dh, cap, window) bytes. */
-QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window);
+ * keeps the last `window` slots, a ring wraps; ring > 0 must be a multiple of 256). d_work is caller
+ * scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring) bytes. */
+QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
 QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                               int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
                               int window, int ring, void* d_work, void* d_out, void* stream);

@@ -92,7 +92,7 @@ def lib() -> ctypes.CDLL:
     L.qwen3_attention_prefill_workspace.restype = sz
     L.qwen3_attention_prefill_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_attention_decode_workspace.restype = sz
-    L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i, i]
+    L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, i, i, _vp, _vp, _vp]
     L.qwen3_op_greedy.argtypes = [_vp, ctypes.c_int64, i, i, i, _vp, _vp, _vp]
     L.qwen3_prefill_padded.argtypes = [_vp, _vp, _i32p, i, i, _vp, i, _vp]
@@ -306,8 +306,8 @@ def op_attention_prefill(q, k_cache, v_cache, len0, out, err=None, kv_split=0, k
                                            _p(out), _p(err), _stream(stream)))
 
 
-def attention_decode_workspace(B, Hq, dh, cap, window=0) -> int:
-    return lib().qwen3_attention_decode_workspace(B, Hq, dh, cap, window)
+def attention_decode_workspace(B, Hq, dh, cap, window=0, ring=0) -> int:
+    return lib().qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring)
 
 
 def op_attention_decode(q, k_cache, v_cache, len0, work, out, seq_meta=None, window=0, ring=0, stream=None):

@@ -263,10 +263,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 tmem_ld_32x32b_x32(tm_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_ld_wait();
             const int k0 = j * TC_BN;
-            // row max over 8 independent partial maxima (short dependency chains)
-            float mx8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+            float mx = -INFINITY;
             // keys to mask in this tile (decided for the whole CTA): past the diagonal, padding of
             // this sequence, or older than some row's window
             const bool diag = k0 + TC_BN - 1 > len0 + q0;
@@ -285,7 +282,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                     const bool vis = ((unsigned)(i - a1) < (unsigned)n1) | ((unsigned)(i - a2) < (unsigned)n2) | (i == lim);
                     const float v = vis ? __uint_as_float(sr[i]) : -INFINITY;
                     sr[i] = __float_as_uint(v);
-                    mx8[i & 7] = fmaxf(mx8[i & 7], v);
+                    mx = fmaxf(mx, v);
                 }
             } else if (diag) {  // only the causal diagonal: keys past the query's slot
                 const int lim = pos - k0;
@@ -293,14 +290,12 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 for (int i = 0; i < TC_BN; ++i) {
                     const float v = i <= lim ? __uint_as_float(sr[i]) : -INFINITY;
                     sr[i] = __float_as_uint(v);
-                    mx8[i & 7] = fmaxf(mx8[i & 7], v);
+                    mx = fmaxf(mx, v);
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < TC_BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+                for (int i = 0; i < TC_BN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
             }
-            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             mx *= sl2;
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
@@ -327,9 +322,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region (a row
             // with no visible key yet keeps m = -inf and gets P = 0)
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            float rs8[8];  // row sum over 8 independent partial sums
-#pragma unroll
-            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+            float rs = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
@@ -337,14 +330,13 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 for (int e = 0; e < 32; ++e) {
                     const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
                     const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
-                    rs8[(2 * e) & 7] += p0;
-                    rs8[(2 * e + 1) & 7] += p1;
+                    rs += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
                 tmem_st_32x32b_x32(tm_s + half * 32, pk);
             }
             tmem_st_wait();
-            l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            l += rs;
             // Observe the previous P V completion before releasing this P: o_done is then never more
             // than one phase ahead of this thread, so its parity waits stay unambiguous.
             if (i > 0) {
@@ -805,36 +797,60 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
 
 
 // ------------------------------------------------------------------------------------- decode
-constexpr int DEC_CHUNK = 256, DEC_THREADS = 128, DEC_UNROLL = 8;
+// Keys per decode CTA: long chunks amortise each CTA's fixed work over long caches, shorter ones keep
+// more CTAs busy on short caches; a rolling buffer uses the shortest so that its ring (a multiple of
+// 256) never wraps inside a chunk.
+constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256, DEC_THREADS = 128, DEC_UNROLL = 4;
+
+// Two fp32 lanes at once (Blackwell paired FMA): d = a * b + c on (x, y).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+          "l"(*reinterpret_cast<unsigned long long*>(&c)));
+    return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t v) { return make_float2(bf16_lo(v), bf16_hi(v)); }
 
 // Workspace layout per (b, q-head, split): [m, l] floats, then DH floats of unnormalised output.
-template <int DH, int G>
+// A CTA owns CH keys of one (sequence, kv head). Eight lanes share a key row (16 elements,
+// two 16-byte loads each), so a warp covers four keys per step and a score needs three shuffle
+// levels; products run as paired fp32 FMAs on (even, odd) element pairs.
+template <int DH, int G, int CH>
 __global__ void __launch_bounds__(DEC_THREADS)
     attn_decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                              const __nv_bfloat16* __restrict__ vc, int Hq, int Hkv, int cap,
                              const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
                              float* __restrict__ work) {
-    constexpr int LPK = DH / 8;   // lanes per key row (16-byte pieces)
-    constexpr int KPW = 32 / LPK;  // keys per warp per step
+    constexpr int UNR = CH == DEC_CHUNK_SHORT ? 8 : DEC_UNROLL;  // key rows in flight per lane and pass
+    constexpr int LPK = 8;                      // lanes per key row
+    constexpr int EPL = DH / LPK;               // elements per lane: 16 (dh 128) or 8 (dh 64)
+    constexpr int WPL = EPL / 2;                // bf16x2 words per lane
+    constexpr int VPL = EPL / 8;                // 16-byte loads per lane and key
+    constexpr int KPW = 32 / LPK;               // keys per warp per step
     constexpr int KPS = KPW * (DEC_THREADS / 32);  // keys per block step
     constexpr int REC = DH + 2;
-    __shared__ float sc[G][DEC_CHUNK];
-    __shared__ float red[DEC_THREADS / 32][G][DH];
+    // scores / probabilities [G][CH], later reused for the cross-warp sums [warps][G][DH]
+    constexpr int SBUF = G * CH > (DEC_THREADS / 32) * G * DH ? G * CH : (DEC_THREADS / 32) * G * DH;
+    __shared__ float sbuf[SBUF];
     __shared__ float stat[G][2];
+    auto sc = reinterpret_cast<float(*)[CH]>(sbuf);
+    auto red = reinterpret_cast<float(*)[G][DH]>(sbuf);
 
     pdl_wait();
     pdl_trigger();
     const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int nsplit = gridDim.x;
     const int n = *len0p + 1;
-    // keys [lo, n): a sliding window keeps the last `window`; chunks are aligned to DEC_CHUNK slots
+    // keys [lo, n): a sliding window keeps the last `window`; chunks are aligned to CH slots
     const int lo = window > 0 ? max(0, n - window) : 0;
-    const int s0 = lo / DEC_CHUNK * DEC_CHUNK + split * DEC_CHUNK, s1 = min(n, s0 + DEC_CHUNK);
+    const int s0 = lo / CH * CH + split * CH, s1 = min(n, s0 + CH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPK, li = lane % LPK;
     float* wb = work + (((size_t)b * Hq + (size_t)j * G) * nsplit + split) * REC;
     // padding slots [ps, pe) of this sequence; slots below psh live in sequence 0; a rolling buffer
-    // stores slot s at s mod ring (ring a multiple of DEC_CHUNK, so a chunk stays contiguous)
+    // stores slot s at s mod ring (ring a multiple of CH, so a chunk stays contiguous)
     int ps = 0, pe = 0, psh = 0;
     if (meta) {
         ps = meta[0];
@@ -852,43 +868,51 @@ __global__ void __launch_bounds__(DEC_THREADS)
     const ptrdiff_t kv_own = (ptrdiff_t)(((size_t)b * Hkv + j) * cap) * DH + shift * DH;
     const ptrdiff_t kv_shared = (ptrdiff_t)((size_t)j * cap) * DH + shift * DH;
     const float sl2 = kLog2e / sqrtf((float)DH);
-    float qv[G][8];
+    // this lane's slice of the G query vectors, pre-scaled into log2 units
+    float2 qv[G][WPL];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        const uint4 v = *reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + (size_t)j * G + h) * DH + li * 8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + (size_t)j * G + h) * DH + li * EPL);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            qv[h][2 * e] = bf16_lo(w[e]) * sl2;
-            qv[h][2 * e + 1] = bf16_hi(w[e]) * sl2;
+        for (int v = 0; v < VPL; ++v) {
+            const uint4 x = src[v];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = bf16x2_f2(w[e]);
+                qv[h][v * 4 + e] = make_float2(f.x * sl2, f.y * sl2);
+            }
         }
     }
+    auto row_ptr = [&](const __nv_bfloat16* base, int s) {
+        return reinterpret_cast<const uint4*>(base + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH + li * EPL);
+    };
     // pass 1: scores (already in log2 units)
-    for (int base = s0; base < s1; base += KPS * DEC_UNROLL) {
-        uint4 kv[DEC_UNROLL];
+    for (int base = s0; base < s1; base += KPS * UNR) {
+        uint4 kv[UNR][VPL];
 #pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
-            kv[u] = s < s1 ? *reinterpret_cast<const uint4*>(kc + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH +
-                                                              li * 8)
-                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) kv[u][v] = s < s1 ? row_ptr(kc, s)[v] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
-            const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
             float d[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float acc = 0.f;
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc = fmaf(qv[h][2 * e], bf16_lo(w[e]), acc);
-                    acc = fmaf(qv[h][2 * e + 1], bf16_hi(w[e]), acc);
+                for (int v = 0; v < VPL; ++v) {
+                    const uint32_t w[4] = {kv[u][v].x, kv[u][v].y, kv[u][v].z, kv[u][v].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc = fma2(bf16x2_f2(w[e]), qv[h][v * 4 + e], acc);
                 }
+                float t = acc.x + acc.y;
 #pragma unroll
-                for (int o = LPK / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                d[h] = acc;
+                for (int o = LPK / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                d[h] = t;
             }
             if (li == 0 && s < s1) {
                 const bool vis = s >= lo && (s < ps || s >= pe);  // outside the window, or padding
@@ -919,62 +943,69 @@ __global__ void __launch_bounds__(DEC_THREADS)
         }
     }
     __syncthreads();
-    // pass 2: weighted sum of V rows
-    float acc[G][8];
+    // pass 2: weighted sum of V rows, (even, odd) element pairs per lane
+    float2 acc[G][WPL];
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-    for (int base = s0; base < s1; base += KPS * DEC_UNROLL) {
-        uint4 vv[DEC_UNROLL];
+        for (int e = 0; e < WPL; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    for (int base = s0; base < s1; base += KPS * UNR) {
+        uint4 vv[UNR][VPL];
 #pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
-            vv[u] = s < s1 ? *reinterpret_cast<const uint4*>(vc + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH +
-                                                              li * 8)
-                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) vv[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < DEC_UNROLL; ++u) {
+        for (int u = 0; u < UNR; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
             if (s >= s1) continue;
-            const uint32_t w[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float p = sc[h][s - s0];
+                const float2 pp = make_float2(p, p);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[h][2 * e] = fmaf(p, bf16_lo(w[e]), acc[h][2 * e]);
-                    acc[h][2 * e + 1] = fmaf(p, bf16_hi(w[e]), acc[h][2 * e + 1]);
+                for (int v = 0; v < VPL; ++v) {
+                    const uint32_t w[4] = {vv[u][v].x, vv[u][v].y, vv[u][v].z, vv[u][v].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[h][v * 4 + e] = fma2(bf16x2_f2(w[e]), pp, acc[h][v * 4 + e]);
                 }
             }
         }
     }
-    // reduce over the KPW key slots in the warp, then over warps
+    // reduce over the KPW key slots of the warp, then over warps
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float v = acc[h][e];
+        for (int e = 0; e < WPL; ++e) {
+            float x = acc[h][e].x, y = acc[h][e].y;
 #pragma unroll
-            for (int o = LPK; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[h][e] = v;
+            for (int o = LPK; o < 32; o <<= 1) {
+                x += __shfl_xor_sync(0xffffffffu, x, o);
+                y += __shfl_xor_sync(0xffffffffu, y, o);
+            }
+            acc[h][e] = make_float2(x, y);
         }
+    __syncthreads();  // every warp is done with the probabilities before their space is reused
     if (sub == 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) red[warp][h][li * 8 + e] = acc[h][e];
+            for (int e = 0; e < WPL; ++e) {
+                red[warp][h][li * EPL + 2 * e] = acc[h][e].x;
+                red[warp][h][li * EPL + 2 * e + 1] = acc[h][e].y;
+            }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < G * DH; i += DEC_THREADS) {
-        const int h = i / DH, d = i % DH;
+        const int h = i / DH, dd = i % DH;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < DEC_THREADS / 32; ++w) v += red[w][h][d];
+        for (int w = 0; w < DEC_THREADS / 32; ++w) v += red[w][h][dd];
         float* rec = wb + (size_t)h * nsplit * REC;
-        rec[2 + d] = v;
-        if (d == 0) {
+        rec[2 + dd] = v;
+        if (dd == 0) {
             rec[0] = stat[h][0];
             rec[1] = stat[h][1];
         }
@@ -1004,18 +1035,33 @@ __global__ void attn_decode_combine_kernel(const float* __restrict__ work, int H
 }
 
 // Chunks per (sequence, kv head): enough to cover every slot, or a window's keys at any alignment.
-int decode_nsplit(int cap, int window) {
-    const int all = (cap + DEC_CHUNK - 1) / DEC_CHUNK;
-    return window > 0 ? std::min(all, (window + DEC_CHUNK - 1) / DEC_CHUNK + 1) : all;
+int decode_chunk(int cap, int ring) { return ring ? DEC_CHUNK_RING : (cap >= 16384 ? DEC_CHUNK : DEC_CHUNK_SHORT); }
+int decode_nsplit(int cap, int window, int ring) {
+    const int ch = decode_chunk(cap, ring);
+    const int all = (cap + ch - 1) / ch;
+    return window > 0 ? std::min(all, (window + ch - 1) / ch + 1) : all;
 }
 
 template <int DH, int G>
 cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                             cudaStream_t st) {
-    const int nsplit = decode_nsplit(cap, sm.window);
-    cudaError_t e = launch_pdl(attn_decode_split_kernel<DH, G>, dim3(nsplit, Hkv, B), dim3(DEC_THREADS), 0, st, q, kc, vc,
-                               Hq, Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
+    const int nsplit = decode_nsplit(cap, sm.window, sm.ring);
+    const dim3 grid(nsplit, Hkv, B);
+    cudaError_t e;
+    switch (decode_chunk(cap, sm.ring)) {
+        case DEC_CHUNK_RING:
+            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK_RING>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq,
+                           Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
+            break;
+        case DEC_CHUNK_SHORT:
+            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK_SHORT>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq,
+                           Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
+            break;
+        default:
+            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq, Hkv,
+                           cap, len0, sm.meta, sm.window, sm.ring, work);
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, out);
 }
@@ -1125,8 +1171,8 @@ void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* spl
     }
 }
 
-size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window) {
-    const size_t nsplit = (size_t)decode_nsplit(cap, window);
+size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring) {
+    const size_t nsplit = (size_t)decode_nsplit(cap, window, ring);
     return (size_t)B * Hq * nsplit * (dh + 2) * sizeof(float);
 }
 
@@ -1134,7 +1180,7 @@ cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, 
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                                cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
-    if (sm.ring && (sm.ring % DEC_CHUNK || sm.ring != cap)) return cudaErrorInvalidValue;
+    if (sm.ring && (sm.ring % DEC_CHUNK_RING || sm.ring != cap)) return cudaErrorInvalidValue;
     if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
     if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
     return cudaErrorInvalidValue;

@@ -161,7 +161,7 @@ cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc,
 int attn_heads_per_cta(int Hq, int Hkv);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
-size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window);
+size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                                cudaStream_t st);

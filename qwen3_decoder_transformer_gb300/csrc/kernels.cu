@@ -311,7 +311,7 @@ __global__ void add_len_kernel(int* len, int delta) {
 // one CTA per row finds the largest logit, the lowest index on ties, a NaN counting as the largest
 // (torch.argmax's rule). With stop_id >= 0 a finished row emits stop_id, and a row that emits it is
 // finished; `alive` counts the rows still running after this step.
-constexpr int GREEDY_THREADS = 512;
+constexpr int GREEDY_THREADS = 1024, GREEDY_UNROLL = 4;
 __device__ __forceinline__ bool greedy_better(float v, int i, float bv, int bi) {
     const bool nv = v != v, nb = bv != bv;
     if (nv != nb) return nv;
@@ -327,15 +327,25 @@ __global__ void __launch_bounds__(GREEDY_THREADS)
     const float* row = logits + (size_t)b * ld;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int i = threadIdx.x * 4; i < V; i += GREEDY_THREADS * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(row + i);
-        const float e[4] = {v.x, v.y, v.z, v.w};
+    // GREEDY_UNROLL independent 16-byte loads in flight per thread
+    for (int base = threadIdx.x * 4; base < V; base += GREEDY_THREADS * 4 * GREEDY_UNROLL) {
+        float4 v[GREEDY_UNROLL];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (greedy_better(e[k], i + k, bv, bi)) {
-                bv = e[k];
-                bi = i + k;
-            }
+        for (int u = 0; u < GREEDY_UNROLL; ++u) {
+            const int i = base + u * GREEDY_THREADS * 4;
+            v[u] = i < V ? *reinterpret_cast<const float4*>(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < GREEDY_UNROLL; ++u) {
+            const int i = base + u * GREEDY_THREADS * 4;
+            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (i + k < V && greedy_better(e[k], i + k, bv, bi)) {
+                    bv = e[k];
+                    bi = i + k;
+                }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

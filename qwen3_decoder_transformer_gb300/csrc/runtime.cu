@@ -475,7 +475,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
               dmalloc(&c->q, rows * c->q_width) == cudaSuccess &&
               dmalloc(&c->attn, arows * c->q_width) == cudaSuccess && dmalloc(&c->h, arows * F) == cudaSuccess &&
               dmalloc(&c->hn, arows * d) == cudaSuccess &&
-              dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, c->slots, c->window) / 4) ==
+              dmalloc(&c->dec_work, attn_decode_workspace(max_batch, g->n_q_heads, dh, c->slots, c->window, c->ring) / 4) ==
                   cudaSuccess &&
               dmalloc(&c->d_seq, (size_t)kSeqMetaHead + max_batch) == cudaSuccess &&
               dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
@@ -923,9 +923,9 @@ int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, in
                : QWEN3_E_CUDA;
 }
 
-size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window) {
-    if (B < 1 || Hq < 1 || cap < 1 || window < 0) return 0;
-    return attn_decode_workspace(B, Hq, dh, cap, window);
+size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring) {
+    if (B < 1 || Hq < 1 || cap < 1 || window < 0 || ring < 0) return 0;
+    return attn_decode_workspace(B, Hq, dh, cap, window, ring);
 }
 
 int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh, int cap,
@@ -952,7 +952,7 @@ int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void*
         return QWEN3_E_ARG;
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
-    if (attn_decode_workspace(B, Hq, dh, cap, 0) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
+    if (attn_decode_workspace(B, Hq, dh, cap, 0, 0) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
     float* scratch = nullptr;
     if (attn_decode_noalloc_scratch(&scratch) != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,

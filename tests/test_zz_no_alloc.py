@@ -61,7 +61,7 @@ def test_noalloc_matches_workspace_entry_point(L):
 
 def test_noalloc_refuses_oversized_workspace(L):
     binding, lib = L
-    Bq, Hq, Hkv, dh, cap = 16, 32, 8, 128, 32832
+    Bq, Hq, Hkv, dh, cap = 64, 32, 8, 128, 32832
     assert binding.attention_decode_workspace(Bq, Hq, dh, cap) > (16 << 20)
     q = torch.zeros(Bq, Hq, dh, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(1, dtype=torch.bfloat16, device="cuda")
