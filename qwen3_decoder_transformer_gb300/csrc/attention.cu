@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 tmem_ld_32x32b_x32(tm_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tmem_ld_wait();
             const int k0 = j * TC_BN;
-            float mx = -INFINITY;
             // keys to mask in this tile (decided for the whole CTA): past the diagonal, padding of
             // this sequence, or older than some row's window
             const bool diag = k0 + TC_BN - 1 > len0 + q0;
@@ -280,22 +279,16 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < TC_BN; ++i) {
                     const bool vis = ((unsigned)(i - a1) < (unsigned)n1) | ((unsigned)(i - a2) < (unsigned)n2) | (i == lim);
-                    const float v = vis ? __uint_as_float(sr[i]) : -INFINITY;
-                    sr[i] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
+                    sr[i] = vis ? sr[i] : __float_as_uint(-INFINITY);
                 }
             } else if (diag) {  // only the causal diagonal: keys past the query's slot
                 const int lim = pos - k0;
 #pragma unroll
-                for (int i = 0; i < TC_BN; ++i) {
-                    const float v = i <= lim ? __uint_as_float(sr[i]) : -INFINITY;
-                    sr[i] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < TC_BN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+                for (int i = 0; i < TC_BN; ++i) sr[i] = i <= lim ? sr[i] : __float_as_uint(-INFINITY);
             }
+            float mx = -INFINITY;  // three-input maxima: two scores per instruction
+#pragma unroll
+            for (int i = 0; i < TC_BN; i += 2) mx = fmax3(mx, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
             mx *= sl2;
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
@@ -309,8 +302,13 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                     uint32_t o[32];
                     tmem_ld_32x32b_x32(tm_o + c * 32, o);
                     tmem_ld_wait();
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 r2 = mul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                        o[e] = __float_as_uint(r2.x);
+                        o[e + 1] = __float_as_uint(r2.y);
+                    }
                     tmem_st_32x32b_x32(tm_o + c * 32, o);
                 }
                 tmem_st_wait();
@@ -322,21 +320,24 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this head's S region (a row
             // with no visible key yet keeps m = -inf and gets P = 0)
             const float nm = m_used == -INFINITY ? 0.f : -m_used;
-            float rs = 0.f;
+            const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+            float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
-                    rs += p0 + p1;
-                    pk[e] = pack_bf16(p0, p1);
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[half * 64 + 2 * e]),
+                                                      __uint_as_float(sr[half * 64 + 2 * e + 1])),
+                                          sl2x2, nmx2);
+                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    rs2 = add2(rs2, pp);
+                    pk[e] = pack_bf16(pp.x, pp.y);
                 }
                 tmem_st_32x32b_x32(tm_s + half * 32, pk);
             }
             tmem_st_wait();
-            l += rs;
+            l += rs2.x + rs2.y;
             // Observe the previous P V completion before releasing this P: o_done is then never more
             // than one phase ahead of this thread, so its parity waits stay unambiguous.
             if (i > 0) {
@@ -677,7 +678,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     tmem_ld_32x32b_x32(tm_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
                 tmem_ld_wait();
                 const int k0 = j * TC_BN;
-                float mx = -INFINITY;
                 const bool diag = k0 + TC_BN - 1 > len0 + it.q0;
                 const bool pads = k0 < it.pe && k0 + TC_BN > it.ps;
                 const bool old = window > 0 && k0 < len0 + it.q_end - window;
@@ -691,22 +691,16 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     for (int e = 0; e < TC_BN; ++e) {
                         const bool vis =
                             ((unsigned)(e - a1) < (unsigned)n1) | ((unsigned)(e - a2) < (unsigned)n2) | (e == lim);
-                        const float v = vis ? __uint_as_float(sr[e]) : -INFINITY;
-                        sr[e] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
+                        sr[e] = vis ? sr[e] : __float_as_uint(-INFINITY);
                     }
                 } else if (diag) {
                     const int lim = pos - k0;
 #pragma unroll
-                    for (int e = 0; e < TC_BN; ++e) {
-                        const float v = e <= lim ? __uint_as_float(sr[e]) : -INFINITY;
-                        sr[e] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < TC_BN; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]));
+                    for (int e = 0; e < TC_BN; ++e) sr[e] = e <= lim ? sr[e] : __float_as_uint(-INFINITY);
                 }
+                float mx = -INFINITY;  // three-input maxima: two scores per instruction
+#pragma unroll
+                for (int e = 0; e < TC_BN; e += 2) mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
                 mx *= sl2;
                 const bool grow = mx > m_used + 8.0f;
                 const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
@@ -719,8 +713,13 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                         uint32_t o[32];
                         tmem_ld_32x32b_x32(tm_o + cc * 32, o);
                         tmem_ld_wait();
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 r2 = mul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                            o[e] = __float_as_uint(r2.x);
+                            o[e + 1] = __float_as_uint(r2.y);
+                        }
                         tmem_st_32x32b_x32(tm_o + cc * 32, o);
                     }
                     tmem_st_wait();
@@ -730,21 +729,24 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     m_used = mx;
                 }
                 const float nm = m_used == -INFINITY ? 0.f : -m_used;
-                float rs = 0.f;
+                const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+                float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e]), sl2, nm));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[half * 64 + 2 * e + 1]), sl2, nm));
-                        rs += p0 + p1;
-                        pk[e] = pack_bf16(p0, p1);
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[half * 64 + 2 * e]),
+                                                          __uint_as_float(sr[half * 64 + 2 * e + 1])),
+                                              sl2x2, nmx2);
+                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        rs2 = add2(rs2, pp);
+                        pk[e] = pack_bf16(pp.x, pp.y);
                     }
                     tmem_st_32x32b_x32(tm_s + half * 32, pk);
                 }
                 tmem_st_wait();
-                l += rs;
+                l += rs2.x + rs2.y;
                 // observe the previous PV completion before releasing this P (keeps o_done parity waits
                 // unambiguous: never more than one phase ahead of this thread)
                 if (i > 0) {
@@ -802,15 +804,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
 // 256) never wraps inside a chunk.
 constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256, DEC_THREADS = 128, DEC_UNROLL = 4;
 
-// Two fp32 lanes at once (Blackwell paired FMA): d = a * b + c on (x, y).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
-          "l"(*reinterpret_cast<unsigned long long*>(&c)));
-    return *reinterpret_cast<float2*>(&d);
-}
 __device__ __forceinline__ float2 bf16x2_f2(uint32_t v) { return make_float2(bf16_lo(v), bf16_hi(v)); }
 
 // Workspace layout per (b, q-head, split): [m, l] floats, then DH floats of unnormalised output.
