@@ -110,6 +110,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_attention_masked_gqa_row_f64.restype = ctypes.c_int
     L.oracle_attention_masked_gqa_row_f64.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int64, _u8p, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_int, _f64p]
+    L.oracle_layer_out_masked.restype = ctypes.c_int
+    L.oracle_layer_out_masked.argtypes = [ctypes.POINTER(OracleConfig), ctypes.POINTER(OracleWeights), ctypes.c_int,
+                                          _u16p, _u16p, ctypes.c_int64, _u16p, _u16p, _i32p, ctypes.c_int64, _u8p,
+                                          _u16p]
     L.oracle_forward_masked.restype = ctypes.c_int
     L.oracle_forward_masked.argtypes = [ctypes.POINTER(OracleConfig), ctypes.POINTER(OracleWeights),
                                         _u16p, _u16p, ctypes.c_int, ctypes.c_int64, _i32p, ctypes.c_int,
@@ -385,6 +389,20 @@ class Model:
         lib().oracle_layer_out(ctypes.byref(self.c), ctypes.byref(self.ow), layer, _p(xin, _u16p),
                                _p(q, _u16p), _p(pos, _i32p), n, _p(kc, _u16p), _p(vc, _u16p),
                                _p(kvset, _i32p), kc.shape[2], _p(out, _u16p))
+        return out
+
+    def layer_out_masked(self, layer: int, xin, q, kc, vc, kvset, mask):
+        """Steps a5-a9 with explicit masks: kc/vc [nsets, Hkv, cap, dh]; mask [n, cap] bool over slots."""
+        xin, q, kc, vc = _u16(xin), _u16(q), _u16(kc), _u16(vc)
+        kvset = np.ascontiguousarray(kvset, dtype=np.int32)
+        mask = np.ascontiguousarray(mask, dtype=np.uint8)
+        n = xin.shape[0]
+        out = np.empty_like(xin)
+        rc = lib().oracle_layer_out_masked(ctypes.byref(self.c), ctypes.byref(self.ow), layer, _p(xin, _u16p),
+                                           _p(q, _u16p), n, _p(kc, _u16p), _p(vc, _u16p), _p(kvset, _i32p),
+                                           kc.shape[2], _p(mask, _u8p), _p(out, _u16p))
+        if rc != 0:
+            raise ValueError("a row's mask admits no key")
         return out
 
     def head(self, x):

@@ -28,13 +28,16 @@ from __future__ import annotations
 import numpy as np
 
 
-def left_pad(prompts, pad_id: int, start: int = 0):
-    """Left-pad a batch of token lists after a shared start of ``start`` slots.
+def left_pad(prompts, pad_id: int, start: int = 0, width: int | None = None):
+    """Left-pad a batch of token lists after a shared start of ``start`` slots, to ``width`` columns
+    (default: the longest prompt).
 
     Returns ids [B, width] int32, real [B, start + width] bool, positions [B, width] int32 and
     mask [B, width, start + width] bool (query column t is cache column start + t)."""
     B = len(prompts)
-    width = max(len(p) for p in prompts)
+    width = width or max(len(p) for p in prompts)
+    if width < max(len(p) for p in prompts):
+        raise ValueError("width shorter than a prompt")
     ids = np.full((B, width), pad_id, dtype=np.int32)
     real = np.zeros((B, start + width), dtype=bool)
     real[:, :start] = True
