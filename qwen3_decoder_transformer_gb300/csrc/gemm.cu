@@ -39,11 +39,14 @@ constexpr int STG_BYTES = 32768;
 constexpr int EPI_LEADER = 64;  // thread 0 of warp 2 issues the epilogue's TMA loads and stores
 // Per tile width BN (256, or 128 when 256-wide tiles cannot fill the SMs): stage size, ring depth,
 // TMEM columns (two accumulators) and the instruction descriptor.
+// A stage holds KSUB consecutive 64-wide K boxes of A and B: two for 128-wide tiles, so each
+// barrier round trip carries as many MMA cycles as a 256-wide tile's stage.
 template <int BN>
 struct Cfg {
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int KSUB = BN == 256 ? 1 : 2;
+    static constexpr int B_BYTES = BN * BK * 2;  // per 64-wide K box
+    static constexpr int STAGE_BYTES = KSUB * (A_BYTES + B_BYTES);
+    static constexpr int STAGES = BN == 256 ? 4 : 3;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;  // epilogue staging: 2 boxes of [128 rows][128 B]
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
@@ -353,7 +356,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
-    const int k_blocks = (args.K + BK - 1) / BK;
+    constexpr int KSUB = C::KSUB;
+    const int k_blocks = (args.K + BK * KSUB - 1) / (BK * KSUB);  // stages per tile
     const int total = m_tiles * n_tiles;
 
     if (threadIdx.x == 0) {
@@ -404,10 +408,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) { ok = false; break; }
                 uint8_t* sa = smem + s * STAGE_BYTES;
                 mbar_expect_tx(&full_bar[s], STAGE_BYTES);
-                tma_load_2d(sa, &tmA, &full_bar[s], kb * BK, tl.m0);
 #pragma unroll
-                for (int nb = 0; nb < BN / kGemmBoxN; ++nb)
-                    tma_load_2d(sa + A_BYTES + nb * kGemmBoxN * BK * 2, &tmB, &full_bar[s], kb * BK, tl.n0 + nb * kGemmBoxN);
+                for (int j = 0; j < KSUB; ++j) {  // boxes past K read as zeros
+                    const int kx = (kb * KSUB + j) * BK;
+                    tma_load_2d(sa + j * A_BYTES, &tmA, &full_bar[s], kx, tl.m0);
+#pragma unroll
+                    for (int nb = 0; nb < BN / kGemmBoxN; ++nb)
+                        tma_load_2d(sa + KSUB * A_BYTES + j * C::B_BYTES + nb * kGemmBoxN * BK * 2, &tmB, &full_bar[s], kx,
+                                    tl.n0 + nb * kGemmBoxN);
+                }
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -425,10 +434,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&full_bar[s], ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-                const uint64_t adesc = sdesc_kmajor_sw128(sa), bdesc = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+                for (int j = 0; j < KSUB; ++j) {
+                    const uint64_t adesc = sdesc_kmajor_sw128(sa + j * A_BYTES);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(sa + KSUB * A_BYTES + j * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | j | k) != 0);
+                }
                 umma_commit(&empty_bar[s]);
             }
             if (!ok) break;
