@@ -472,7 +472,7 @@ def run_op(args, wl):
         Bd, ctx = args.rows or wl["decode_batch"] or 16, wl["prefilled_ctx"] or T
         q, kc, vc = rnd(Bd, hq, dh), rnd(Bd, hkv, ctx + 8, dh), rnd(Bd, hkv, ctx + 8, dh)
         len0.fill_(ctx - 1)
-        ws = torch.empty(binding.attention_decode_workspace(Bd, hq, dh, ctx + 8) // 4, dtype=torch.float32,
+        ws = torch.zeros(binding.attention_decode_workspace(Bd, hq, dh, ctx + 8) // 4, dtype=torch.float32,
                          device="cuda")
         out = torch.empty(Bd, hq * dh, dtype=torch.bfloat16, device="cuda")
         fn = lambda: binding.op_attention_decode(q, kc, vc, len0, ws, out)

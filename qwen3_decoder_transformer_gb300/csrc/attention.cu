@@ -5,10 +5,10 @@
 // Prefill: flash attention with an online softmax on the 5th-generation tensor cores (tcgen05,
 // accumulators in tensor memory, operands staged by TMA); see the kernel's own comment.
 //
-// Decode: one query per (sequence, query head) against the whole cache. A CTA owns a 256-key
-// chunk of one (sequence, kv head) and serves all g query heads of that group from one read of
-// K and V (16-byte coalesced loads, 8 in flight per thread). Partial (max, sum, output) triples
-// go to a workspace; a second kernel merges the chunks by log-sum-exp.
+// Decode: one query per (sequence, query head) against the whole cache. A CTA owns a chunk (256 to
+// 1024 keys) of one (sequence, kv head) and serves all g query heads of that group from one read of
+// K and V (16-byte coalesced loads). Partial (max, sum, output) triples go to a workspace; a second
+// kernel merges the chunks by log-sum-exp.
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
@@ -1005,30 +1005,70 @@ __global__ void __launch_bounds__(DEC_THREADS)
     }
 }
 
-// Merge the chunks of one (b, q-head): O = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// Merge the chunks of one (b, q-head) by log-sum-exp: O = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// The chunk weights are computed once into shared memory; each thread then sums its output element
+// over the chunks with four independent chains (four record loads in flight).
+constexpr int COMB_MAX_SPLITS = 1024;
 template <int DH>
-__global__ void attn_decode_combine_kernel(const float* __restrict__ work, int Hq, int nsplit,
-                                           __nv_bfloat16* __restrict__ out) {
+__global__ void __launch_bounds__(DH)
+    attn_decode_combine_kernel(const float* __restrict__ work, int Hq, int nsplit, __nv_bfloat16* __restrict__ out) {
     constexpr int REC = DH + 2;
+    __shared__ float wgt[COMB_MAX_SPLITS];
+    __shared__ float red[DH / 32];
+    __shared__ float inv_l;
     pdl_wait();
     pdl_trigger();
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const float* wb = work + ((size_t)b * Hq + h) * nsplit * REC;
     float M = -INFINITY;
-    for (int i = 0; i < nsplit; ++i) M = fmaxf(M, wb[(size_t)i * REC]);
-    float L = 0.f, acc = 0.f;
-    for (int i = 0; i < nsplit; ++i) {
-        const float mi = wb[(size_t)i * REC];
-        if (mi == -INFINITY) continue;
-        const float f = exp2f(mi - M);
-        L = fmaf(wb[(size_t)i * REC + 1], f, L);
-        acc = fmaf(wb[(size_t)i * REC + 2 + d], f, acc);
+    for (int c = d; c < nsplit; c += DH) {
+        const float mi = wb[(size_t)c * REC];
+        wgt[c] = mi;
+        M = fmaxf(M, mi);
     }
-    out[((size_t)b * Hq + h) * DH + d] = __float2bfloat16_rn(acc / L);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < DH / 32; ++w) M = fmaxf(M, red[w]);
+    float L = 0.f;
+    for (int c = d; c < nsplit; c += DH) {
+        const float mi = wgt[c];
+        const float f = mi == -INFINITY ? 0.f : exp2f(mi - M);
+        wgt[c] = f;
+        L = fmaf(wb[(size_t)c * REC + 1], f, L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = L;
+    __syncthreads();
+    if (d == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < DH / 32; ++w) t += red[w];
+        inv_l = 1.f / t;
+    }
+    __syncthreads();
+    const float* rd = wb + 2 + d;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int c = 0;
+    for (; c + 4 <= nsplit; c += 4) {
+        a0 = fmaf(rd[(size_t)c * REC], wgt[c], a0);
+        a1 = fmaf(rd[(size_t)(c + 1) * REC], wgt[c + 1], a1);
+        a2 = fmaf(rd[(size_t)(c + 2) * REC], wgt[c + 2], a2);
+        a3 = fmaf(rd[(size_t)(c + 3) * REC], wgt[c + 3], a3);
+    }
+    for (; c < nsplit; ++c) a0 = fmaf(rd[(size_t)c * REC], wgt[c], a0);
+    out[((size_t)b * Hq + h) * DH + d] = __float2bfloat16_rn(((a0 + a1) + (a2 + a3)) * inv_l);
 }
 
 // Chunks per (sequence, kv head): enough to cover every slot, or a window's keys at any alignment.
 int decode_chunk(int cap, int ring) { return ring ? DEC_CHUNK_RING : (cap >= 16384 ? DEC_CHUNK : DEC_CHUNK_SHORT); }
+// Per-(b, q-head, chunk) records [m, l, o[DH]].
+size_t decode_records_floats(int B, int Hq, int dh, int nsplit) { return (size_t)B * Hq * nsplit * (dh + 2); }
 int decode_nsplit(int cap, int window, int ring) {
     const int ch = decode_chunk(cap, ring);
     const int all = (cap + ch - 1) / ch;
@@ -1040,6 +1080,7 @@ cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, con
                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                             cudaStream_t st) {
     const int nsplit = decode_nsplit(cap, sm.window, sm.ring);
+    if (nsplit > COMB_MAX_SPLITS) return cudaErrorInvalidValue;
     const dim3 grid(nsplit, Hkv, B);
     cudaError_t e;
     switch (decode_chunk(cap, sm.ring)) {
@@ -1165,8 +1206,7 @@ void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* spl
 }
 
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring) {
-    const size_t nsplit = (size_t)decode_nsplit(cap, window, ring);
-    return (size_t)B * Hq * nsplit * (dh + 2) * sizeof(float);
+    return decode_records_floats(B, Hq, dh, decode_nsplit(cap, window, ring)) * sizeof(float);
 }
 
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,

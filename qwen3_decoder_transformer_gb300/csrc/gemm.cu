@@ -494,12 +494,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 
 // ------------------------------------------------------------------------------ skinny (decode)
-// Weight-streaming GEMM for decode batches. One CTA = 128 weight rows x one K chunk: warp 0 streams
-// 128x64 weight boxes and 64x64 activation boxes through an 8-stage ring, warp 1 issues
-// tcgen05.mma M=128 (weight rows) x N=MP (activation rows) x K=16 into MP TMEM columns, warps 2-5
-// read the accumulator (thread = weight row) and store it into this split's fp32 slice of the
-// workspace, or straight to the output when the K range is not split. With few rows the kernel is
-// bound by reading the weights once.
+// Weight-streaming GEMM for decode batches, persistent: a work item is 128 weight rows x one K chunk
+// (split), and each CTA walks items c, c + G, ... . Warp 0 streams 128x64 weight boxes and 64x64
+// activation boxes through an 8-stage ring without draining it between items, warp 1 issues
+// tcgen05.mma M=128 (weight rows) x N=MP (activation rows) x K=16 into one of two MP-column TMEM
+// accumulators, and warps 2-5 read a finished accumulator (thread = weight row) and store it into the
+// item's fp32 slice of the workspace (or straight to the output when K is not split) while the next
+// item accumulates. With few rows the kernel is bound by reading the weights once.
 constexpr int SK_STAGES = 8;
 constexpr int SK_W_BYTES = 128 * BK * 2;
 constexpr int SK_X_BYTES = kSkinnyRowsBox * BK * 2;
@@ -511,36 +512,39 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const SkinnyArgs args) {
     constexpr uint32_t IDESC = idesc_bf16(128, MP);
-    constexpr uint32_t TCOLS = MP < 32 ? 32 : MP;
+    constexpr uint32_t TCOLS = MP < 32 ? 32 : MP;  // columns of one accumulator; two are allocated
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SK_STAGES * SK_STAGE_BYTES);
     uint64_t* empty_bar = full_bar + SK_STAGES;
-    uint64_t* acc_full = empty_bar + SK_STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* acc_full = empty_bar + SK_STAGES;  // [2]
+    uint64_t* acc_empty = acc_full + 2;          // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * 128;
+    const int row_blocks = (args.N + 127) / 128;
+    const int items = row_blocks * args.splits;
     const int k_blocks = (args.K + BK - 1) / BK;
     const int per = (k_blocks + args.splits - 1) / args.splits;
-    const int kb0 = blockIdx.y * per, kb1 = min(k_blocks, kb0 + per);
-    const int nkb = max(0, kb1 - kb0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SK_STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        mbar_init(acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TCOLS);
+        tmem_alloc(tmem_slot, 2 * TCOLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -551,37 +555,63 @@ __global__ void __launch_bounds__(THREADS, 1)
     pdl_wait();
     pdl_trigger();
 
+    // K range [kb0, kb1) of an item (item = split * row_blocks + row block)
+    auto k_range = [&](int item, int& kb0, int& kb1) {
+        kb0 = (item / row_blocks) * per;
+        kb1 = min(k_blocks, kb0 + per);
+    };
     if (warp == 0 && lane == 0) {
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % SK_STAGES;
-            if (!mbar_wait(&empty_bar[s], ((i / SK_STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            uint8_t* st = smem + s * SK_STAGE_BYTES;
-            mbar_expect_tx(&full_bar[s], SK_STAGE_BYTES);
-            tma_load_2d(st, &tmW, &full_bar[s], (kb0 + i) * BK, n0);
-            tma_load_2d(st + SK_W_BYTES, &tmX, &full_bar[s], (kb0 + i) * BK, 0);
+        int it = 0;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+            int kb0, kb1;
+            k_range(item, kb0, kb1);
+            const int n0 = (item % row_blocks) * 128;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % SK_STAGES;
+                if (!mbar_wait(&empty_bar[s], ((it / SK_STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                uint8_t* st = smem + s * SK_STAGE_BYTES;
+                mbar_expect_tx(&full_bar[s], SK_STAGE_BYTES);
+                tma_load_2d(st, &tmW, &full_bar[s], kb * BK, n0);
+                tma_load_2d(st + SK_W_BYTES, &tmX, &full_bar[s], kb * BK, 0);
+            }
         }
     } else if (warp == 1 && lane == 0) {
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % SK_STAGES;
-            if (!mbar_wait(&full_bar[s], (i / SK_STAGES) & 1, abort_flag)) { ok = false; break; }
+        int it = 0, local = 0;
+        for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++local) {
+            int kb0, kb1;
+            k_range(item, kb0, kb1);
+            const int acc = local & 1;
+            if (!mbar_wait(&acc_empty[acc], ((local >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * SK_STAGE_BYTES);
-            const uint64_t wdesc = sdesc_kmajor_sw128(sa), xdesc = sdesc_kmajor_sw128(sa + SK_W_BYTES);
+            const uint32_t d = tmem + acc * TCOLS;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % SK_STAGES;
+                if (!mbar_wait(&full_bar[s], (it / SK_STAGES) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * SK_STAGE_BYTES);
+                const uint64_t wdesc = sdesc_kmajor_sw128(sa), xdesc = sdesc_kmajor_sw128(sa + SK_W_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) umma_bf16_ss(tmem, wdesc + 2 * k, xdesc + 2 * k, IDESC, (i | k) != 0);
-            umma_commit(&empty_bar[s]);
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16_ss(d, wdesc + 2 * k, xdesc + 2 * k, IDESC, (kb > kb0 || k > 0));
+                umma_commit(&empty_bar[s]);
+            }
+            if (!ok) break;
+            umma_commit(&acc_full[acc]);
         }
-        if (ok) umma_commit(acc_full);
     } else if (warp >= 2) {
         const int quarter = warp & 3;
-        const int n = n0 + quarter * 32 + lane;  // this thread's weight row = TMEM lane
-        const bool w = nkb == 0 || mbar_wait(acc_full, 0, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) {
-            ok = false;
-        } else if (nkb > 0) {
+        int local = 0;
+        for (int item = blockIdx.x; item < items; item += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const int n = (item % row_blocks) * 128 + quarter * 32 + lane;  // weight row = TMEM lane
+            const int split = item / row_blocks;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (local >> 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             uint32_t v[MP];
-            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16);
+            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + acc * TCOLS;
             if constexpr (MP == 16) {
                 tmem_ld_32x32b_x16(ta, v);
             } else {
@@ -590,13 +620,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld_32x32b_x32(ta + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
             }
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&acc_empty[acc]);
             if (n < args.N) {
                 if (args.splits == 1 && args.out) {
 #pragma unroll
                     for (int b = 0; b < MP; ++b)
                         if (b < args.M) args.out[(size_t)b * args.ldo + n] = __uint_as_float(v[b]);
                 } else {
-                    float* slice = args.ws + (size_t)blockIdx.y * args.M * args.ldw;
+                    float* slice = args.ws + (size_t)split * args.M * args.ldw;
 #pragma unroll
                     for (int b = 0; b < MP; ++b)
                         if (b < args.M) slice[(size_t)b * args.ldw + n] = __uint_as_float(v[b]);
@@ -613,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, TCOLS);
+        tmem_dealloc(tmem, 2 * TCOLS);
     }
 }
 
@@ -752,19 +784,33 @@ bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_
 }
 
 int skinny_splits(int N, int K) {
-    // enough CTAs for about two per SM, each with at least two 64-wide K blocks, at most 16 slices
-    const int tiles = (N + 127) / 128, k_blocks = (K + BK - 1) / BK;
-    int s = (2 * device_sm_count() + tiles - 1) / tiles;
-    s = std::min(std::min(s, 16), std::max(1, k_blocks / 2));
-    // no empty splits: every split must own at least one K block
-    const int per = (k_blocks + s - 1) / s;
-    return std::max(1, (k_blocks + per - 1) / per);
+    // The persistent kernel spreads tiles x splits items over the SMs; its time goes as the items of the
+    // busiest CTA times the K blocks of an item, plus the slices the finalize step reads back (counted
+    // for 64 rows, in 16-KB weight-block units per SM). Take the split count (<= 16, >= 2 K blocks per
+    // item) that minimises the sum, the fewest splits among equals.
+    const int tiles = (N + 127) / 128, k_blocks = (K + BK - 1) / BK, sms = device_sm_count();
+    int best = 1;
+    long long best_cost = -1;
+    for (int s = 1; s <= 16 && (s == 1 || k_blocks / s >= 2); ++s) {
+        const int per = (k_blocks + s - 1) / s;
+        const int used = (k_blocks + per - 1) / per;  // no empty splits
+        if (used != s) continue;
+        const long long rounds = ((long long)tiles * s + sms - 1) / sms;
+        const double slices = (double)s * kSkinnyRowsBox * N * 4 / ((double)sms * 128 * BK * 2);
+        const long long cost = rounds * per + (long long)(slices + 0.5);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 cudaError_t gemm_skinny_launch(const CUtensorMap& tw, const CUtensorMap& tx, const SkinnyArgs& a, cudaStream_t st) {
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
     if (a.M > kSkinnyRowsBox) return cudaErrorInvalidValue;
-    const dim3 grid((a.N + 127) / 128, a.splits);
+    const int items = (a.N + 127) / 128 * a.splits;
+    const dim3 grid(std::min(items, device_sm_count()));
     if (a.M <= 16) return launch_pdl(gemm_skinny_kernel<16>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);
     if (a.M <= 32) return launch_pdl(gemm_skinny_kernel<32>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);
     return launch_pdl(gemm_skinny_kernel<64>, grid, dim3(THREADS), SK_SMEM, st, tw, tx, a);

@@ -129,9 +129,11 @@ cudaError_t qknorm_rope_append_launch(const __nv_bfloat16* qkv, int B, int T, in
                                       __nv_bfloat16* vc, int cap, cudaStream_t st);
 // Decode finalize kernels: sum the `splits` fp32 slices of the skinny GEMM ([splits][M][ldw]) in order,
 // then apply the epilogue.
+// part: [M][finalize_norm_chunks(n)] floats; tick: [M] ints, zero on entry (left zero).
+int finalize_norm_chunks(int n);
 cudaError_t finalize_residual_rmsnorm_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* x,
                                              const __nv_bfloat16* g, int M, int n, float eps, __nv_bfloat16* y,
-                                             cudaStream_t st);
+                                             float* part, int* tick, cudaStream_t st);
 cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* h, int M, int F,
                                    cudaStream_t st);
 cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, int Hq, int Hkv, int dh, const __nv_bfloat16* qg,
@@ -162,6 +164,7 @@ int attn_heads_per_cta(int Hq, int Hkv);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
+// work: attn_decode_workspace() bytes of chunk records, merged by a second kernel.
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
                                cudaStream_t st);

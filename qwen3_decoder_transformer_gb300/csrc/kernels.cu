@@ -210,16 +210,80 @@ __global__ void qknorm_rope_append_kernel(const __nv_bfloat16* __restrict__ qkv,
 
 // x = bf16(x + bf16(acc)) for the decode rows (acc = the sum of the split-K slices, added in order),
 // then y = RMSNorm(x) with gain g: the residual add of o_proj / down_proj fused with the RMSNorm that
-// follows it (post-attention norm, the next layer's input norm, or the final norm). One 256-thread
-// CTA per row; each thread owns 8-element groups of the row and issues all its slice loads at once.
-constexpr int FIN_THREADS = 256;
+// follows it (post-attention norm, the next layer's input norm, or the final norm). A row is spread
+// over n / FIN_COLS CTAs: each adds its columns, stores x and its partial sum of squares; the last
+// CTA of the row (ticket) adds the partials in chunk order and normalises the whole row, so the
+// result does not depend on which CTA finishes last. part [M][chunks] and tick [M] are scratch; the
+// tickets are zero on entry and left zero.
+constexpr int FIN_THREADS = 128, FIN_COLS = FIN_THREADS * 4;
 __global__ void __launch_bounds__(FIN_THREADS)
     finalize_residual_rmsnorm_kernel(const float* __restrict__ ws, int splits, long long ldw,
+                                     __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int M, int n,
+                                     float eps, __nv_bfloat16* __restrict__ y, float* __restrict__ part,
+                                     int* __restrict__ tick) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[FIN_THREADS / 32];
+    __shared__ int last;
+    const int row = blockIdx.x, chunk = blockIdx.y, chunks = gridDim.y;
+    const int col = chunk * FIN_COLS + threadIdx.x * 4;
+    const size_t slice = (size_t)M * ldw;
+    float ss = 0.f;
+    if (col < n) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* wr = ws + (size_t)row * ldw + col;
+#pragma unroll 4
+        for (int sp = 0; sp < splits; ++sp) {
+            const float4 a = *reinterpret_cast<const float4*>(wr + sp * slice);
+            acc[0] += a.x, acc[1] += a.y, acc[2] += a.z, acc[3] += a.w;
+        }
+        uint2* xp = reinterpret_cast<uint2*>(x + (size_t)row * n + col);
+        const uint2 xv = *xp;
+        const uint32_t xw[2] = {xv.x, xv.y};
+        uint32_t o[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            o[e] = pack_bf16(bf16_lo(xw[e]) + rbf(acc[2 * e]), bf16_hi(xw[e]) + rbf(acc[2 * e + 1]));
+            const float rl = bf16_lo(o[e]), rh = bf16_hi(o[e]);
+            ss = fmaf(rl, rl, ss);
+            ss = fmaf(rh, rh, ss);
+        }
+        *xp = make_uint2(o[0], o[1]);
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < FIN_THREADS / 32; ++w) tot += red[w];
+        part[(size_t)row * chunks + chunk] = tot;
+        __threadfence();
+        last = atomicAdd(&tick[row], 1) == chunks - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    float tot = 0.f;
+    for (int c = 0; c < chunks; ++c) tot += part[(size_t)row * chunks + c];  // fixed order
+    const float r = __frsqrt_rn(tot / (float)n + eps);
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * n);
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * n);
+    for (int v = threadIdx.x; v < n / 8; v += FIN_THREADS) yr[v] = norm8(xr[v], __ldg(gr + v), r);
+    if (threadIdx.x == 0) tick[row] = 0;  // ready for the next launch
+}
+
+// The same with one 256-thread CTA per row (rows of up to 4096 elements stay in registers); used when
+// there are enough rows to fill the GPU without splitting them.
+constexpr int FIN_ROW_THREADS = 256;
+__global__ void __launch_bounds__(FIN_ROW_THREADS)
+    finalize_residual_rmsnorm_row_kernel(const float* __restrict__ ws, int splits, long long ldw,
                                      __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int M, int n,
                                      float eps, __nv_bfloat16* __restrict__ y) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float red[FIN_THREADS / 32];
+    __shared__ float red[FIN_ROW_THREADS / 32];
     const int row = blockIdx.x;
     constexpr int MAXG = 2;  // 8-element groups per thread: rows up to 256 * 8 * 2 = 4096 elements
     uint4 keep[MAXG];
@@ -228,7 +292,7 @@ __global__ void __launch_bounds__(FIN_THREADS)
     const size_t slice = (size_t)M * ldw;
 #pragma unroll
     for (int i = 0; i < MAXG; ++i) {
-        const int v = threadIdx.x + FIN_THREADS * i;
+        const int v = threadIdx.x + FIN_ROW_THREADS * i;
         if (v < n / 8) {
             const uint4 xv = xr[v];
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -258,13 +322,13 @@ __global__ void __launch_bounds__(FIN_THREADS)
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < FIN_THREADS / 32; ++w) tot += red[w];
+    for (int w = 0; w < FIN_ROW_THREADS / 32; ++w) tot += red[w];
     const float r = __frsqrt_rn(tot / (float)n + eps);
     const uint4* gr = reinterpret_cast<const uint4*>(g);
     uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * n);
 #pragma unroll
     for (int i = 0; i < MAXG; ++i) {
-        const int v = threadIdx.x + FIN_THREADS * i;
+        const int v = threadIdx.x + FIN_ROW_THREADS * i;
         if (v < n / 8) yr[v] = norm8(keep[i], __ldg(gr + v), r);
     }
 }
@@ -474,13 +538,18 @@ cudaError_t add_len_launch(int* len, int delta, cudaStream_t st) {
     return launch_pdl(add_len_kernel, dim3(1), dim3(1), 0, st, len, delta);
 }
 
+int finalize_norm_chunks(int n) { return (n + FIN_COLS - 1) / FIN_COLS; }
+
 cudaError_t finalize_residual_rmsnorm_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* x,
                                              const __nv_bfloat16* g, int M, int n, float eps, __nv_bfloat16* y,
-                                             cudaStream_t st) {
+                                             float* part, int* tick, cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
-    if (n % 8 || n > 4096 || ldw % 4) return cudaErrorInvalidValue;
-    return launch_pdl(finalize_residual_rmsnorm_kernel, dim3(M), dim3(FIN_THREADS), 0, st, ws, splits, ldw, x, g, M, n,
-                      eps, y);
+    if (n % 8 || ldw % 4 || !part || !tick) return cudaErrorInvalidValue;
+    if (M >= 32 && n <= 4096)
+        return launch_pdl(finalize_residual_rmsnorm_row_kernel, dim3(M), dim3(FIN_ROW_THREADS), 0, st, ws, splits, ldw, x,
+                          g, M, n, eps, y);
+    return launch_pdl(finalize_residual_rmsnorm_kernel, dim3(M, finalize_norm_chunks(n)), dim3(FIN_THREADS), 0, st, ws,
+                      splits, ldw, x, g, M, n, eps, y, part, tick);
 }
 
 cudaError_t finalize_swiglu_launch(const float* ws, int splits, long long ldw, __nv_bfloat16* h, int M, int F,

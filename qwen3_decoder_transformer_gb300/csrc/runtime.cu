@@ -88,6 +88,8 @@ struct qwen3_ctx {
     bf16 *x = nullptr, *xn = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *hn = nullptr;
     float* dec_work = nullptr;
     float* skinny_ws = nullptr;  // decode split-K GEMM accumulator [64][max N] fp32, kept zero between uses
+    float* fin_part = nullptr;   // decode residual + RMSNorm: per-(row, chunk) partial sums of squares
+    int* fin_tick = nullptr;     // and per-row tickets (zero between launches)
     long long skinny_ld = 0;
     CUtensorMap tX_xn, tX_attn, tX_h, tX_hn;  // decode activation maps (64-row boxes)
     float* attn_ws = nullptr;  // split prefill attention: tickets + partials (zeroed at init)
@@ -216,7 +218,7 @@ int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits
         TRY(skinny(c, K_GEMM_O, c->tB_o[l], c->tX_attn, B, d, c->q_width, nullptr, s_o, st));
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
             return finalize_residual_rmsnorm_launch(c->skinny_ws, s_o, d, c->x, c->post_norm[l], B, d, g.rms_eps, c->xn,
-                                                    st);
+                                                    c->fin_part, c->fin_tick, st);
         }));
         TRY(skinny(c, K_GEMM_GATEUP, c->tB_gu[l], c->tX_xn, B, 2 * F, d, nullptr, s_gu, st));
         TRY(timed(c, K_FINALIZE, 1, st,
@@ -225,7 +227,7 @@ int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits
         const bool last = l == L - 1;
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
             return finalize_residual_rmsnorm_launch(c->skinny_ws, s_dn, d, c->x, last ? c->final_norm : c->in_norm[l + 1],
-                                                    B, d, g.rms_eps, last ? c->hn : c->xn, st);
+                                                    B, d, g.rms_eps, last ? c->hn : c->xn, c->fin_part, c->fin_tick, st);
         }));
         if (l == c->tap_layer && c->tap_out)
             if (cudaMemcpyAsync(c->tap_out, c->x, (size_t)B * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -341,7 +343,7 @@ void release(qwen3_ctx* c) {
     void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
                     c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->skinny_ws, c->d_len,
                     c->d_err, c->d_ids_buf, c->d_logits_buf, c->d_seq, c->gen_logits, c->gen_done, c->gen_next,
-                    c->gen_alive};
+                    c->gen_alive, c->fin_part, c->fin_tick};
     for (void* p : bufs)
         if (p) cudaFree(p);
     if (c->h_alive) cudaFreeHost(c->h_alive);
@@ -486,7 +488,10 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
             std::max((long long)skinny_splits(c->qkv_n, d) * c->qkv_n, (long long)skinny_splits(d, c->q_width) * d),
             std::max((long long)skinny_splits(2 * F, d) * 2 * F, (long long)skinny_splits(d, F) * d));
         c->skinny_ld = need;
-        ok = dmalloc(&c->skinny_ws, (size_t)kSkinnyRowsBox * need) == cudaSuccess;
+        ok = dmalloc(&c->skinny_ws, (size_t)kSkinnyRowsBox * need) == cudaSuccess &&
+             dmalloc(&c->fin_part, (size_t)kSkinnyRowsBox * finalize_norm_chunks(d)) == cudaSuccess &&
+             dmalloc(&c->fin_tick, (size_t)kSkinnyRowsBox) == cudaSuccess &&
+             cudaMemsetAsync(c->fin_tick, 0, (size_t)kSkinnyRowsBox * sizeof(int), st) == cudaSuccess;
     }
     // split-attention workspace: sized for the largest split the planner can choose (work items up to
     // the SM count, up to 4 chunks each)

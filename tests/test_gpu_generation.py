@@ -272,7 +272,7 @@ def test_decode_attention_layout_op(bd):
     ps, psh, pads = 300, 256, [0, 17, 250]
     meta = np.array([ps, psh] + pads, dtype=np.int32)
     out = torch.empty(B, Hq * dh, dtype=torch.bfloat16, device="cuda")
-    work = torch.empty(bd.attention_decode_workspace(B, Hq, dh, cap) // 4 + 1, dtype=torch.float32, device="cuda")
+    work = torch.zeros(bd.attention_decode_workspace(B, Hq, dh, cap) // 4 + 1, dtype=torch.float32, device="cuda")
     len_t = torch.tensor([n - 1], dtype=torch.int32, device="cuda")
     bd.op_attention_decode(synth.from_numpy_bits(q, "cuda"), synth.from_numpy_bits(kc, "cuda"),
                            synth.from_numpy_bits(vc, "cuda"), len_t, work, out,

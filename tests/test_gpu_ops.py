@@ -298,11 +298,14 @@ def test_attention_decode(bd, Bq, Hq, Hkv, dh, n):
     vc = rand_bf16(rng, (Bq, Hkv, cap, dh))
     kc[:, :, n:] = 0x7FC0
     vc[:, :, n:] = 0x7FC0
-    work = torch.empty(bd.attention_decode_workspace(Bq, Hq, dh, cap) // 4, dtype=torch.float32, device="cuda")
+    work = torch.zeros(bd.attention_decode_workspace(Bq, Hq, dh, cap) // 4, dtype=torch.float32, device="cuda")
     out = torch.empty(Bq, Hq * dh, dtype=torch.bfloat16, device="cuda")
     len_t = torch.tensor([n - 1], dtype=torch.int32, device="cuda")
     bd.op_attention_decode(dev(q), dev(kc), dev(vc), len_t, work, out)
+    first = out.clone()
+    bd.op_attention_decode(dev(q), dev(kc), dev(vc), len_t, work, out)  # merge counters were left at zero
     torch.cuda.synchronize()
+    assert torch.equal(first, out)
     ref = np.stack([O.attention_gqa_row_f64(q[b], kc[b], vc[b], n).ravel() for b in range(Bq)])
     got = widen(bits(out))
     assert np.isfinite(got).all()

@@ -47,7 +47,7 @@ def test_noalloc_matches_workspace_entry_point(L):
     cases = [(1, 4, 16, 8, 128, 4097, 4224), (2, 2, 32, 8, 128, 1000, 1100)]
     for seed, Bq, Hq, Hkv, dh, n, cap in cases:
         q, kc, vc, len_t = _case(seed, Bq, Hq, Hkv, dh, n, cap)
-        work = torch.empty(binding.attention_decode_workspace(Bq, Hq, dh, cap) // 4, dtype=torch.float32,
+        work = torch.zeros(binding.attention_decode_workspace(Bq, Hq, dh, cap) // 4, dtype=torch.float32,
                            device="cuda")
         ref = torch.empty(Bq, Hq * dh, dtype=torch.bfloat16, device="cuda")
         binding.op_attention_decode(q, kc, vc, len_t, work, ref)
