@@ -19,7 +19,6 @@
 namespace q3 {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
 
 // --------------------------------------------------------------------------- prefill (tcgen05)
 // One CTA = 128 query rows of NH query heads that share one kv head. Tensor memory holds two

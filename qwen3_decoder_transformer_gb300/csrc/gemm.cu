@@ -163,11 +163,17 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
                     uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
+                        // columns j, j + 1 in paired fp32: silu(g) = g / (1 + 2^(-g log2 e))
                         const int j = q * 8 + 2 * e;
-                        const float g0 = rbf(__uint_as_float(g[j])), g1 = rbf(__uint_as_float(g[j + 1]));
-                        const float s0 = rbf(__fdividef(g0, 1.0f + __expf(-g0)));
-                        const float s1 = rbf(__fdividef(g1, 1.0f + __expf(-g1)));
-                        wv[e] = pack_bf16(s0 * rbf(__uint_as_float(u[j])), s1 * rbf(__uint_as_float(u[j + 1])));
+                        const uint32_t gb = pack_bf16(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
+                        const float2 gf = make_float2(bf16_lo(gb), bf16_hi(gb));
+                        const float2 t = mul2(gf, make_float2(-kLog2e, -kLog2e));
+                        const float2 den = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+                        const float2 sv = mul2(gf, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+                        const uint32_t sb = pack_bf16(sv.x, sv.y);
+                        const uint32_t ub = pack_bf16(__uint_as_float(u[j]), __uint_as_float(u[j + 1]));
+                        const float2 pv = mul2(make_float2(bf16_lo(sb), bf16_hi(sb)), make_float2(bf16_lo(ub), bf16_hi(ub)));
+                        wv[e] = pack_bf16(pv.x, pv.y);
                     }
                     *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
@@ -394,6 +400,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     bool ok = true;
+    // B boxes of the first tile's first stages, issued before the wait on the previous kernel when
+    // the weights do not depend on it (their DRAM latency then overlaps that kernel's tail)
+    auto load_b = [&](uint8_t* sa, uint64_t* bar, int kb, int n0) {
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j)
+#pragma unroll
+            for (int nb = 0; nb < BN / kGemmBoxN; ++nb)
+                tma_load_2d(sa + KSUB * A_BYTES + j * C::B_BYTES + nb * kGemmBoxN * BK * 2, &tmB, bar,
+                            (kb * KSUB + j) * BK, n0 + nb * kGemmBoxN);
+    };
+    int pre = 0;
+    if (warp == 0 && lane == 0 && args.b_independent && (int)blockIdx.x < total) {
+        const Tile tl = tile_of<BN>(blockIdx.x, m_tiles, n_tiles);
+        pre = min(STAGES, k_blocks);
+        for (int kb = 0; kb < pre; ++kb) {
+            mbar_expect_tx(&full_bar[kb], STAGE_BYTES);
+            load_b(smem + kb * STAGE_BYTES, &full_bar[kb], kb, tl.n0);
+        }
+    }
     pdl_wait();  // inputs of this GEMM come from the previous kernel
     pdl_trigger();
 
@@ -405,18 +430,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
-                if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) { ok = false; break; }
                 uint8_t* sa = smem + s * STAGE_BYTES;
-                mbar_expect_tx(&full_bar[s], STAGE_BYTES);
-#pragma unroll
-                for (int j = 0; j < KSUB; ++j) {  // boxes past K read as zeros
-                    const int kx = (kb * KSUB + j) * BK;
-                    tma_load_2d(sa + j * A_BYTES, &tmA, &full_bar[s], kx, tl.m0);
-#pragma unroll
-                    for (int nb = 0; nb < BN / kGemmBoxN; ++nb)
-                        tma_load_2d(sa + KSUB * A_BYTES + j * C::B_BYTES + nb * kGemmBoxN * BK * 2, &tmB, &full_bar[s], kx,
-                                    tl.n0 + nb * kGemmBoxN);
+                if (it >= pre) {
+                    if (!mbar_wait(&empty_bar[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(&full_bar[s], STAGE_BYTES);
+                    load_b(sa, &full_bar[s], kb, tl.n0);
                 }
+#pragma unroll
+                for (int j = 0; j < KSUB; ++j)  // boxes past K read as zeros
+                    tma_load_2d(sa + j * A_BYTES, &tmA, &full_bar[s], (kb * KSUB + j) * BK, tl.m0);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -476,8 +498,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
-        // the last TMA stores must finish before the CTA exits
-        if (threadIdx.x == EPI_LEADER) bulk_wait_all();
+        // shared memory must outlive the reads of the last TMA stores; their global writes complete
+        // with the grid, which the next kernel's dependency wait (or stream order) covers
+        if (threadIdx.x == EPI_LEADER) bulk_wait_read();
     }
     if (!ok) {
         *abort_flag = 1;
@@ -552,14 +575,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
-    pdl_wait();
-    pdl_trigger();
 
     // K range [kb0, kb1) of an item (item = split * row_blocks + row block)
     auto k_range = [&](int item, int& kb0, int& kb1) {
         kb0 = (item / row_blocks) * per;
         kb1 = min(k_blocks, kb0 + per);
     };
+    // weight boxes of the first item's first stages, issued before the wait on the previous kernel
+    // when the weights do not depend on it
+    int pre = 0;
+    if (warp == 0 && lane == 0 && args.w_independent && (int)blockIdx.x < items) {
+        int kb0, kb1;
+        k_range(blockIdx.x, kb0, kb1);
+        const int n0 = (blockIdx.x % row_blocks) * 128;
+        pre = max(0, min(SK_STAGES, kb1 - kb0));
+        for (int i = 0; i < pre; ++i) {
+            mbar_expect_tx(&full_bar[i], SK_STAGE_BYTES);
+            tma_load_2d(smem + i * SK_STAGE_BYTES, &tmW, &full_bar[i], (kb0 + i) * BK, n0);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+
     if (warp == 0 && lane == 0) {
         int it = 0;
         for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
@@ -568,10 +605,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int n0 = (item % row_blocks) * 128;
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % SK_STAGES;
-                if (!mbar_wait(&empty_bar[s], ((it / SK_STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 uint8_t* st = smem + s * SK_STAGE_BYTES;
-                mbar_expect_tx(&full_bar[s], SK_STAGE_BYTES);
-                tma_load_2d(st, &tmW, &full_bar[s], kb * BK, n0);
+                if (it >= pre) {
+                    if (!mbar_wait(&empty_bar[s], ((it / SK_STAGES) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(&full_bar[s], SK_STAGE_BYTES);
+                    tma_load_2d(st, &tmW, &full_bar[s], kb * BK, n0);
+                }
                 tma_load_2d(st + SK_W_BYTES, &tmX, &full_bar[s], kb * BK, 0);
             }
         }

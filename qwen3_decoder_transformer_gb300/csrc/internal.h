@@ -72,6 +72,7 @@ cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st);
 struct GemmArgs {
     int M, N, K;
     int epi;
+    int b_independent;  // nonzero: B is not written by the previous kernel on the stream (model weights)
     void* C;
     long long ldc;
     const __nv_bfloat16* R;
@@ -109,6 +110,7 @@ struct SkinnyArgs {
     float* out;
     long long ldo;
     int* err;
+    int w_independent;  // nonzero: the weights are not written by the previous kernel on the stream
 };
 constexpr int kSkinnyRowsBox = 64;  // TMA box rows of the activation operand
 bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_t K);

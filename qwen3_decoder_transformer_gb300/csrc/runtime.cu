@@ -171,7 +171,7 @@ int timed(qwen3_ctx* c, int cls, int launches, cudaStream_t st, F&& fn) {
 int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tc,
          const CUtensorMap* tr, int M, int N, int K, int epi, void* C, long long ldc, const bf16* R, long long ldr,
          cudaStream_t st) {
-    GemmArgs a{M, N, K, epi, C, ldc, R, ldr, c->d_err, {}};
+    GemmArgs a{M, N, K, epi, 1, C, ldc, R, ldr, c->d_err, {}};
     GemmMaps m;
     std::memset(&m, 0, sizeof(m));
     m.a = ta;
@@ -187,7 +187,7 @@ bf16* layer_v(qwen3_ctx* c, int l) { return c->vcache + (size_t)l * c->layer_ele
 
 int skinny(qwen3_ctx* c, int cls, const CUtensorMap& tw, const CUtensorMap& tx, int M, int N, int K, float* out,
            int splits, cudaStream_t st) {
-    SkinnyArgs a{M, N, K, splits, c->skinny_ws, N, out, N, c->d_err};
+    SkinnyArgs a{M, N, K, splits, c->skinny_ws, N, out, N, c->d_err, 1};
     return timed(c, cls, 1, st, [&] { return gemm_skinny_launch(tw, tx, a, st); });
 }
 
@@ -258,7 +258,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
                   [&] { return rmsnorm_launch(c->x, c->in_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
         {
             // fused: Q/K/V projection, q_norm/k_norm, RoPE, Q to attention layout, K/V into the cache
-            GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, nullptr, 0, nullptr, 0, c->d_err,
+            GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, 1, nullptr, 0, nullptr, 0, c->d_err,
                        QkvRopeArgs{c->q_norm[l], c->k_norm[l], c->rope, c->d_len, c->q, layer_k(c, l), layer_v(c, l), T,
                                    g.n_q_heads, g.n_kv_heads, dh, c->slots, g.rms_eps, c->d_seq, c->ring != 0}};
             GemmMaps m;
@@ -854,7 +854,7 @@ int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, vo
     if (!encode_tmap_out(&m.c, C, epi == EPI_F32, out_cols, (uint64_t)M, (uint64_t)ldc)) return QWEN3_E_CUDA;
     if (epi == EPI_RESIDUAL && !encode_tmap_out(&m.r, R, false, (uint64_t)N, (uint64_t)M, (uint64_t)ldr))
         return QWEN3_E_CUDA;
-    GemmArgs a{M, N, K, epi, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
+    GemmArgs a{M, N, K, epi, 0, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
     return gemm_launch(m, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
@@ -872,7 +872,7 @@ int qwen3_op_gemm_skinny(const void* A, const void* B, int M, int N, int K, int 
     if (!encode_tmap_bf16_2d(&tw, B, K, N, (uint64_t)K * 2, kGemmBK, kGemmBoxN) ||
         !encode_skinny_x_map(&tx, A, (uint64_t)M, (uint64_t)K))
         return QWEN3_E_CUDA;
-    SkinnyArgs a{M, N, K, splits, slices, N, splits == 1 ? out : nullptr, N, err};
+    SkinnyArgs a{M, N, K, splits, slices, N, splits == 1 ? out : nullptr, N, err, 0};
     return gemm_skinny_launch(tw, tx, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
