@@ -48,12 +48,16 @@ struct TimedLaunch {
     cudaEvent_t start, stop;
 };
 
-struct DecodeGraph {
-    int B;
+// A captured forward pass. Everything the host decides for a call is in the key: the shape, the
+// flags, the device buffers baked into the launches, and (prefill) the cache length, which picks the
+// attention split; the cache length itself, the sequence layout and the weights are read on the device.
+struct ForwardGraph {
+    int B, T, flags, decode, len;
     const int32_t* ids;
     float* logits;
     cudaGraphExec_t exec;
 };
+constexpr size_t kMaxGraphs = 16;  // oldest captured pass is dropped beyond this
 
 bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -116,8 +120,8 @@ struct qwen3_ctx {
     std::vector<CUtensorMap> tB_qkv, tB_o, tB_gu, tB_down;
     std::vector<CUtensorMap> tK3, tV3;  // per-layer cache maps [max_batch*Hkv][cap][dh] for the fused QKV stores
     CUtensorMap tB_head;
-    // decode graphs
-    std::vector<DecodeGraph> graphs;
+    // captured forward passes (replayed when a call repeats)
+    std::vector<ForwardGraph> graphs;
     cudaStream_t cap_stream = nullptr;
     // timing
     bool timing = false;
@@ -312,6 +316,46 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
              nullptr, 0, st));
     TRY(timed(c, K_LENGTH, 1, st, [&] { return add_len_launch(c->d_len, T, st); }));
     return QWEN3_OK;
+}
+
+// Enqueue one forward pass, replaying a captured CUDA graph of it when the same call was made before
+// (the whole pass is then one launch for the host). Timing, the debug tap and a caller's stream that is
+// itself being captured run it eagerly.
+int run_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logits, int flags, bool decode,
+                cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return QWEN3_E_CUDA;
+    // the caller's own capture records the launches themselves
+    if (c->timing || c->tap_layer >= 0 || cs != cudaStreamCaptureStatusNone)
+        return enqueue_forward(c, ids, B, T, logits, flags, decode, st);
+    const int len = decode ? -1 : c->len;
+    ForwardGraph* gph = nullptr;
+    for (auto& x : c->graphs)
+        if (x.B == B && x.T == T && x.flags == flags && x.decode == (int)decode && x.len == len && x.ids == ids &&
+            x.logits == logits)
+            gph = &x;
+    if (!gph) {
+        cudaGraph_t graph = nullptr;
+        cudaGraphExec_t exec = nullptr;
+        if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return QWEN3_E_CUDA;
+        const int rc = enqueue_forward(c, ids, B, T, logits, flags, decode, c->cap_stream);
+        cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+        if (rc != QWEN3_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return rc;
+        }
+        if (e != cudaSuccess) return QWEN3_E_CUDA;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return QWEN3_E_CUDA;
+        if (c->graphs.size() >= kMaxGraphs) {
+            cudaGraphExecDestroy(c->graphs.front().exec);
+            c->graphs.erase(c->graphs.begin());
+        }
+        c->graphs.push_back({B, T, flags, (int)decode, len, ids, logits, exec});
+        gph = &c->graphs.back();
+    }
+    return cudaGraphLaunch(gph->exec, st) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 
 int check_call(qwen3_ctx* c, int B, int T) {
@@ -571,7 +615,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
 int qwen3_prefill(qwen3_ctx* c, const int32_t* d_ids, int B, int T, float* d_logits, int flags, void* stream) {
     if (!c || !d_ids || !d_logits) return QWEN3_E_ARG;
     TRY(check_call(c, B, T));
-    TRY(enqueue_forward(c, d_ids, B, T, d_logits, flags, false, static_cast<cudaStream_t>(stream)));
+    TRY(run_forward(c, d_ids, B, T, d_logits, flags, false, static_cast<cudaStream_t>(stream)));
     c->len += T;
     c->batch = B;
     return QWEN3_OK;
@@ -580,30 +624,7 @@ int qwen3_prefill(qwen3_ctx* c, const int32_t* d_ids, int B, int T, float* d_log
 int qwen3_decode_step(qwen3_ctx* c, const int32_t* d_ids, int B, float* d_logits, void* stream) {
     if (!c || !d_ids || !d_logits) return QWEN3_E_ARG;
     TRY(check_call(c, B, 1));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (c->timing || c->tap_layer >= 0) {
-        TRY(enqueue_forward(c, d_ids, B, 1, d_logits, 0, true, st));
-    } else {
-        DecodeGraph* gph = nullptr;
-        for (auto& x : c->graphs)
-            if (x.B == B && x.ids == d_ids && x.logits == d_logits) gph = &x;
-        if (!gph) {
-            cudaGraph_t graph = nullptr;
-            cudaGraphExec_t exec = nullptr;
-            if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
-                return QWEN3_E_CUDA;
-            int rc = enqueue_forward(c, d_ids, B, 1, d_logits, 0, true, c->cap_stream);
-            cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
-            if (rc != QWEN3_OK) return rc;
-            if (e != cudaSuccess) return QWEN3_E_CUDA;
-            e = cudaGraphInstantiate(&exec, graph, 0);
-            cudaGraphDestroy(graph);
-            if (e != cudaSuccess) return QWEN3_E_CUDA;
-            c->graphs.push_back({B, d_ids, d_logits, exec});
-            gph = &c->graphs.back();
-        }
-        if (cudaGraphLaunch(gph->exec, st) != cudaSuccess) return QWEN3_E_CUDA;
-    }
+    TRY(run_forward(c, d_ids, B, 1, d_logits, 0, true, static_cast<cudaStream_t>(stream)));
     c->len += 1;
     c->batch = B;
     return QWEN3_OK;
@@ -628,7 +649,7 @@ int qwen3_prefill_padded(qwen3_ctx* c, const int32_t* d_ids, const int32_t* h_re
         TRY(write_seq(c, v, st));
         c->padded = true;
     }
-    TRY(enqueue_forward(c, d_ids, B, T, d_logits, flags, false, st));
+    TRY(run_forward(c, d_ids, B, T, d_logits, flags, false, st));
     c->len += T;
     c->batch = B;
     return QWEN3_OK;
