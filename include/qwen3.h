@@ -232,6 +232,22 @@ QWEN3_API int qwen3_op_rmsnorm(const void* d_x, const void* d_gamma, int rows, i
 QWEN3_API int qwen3_op_gemm(const void* d_A, const void* d_B, int M, int N, int K, int epilogue, void* d_C,
                   int ldc, const void* d_R, int ldr, int* d_err, void* stream);
 
+/* Residual GEMM fused with the next RMSNorm (the pre-norm block: each residual add is followed by
+ * the next sub-layer's RMSNorm): X [M, N] bf16 (row stride N) is updated in place to
+ * bf16(X + bf16(A B^T)), then Y [M, N] bf16 = bf16(gamma * bf16(X * rsqrt(mean(X^2) + eps))) over
+ * each full updated row, the mean in fp32. The N / BN column tiles of a row block (BN = 128 or 256,
+ * the tile width the library picks for [M, N]) run concurrently in one cooperative launch and
+ * exchange per-row partial sums; qwen3_gemm_norm_supported says whether a shape qualifies (N a
+ * multiple of the tile width, at most 8 tiles). d_part is scratch of qwen3_gemm_norm_part_floats(M)
+ * 4-byte words, zeroed before the first call and otherwise left to the library (each call leaves its
+ * counters zero; after a call that set d_err, zero it again). Returns QWEN3_E_ARG for an unsupported
+ * shape; d_err receives bit 2 if a bounded wait gave up. */
+QWEN3_API int qwen3_gemm_norm_supported(int M, int N);
+QWEN3_API size_t qwen3_gemm_norm_part_floats(int M);
+QWEN3_API int qwen3_op_gemm_residual_norm(const void* d_A, const void* d_B, int M, int N, int K, void* d_X,
+                                          const void* d_gamma, float eps, void* d_Y, float* d_part, int* d_err,
+                                          void* stream);
+
 /* Weight-streaming GEMM for a few rows (decode batches, 1 <= M <= 64): acc[b][n] = sum_k A[b][k] B[n][k]
  * in fp32 on the tensor cores, with the weights B [N, K] as the 128-row MMA operand and the K range
  * split over `splits` CTAs per 128 weight rows (qwen3_gemm_skinny_splits gives the runtime's choice).

@@ -82,6 +82,10 @@ def lib() -> ctypes.CDLL:
     L.qwen3_op_rmsnorm.argtypes = [_vp, _vp, i, i, i, i, ctypes.c_float, _vp, _vp]
     L.qwen3_op_gemm.argtypes = [_vp, _vp, i, i, i, i, _vp, i, _vp, i, _vp, _vp]
     L.qwen3_op_pack_gate_up.argtypes = [_vp, _vp, i, i, _vp, _vp]
+    L.qwen3_gemm_norm_supported.argtypes = [i, i]
+    L.qwen3_gemm_norm_part_floats.restype = sz
+    L.qwen3_gemm_norm_part_floats.argtypes = [i]
+    L.qwen3_op_gemm_residual_norm.argtypes = [_vp, _vp, i, i, i, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
     L.qwen3_gemm_skinny_splits.argtypes = [i, i]
     L.qwen3_op_gemm_skinny.argtypes = [_vp, _vp, i, i, i, i, _vp, _vp, _vp, _vp]
     L.qwen3_op_rope_table.argtypes = [ctypes.c_float, i, i, _vp, _vp]
@@ -264,6 +268,22 @@ def op_gemm(A, B, epi, C, R=None, err=None, stream=None):
     N = B.shape[0]
     check(lib().qwen3_op_gemm(_p(A), _p(B), M, N, K, epi, _p(C), C.shape[1], _p(R),
                               R.shape[1] if R is not None else 0, _p(err), _stream(stream)))
+
+
+def gemm_norm_supported(M, N) -> bool:
+    return bool(lib().qwen3_gemm_norm_supported(M, N))
+
+
+def gemm_norm_part_floats(M) -> int:
+    return lib().qwen3_gemm_norm_part_floats(M)
+
+
+def op_gemm_residual_norm(A, B, X, gamma, eps, Y, part, err=None, stream=None):
+    """X [M, N] += A B^T in place (bf16 rounding as QWEN3_EPI_RESIDUAL), Y = RMSNorm(X; gamma)."""
+    M, K = A.shape
+    N = B.shape[0]
+    check(lib().qwen3_op_gemm_residual_norm(_p(A), _p(B), M, N, K, _p(X), _p(gamma), eps, _p(Y), _p(part), _p(err),
+                                            _stream(stream)))
 
 
 def gemm_skinny_splits(N, K) -> int:

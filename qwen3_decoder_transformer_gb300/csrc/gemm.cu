@@ -228,6 +228,114 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
     return ok;
 }
 
+// Residual epilogue followed by the next RMSNorm ("A modern architecture: Qwen3", section RMSNorm and
+// the pre-norm block) for one of the csize column tiles of a row block, which run concurrently on
+// different CTAs: X = bf16(R + bf16(acc)) is stored as in EPI_RESIDUAL and kept in tensor memory
+// (packed over the accumulator's own columns); each row's sum of squares over the tile goes to
+// part[row block][rank][row]. When all csize CTAs have arrived on the row block's counter, the
+// partial sums are added in rank order (the same in every CTA), r = rsqrt(sum / N + eps), and
+// Y = bf16(gamma * bf16(X * r)) is stored through the v map. The accumulator is released last.
+template <int BN>
+__device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmR,
+                                                       const CUtensorMap* tmY, uint8_t* stg, EpiSync& es, uint32_t tacc,
+                                                       int r, int m0, int n0, int rank, int csize, uint64_t* acc_empty,
+                                                       uint64_t* acc_full, uint32_t aph, volatile int* abort_flag) {
+    constexpr int PASSES = BN / 128;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int p = 0; p < PASSES; ++p) {
+        stg_acquire();
+        if (threadIdx.x == EPI_LEADER) {
+            mbar_expect_tx(es.res_bar, STG_BYTES);
+            tma_load_2d(stg, tmR, es.res_bar, n0 + p * 128, m0);
+            tma_load_2d(stg + 16384, tmR, es.res_bar, n0 + p * 128 + 64, m0);
+        }
+        if (p == 0) {
+            const bool w = mbar_wait(acc_full, aph, abort_flag);
+            if (!epi_agree(w, es.fail)) return false;
+            tc_fence_after();
+        }
+        uint32_t v[128];
+        tmem_ld_128(tacc + p * 128, v);
+        {
+            const bool w = mbar_wait(es.res_bar, es.res_phase & 1, abort_flag);
+            ++es.res_phase;
+            if (!epi_agree(w, es.fail)) return false;
+        }
+        uint32_t xw[64];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, u));
+            const uint4 q = *cp;
+            const uint32_t rr[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t xv = pack_bf16(bf16_lo(rr[e]) + rbf(__uint_as_float(v[8 * u + 2 * e])),
+                                              bf16_hi(rr[e]) + rbf(__uint_as_float(v[8 * u + 2 * e + 1])));
+                xw[4 * u + e] = xv;
+                ss = fmaf(bf16_lo(xv), bf16_lo(xv), ss);
+                ss = fmaf(bf16_hi(xv), bf16_hi(xv), ss);
+            }
+            *cp = make_uint4(xw[4 * u], xw[4 * u + 1], xw[4 * u + 2], xw[4 * u + 3]);
+        }
+        tmem_st_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
+        tmem_st_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
+        stg_store(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
+    }
+    tmem_st_wait();
+    // this tile's partial sums of squares, then meet the row block's other column tiles
+    const size_t rb = (size_t)(m0 / BM);
+    a.norm.part[(rb * csize + rank) * BM + r] = ss;
+    named_barrier(1, 128);
+    bool met = true;
+    if (threadIdx.x == EPI_LEADER) {
+        unsigned* arrive = a.norm.count + 2 * rb;
+        __threadfence();  // the partial sums are visible before the arrival
+        atomicAdd(arrive, 1u);
+        const uint64_t t0 = globaltimer();
+        for (uint32_t i = 1; ld_acquire_gpu(arrive) < (unsigned)csize; ++i) {
+            if ((i & 63u) == 0 && (*abort_flag || globaltimer() - t0 > kWaitTimeoutNs)) {
+                met = false;
+                break;
+            }
+        }
+        // the last CTA to leave resets the counters for the next launch
+        if (met && atomicAdd(arrive + 1, 1u) == (unsigned)csize - 1) {
+            arrive[0] = 0;
+            arrive[1] = 0;
+        }
+    }
+    if (!epi_agree(met, es.fail)) return false;
+    float tot = 0.f;
+    for (int q = 0; q < csize; ++q) tot += __ldcg(a.norm.part + (rb * csize + q) * BM + r);
+    const float rn = __frsqrt_rn(tot / (float)(csize * BN) + a.norm.eps);
+#pragma unroll 1
+    for (int p = 0; p < PASSES; ++p) {
+        uint32_t xw[64];
+        tmem_ld_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
+        tmem_ld_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
+        tmem_ld_wait();
+        stg_acquire();
+        const uint4* gp = reinterpret_cast<const uint4*>(a.norm.gamma + n0 + p * 128);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const uint4 gv = __ldg(gp + u);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t xv = xw[4 * u + e];
+                o[e] = pack_bf16(bf16_lo(gw[e]) * rbf(bf16_lo(xv) * rn), bf16_hi(gw[e]) * rbf(bf16_hi(xv) * rn));
+            }
+            *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        stg_store(stg, tmY, n0 + p * 128, n0 + p * 128 + 64, m0);
+    }
+    tc_fence_before();
+    mbar_arrive(acc_empty);
+    return true;
+}
+
 // Fused QKV epilogue for one tile: per head of the tile, each thread (one token row) rounds its
 // projection to bf16, then V heads are copied and Q/K heads get RMSNorm over head_dim (fp32 reduce,
 // bf16 cast, then gamma) and RoPE (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the
@@ -364,7 +472,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
     constexpr int KSUB = C::KSUB;
     const int k_blocks = (args.K + BK * KSUB - 1) / (BK * KSUB);  // stages per tile
-    const int total = m_tiles * n_tiles;
+    // Work walk: tiles blockIdx.x, + gridDim.x, ... With the fused norm the tiles go row block by row
+    // block and the grid is a multiple of n_tiles, so the column tiles of a row block run at the same
+    // time on consecutive CTAs and a CTA keeps one column tile (rank).
+    constexpr bool RN = EPI == EPI_RESIDUAL_NORM;
+    const int rank = RN ? (int)blockIdx.x % n_tiles : 0;
+    const int first = (int)blockIdx.x, step = (int)gridDim.x, limit = m_tiles * n_tiles;
+    auto tile_at = [&](int t) -> Tile {
+        return RN ? Tile{t / n_tiles * BM, t % n_tiles * BN} : tile_of<BN>(t, m_tiles, n_tiles);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -382,7 +498,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if constexpr (EPI != EPI_QKV_ROPE) tma_prefetch_desc(&tmC);
-        if constexpr (EPI == EPI_RESIDUAL) tma_prefetch_desc(&tmR);
+        if constexpr (EPI == EPI_RESIDUAL || RN) tma_prefetch_desc(&tmR);
+        if constexpr (RN) tma_prefetch_desc(&tmV);
         if constexpr (EPI == EPI_QKV_ROPE) {
             if (args.qkv.T % BM == 0) {
                 tma_prefetch_desc(&tmC);
@@ -411,8 +528,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             (kb * KSUB + j) * BK, n0 + nb * kGemmBoxN);
     };
     int pre = 0;
-    if (warp == 0 && lane == 0 && args.b_independent && (int)blockIdx.x < total) {
-        const Tile tl = tile_of<BN>(blockIdx.x, m_tiles, n_tiles);
+    if (warp == 0 && lane == 0 && args.b_independent && first < limit) {
+        const Tile tl = tile_at(first);
         pre = min(STAGES, k_blocks);
         for (int kb = 0; kb < pre; ++kb) {
             mbar_expect_tx(&full_bar[kb], STAGE_BYTES);
@@ -425,8 +542,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
         int it = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
+        for (int t = first; t < limit && ok; t += step) {
+            const Tile tl = tile_at(t);
             for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -444,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
         int it = 0, local = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+        for (int t = first; t < limit && ok; t += step, ++local) {
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             if (!mbar_wait(&acc_empty[acc], aph ^ 1, abort_flag)) { ok = false; break; }
@@ -475,10 +592,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = quarter * 32 + lane;  // tile row = TMEM lane
         EpiSync es{res_bar, 0, epi_fail};
         int local = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+        for (int t = first; t < limit; t += step, ++local) {
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
-            const Tile tl = tile_of<BN>(t, m_tiles, n_tiles);
+            const Tile tl = tile_at(t);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
             if constexpr (EPI == EPI_QKV_ROPE) {
                 const bool w = args.qkv.dh == 128
@@ -487,6 +604,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                                    : epilogue_qkv_rope<64, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0,
                                                                &acc_empty[acc], &acc_full[acc], aph, abort_flag);
                 if (!w) {
+                    ok = false;
+                    break;
+                }
+            } else if constexpr (RN) {
+                if (!epilogue_residual_norm<BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0, rank, n_tiles,
+                                                &acc_empty[acc], &acc_full[acc], aph, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -702,6 +825,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// EPI_RESIDUAL_NORM: one cooperative launch (all CTAs resident at once, which the row blocks' meeting
+// points rely on) of a multiple of N / BN CTAs, at most one per SM.
+template <int BN>
+cudaError_t launch_norm(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
+    const int csize = a.N / BN, tiles = ((a.M + BM - 1) / BM) * csize;
+    if (a.N % BN || csize < 1 || csize > 8 || !a.norm.gamma || !a.norm.part || !a.norm.count)
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(tiles, device_sm_count() / csize * csize));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<EPI_RESIDUAL_NORM, BN>, m.a, m.b, m.c, m.r, m.v, a);
+}
+
 template <int EPI, int BN>
 cudaError_t launch_epi(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
@@ -729,9 +874,11 @@ cudaError_t gemm_prepare() {
     cudaError_t e = cudaSuccess;
     const void* f256[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16, 256>, (const void*)gemm_tcgen05_kernel<EPI_SWIGLU, 256>,
                           (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL, 256>, (const void*)gemm_tcgen05_kernel<EPI_F32, 256>,
-                          (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 256>};
+                          (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 256>,
+                          (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL_NORM, 256>};
     const void* f128[] = {(const void*)gemm_tcgen05_kernel<EPI_BF16, 128>, (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL, 128>,
-                          (const void*)gemm_tcgen05_kernel<EPI_F32, 128>, (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 128>};
+                          (const void*)gemm_tcgen05_kernel<EPI_F32, 128>, (const void*)gemm_tcgen05_kernel<EPI_QKV_ROPE, 128>,
+                          (const void*)gemm_tcgen05_kernel<EPI_RESIDUAL_NORM, 128>};
     for (const void* f : f256) {
         cudaError_t r = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<256>::SMEM_BYTES);
         if (r != cudaSuccess) e = r;
@@ -814,9 +961,26 @@ cudaError_t gemm_launch(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
         case EPI_RESIDUAL: return narrow ? launch_epi<EPI_RESIDUAL, 128>(m, a, st) : launch_epi<EPI_RESIDUAL, 256>(m, a, st);
         case EPI_F32: return narrow ? launch_epi<EPI_F32, 128>(m, a, st) : launch_epi<EPI_F32, 256>(m, a, st);
         case EPI_QKV_ROPE: return narrow ? launch_epi<EPI_QKV_ROPE, 128>(m, a, st) : launch_epi<EPI_QKV_ROPE, 256>(m, a, st);
+        case EPI_RESIDUAL_NORM: return narrow ? launch_norm<128>(m, a, st) : launch_norm<256>(m, a, st);
     }
     return cudaErrorInvalidValue;
 }
+
+bool gemm_norm_fusable(int M, int N) {
+    const int bn = gemm_tile_n(M, N, EPI_RESIDUAL_NORM);
+    return M > 0 && N % bn == 0 && N / bn <= 8;
+}
+
+bool gemm_norm_preferred(int M, int N) {
+    // The row blocks' meeting adds a few microseconds to a tile's epilogue; with at least two tiles per
+    // SM it hides behind the next tile's main loop and the fusion saves the separate RMSNorm pass.
+    if (!gemm_norm_fusable(M, N)) return false;
+    const long long tiles = (long long)((M + BM - 1) / BM) * (N / gemm_tile_n(M, N, EPI_RESIDUAL_NORM));
+    return tiles >= 2LL * device_sm_count();
+}
+
+size_t gemm_norm_part_floats(int M) { return (size_t)((M + BM - 1) / BM) * 8 * BM; }
+size_t gemm_norm_count_ints(int M) { return (size_t)((M + BM - 1) / BM) * 2; }
 
 bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_t K) {
     return encode_tmap_bf16_2d(map, X, K, rows, K * 2, BK, kSkinnyRowsBox);

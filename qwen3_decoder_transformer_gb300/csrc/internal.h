@@ -32,7 +32,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Device error-flag bits (one int per context, read by qwen3_get_error).
 enum : int { ERR_TOKEN = 1, ERR_TIMEOUT = 2 };
 
-enum Epilogue : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_RESIDUAL = 2, EPI_F32 = 3, EPI_QKV_ROPE = 4 };
+enum Epilogue : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_RESIDUAL = 2, EPI_F32 = 3, EPI_QKV_ROPE = 4, EPI_RESIDUAL_NORM = 5 };
 
 // ---------------------------------------------------------------- host utilities (gemm.cu)
 int device_sm_count();
@@ -69,6 +69,17 @@ struct SeqMap {
 constexpr int kSeqMetaHead = 2;
 constexpr int kSeqChunk = 1000;  // ints per set_seq launch (carried as a kernel parameter)
 cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st);
+// EPI_RESIDUAL_NORM: the residual epilogue followed by the next RMSNorm of the updated rows,
+// Y = bf16(gamma * bf16(X * rsqrt(mean(X^2) + eps))) with X the new residual stream. The N / BN column
+// tiles of a row block (at most 8) run at the same time on different CTAs of one cooperative launch and
+// exchange per-row partial sums of squares through part ([row blocks][8][128] floats), meeting on
+// count ([row blocks][2]: arrivals, departures; zero before the first launch, left zero by each).
+struct NormArgs {
+    const __nv_bfloat16* gamma;
+    float eps;
+    float* part;
+    unsigned* count;
+};
 struct GemmArgs {
     int M, N, K;
     int epi;
@@ -79,7 +90,14 @@ struct GemmArgs {
     long long ldr;
     int* err;
     QkvRopeArgs qkv;
+    NormArgs norm;
 };
+// Whether EPI_RESIDUAL_NORM can run for an [M, N] output (N a multiple of the tile width, at most 8
+// tiles); the sizes of NormArgs::part (floats) and NormArgs::count (ints) for up to M rows.
+bool gemm_norm_fusable(int M, int N);
+bool gemm_norm_preferred(int M, int N);  // fusable and expected to beat GEMM + separate RMSNorm
+size_t gemm_norm_part_floats(int M);
+size_t gemm_norm_count_ints(int M);
 // Tile rows of A, TMA box rows of B (a 256-wide tile loads two boxes), K per stage.
 constexpr int kGemmBM = 128, kGemmBoxN = 128, kGemmBK = 64;
 // A: [rows >= M, K] activations; B: [N, K] weights. Both maps are built with encode_gemm_maps.
@@ -90,7 +108,8 @@ bool encode_gemm_maps(CUtensorMap* ta, CUtensorMap* tb, const void* A, uint64_t 
 bool encode_tmap_out(CUtensorMap* map, const void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t ld);
 // The tensor maps of one GEMM launch: A, B, the output C (staged epilogues) and the residual R. The
 // fused QKV epilogue uses c, r, v as the 3-D store maps of Q [B*Hq][T][dh] and the K / V caches
-// [B*Hkv][cap][dh] (boxes of 64 x 128 x 1, encode_tmap_bf16_3d).
+// [B*Hkv][cap][dh] (boxes of 64 x 128 x 1, encode_tmap_bf16_3d); EPI_RESIDUAL_NORM stores the
+// normalised rows through v (an encode_tmap_out map like c).
 struct GemmMaps {
     CUtensorMap a, b, c, r, v;
 };

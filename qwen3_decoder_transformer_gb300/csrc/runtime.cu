@@ -117,6 +117,9 @@ struct qwen3_ctx {
     // tensor maps: A operands (activation buffers) and B operands (weights) per layer
     CUtensorMap tA_xn, tA_attn, tA_h, tA_hn;
     CUtensorMap tC_x, tC_h;  // staged-epilogue outputs: residual stream (also the residual input), SwiGLU output
+    CUtensorMap tC_xn;       // normalised rows written by the fused residual + RMSNorm epilogue
+    float* norm_part = nullptr;     // its per-row partial sums of squares
+    unsigned* norm_count = nullptr;  // and the row blocks' meeting counters (zero between launches)
     std::vector<CUtensorMap> tB_qkv, tB_o, tB_gu, tB_down;
     std::vector<CUtensorMap> tK3, tV3;  // per-layer cache maps [max_batch*Hkv][cap][dh] for the fused QKV stores
     CUtensorMap tB_head;
@@ -182,6 +185,21 @@ int gemm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, co
     m.b = tb;
     if (tc) m.c = *tc;
     if (tr) m.r = *tr;
+    return timed(c, cls, 1, st, [&] { return gemm_launch(m, a, st); });
+}
+
+// Residual GEMM (x += A B^T) whose epilogue also writes xn = RMSNorm(x; gamma), see EPI_RESIDUAL_NORM.
+int gemm_norm(qwen3_ctx* c, int cls, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+              const bf16* gamma, cudaStream_t st) {
+    GemmArgs a{M, N, K, EPI_RESIDUAL_NORM, 1, c->x, N, c->x, N, c->d_err, {},
+               NormArgs{gamma, c->cfg.rms_eps, c->norm_part, c->norm_count}};
+    GemmMaps m;
+    std::memset(&m, 0, sizeof(m));
+    m.a = ta;
+    m.b = tb;
+    m.c = c->tC_x;
+    m.r = c->tC_x;
+    m.v = c->tC_xn;
     return timed(c, cls, 1, st, [&] { return gemm_launch(m, a, st); });
 }
 
@@ -254,12 +272,15 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
     // Q [B*Hq][T][dh] store map for the fused QKV epilogue (used when T is a multiple of 128)
     CUtensorMap tq3;
     if (!encode_tmap_bf16_3d(&tq3, c->q, dh, T, (uint64_t)B * g.n_q_heads)) return QWEN3_E_CUDA;
+    // o_proj and down_proj write the next RMSNorm's output too (all but the last layer's down_proj)
+    const bool fuse = gemm_norm_preferred(M, d);
     for (int l = 0; l < g.n_layers; ++l) {
         if (l == c->tap_layer && c->tap_in)
             if (cudaMemcpyAsync(c->tap_in, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
                 return QWEN3_E_CUDA;
-        TRY(timed(c, K_RMSNORM, 1, st,
-                  [&] { return rmsnorm_launch(c->x, c->in_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
+        if (!fuse || l == 0)
+            TRY(timed(c, K_RMSNORM, 1, st,
+                      [&] { return rmsnorm_launch(c->x, c->in_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
         {
             // fused: Q/K/V projection, q_norm/k_norm, RoPE, Q to attention layout, K/V into the cache
             GemmArgs a{M, c->qkv_n, d, EPI_QKV_ROPE, 1, nullptr, 0, nullptr, 0, c->d_err,
@@ -292,14 +313,22 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
                                            c->attn_ws, 0, st);
             }));
         }
-        TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
-                 c->x, d, st));
-        TRY(timed(c, K_RMSNORM, 1, st,
-                  [&] { return rmsnorm_launch(c->x, c->post_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
+        if (fuse) {
+            TRY(gemm_norm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], M, d, c->q_width, c->post_norm[l], st));
+        } else {
+            TRY(gemm(c, K_GEMM_O, c->tA_attn, c->tB_o[l], &c->tC_x, &c->tC_x, M, d, c->q_width, EPI_RESIDUAL, c->x, d,
+                     c->x, d, st));
+            TRY(timed(c, K_RMSNORM, 1, st,
+                      [&] { return rmsnorm_launch(c->x, c->post_norm[l], M, d, 1, 0, g.rms_eps, c->xn, st); }));
+        }
         TRY(gemm(c, K_GEMM_GATEUP, c->tA_xn, c->tB_gu[l], &c->tC_h, nullptr, M, 2 * F, d, EPI_SWIGLU, c->h, F,
                  nullptr, 0, st));
-        TRY(gemm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], &c->tC_x, &c->tC_x, M, d, F, EPI_RESIDUAL, c->x, d, c->x, d,
-                 st));
+        if (fuse && l + 1 < g.n_layers) {
+            TRY(gemm_norm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], M, d, F, c->in_norm[l + 1], st));
+        } else {
+            TRY(gemm(c, K_GEMM_DOWN, c->tA_h, c->tB_down[l], &c->tC_x, &c->tC_x, M, d, F, EPI_RESIDUAL, c->x, d, c->x,
+                     d, st));
+        }
         if (l == c->tap_layer && c->tap_out)
             if (cudaMemcpyAsync(c->tap_out, c->x, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
                 return QWEN3_E_CUDA;
@@ -387,7 +416,7 @@ void release(qwen3_ctx* c) {
     void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
                     c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->skinny_ws, c->d_len,
                     c->d_err, c->d_ids_buf, c->d_logits_buf, c->d_seq, c->gen_logits, c->gen_done, c->gen_next,
-                    c->gen_alive, c->fin_part, c->fin_tick};
+                    c->gen_alive, c->fin_part, c->fin_tick, c->norm_part, c->norm_count};
     for (void* p : bufs)
         if (p) cudaFree(p);
     if (c->h_alive) cudaFreeHost(c->h_alive);
@@ -525,7 +554,9 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
                   cudaSuccess &&
               dmalloc(&c->d_seq, (size_t)kSeqMetaHead + max_batch) == cudaSuccess &&
               dmalloc(&c->d_len, 1) == cudaSuccess && dmalloc(&c->d_err, 1) == cudaSuccess &&
-              dmalloc(&c->d_ids_buf, rows) == cudaSuccess;
+              dmalloc(&c->d_ids_buf, rows) == cudaSuccess &&
+              dmalloc(&c->norm_part, gemm_norm_part_floats((int)rows)) == cudaSuccess &&
+              dmalloc(&c->norm_count, gemm_norm_count_ints((int)rows)) == cudaSuccess;
     // decode split-K workspace: the largest [splits][64][N] fp32 set of slices over the four projections
     if (ok) {
         const long long need = std::max(
@@ -559,7 +590,8 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          cudaMemsetAsync(c->hn, 0, arows * d * 2, st) == cudaSuccess &&
          cudaMemsetAsync(c->d_len, 0, sizeof(int), st) == cudaSuccess &&
          cudaMemsetAsync(c->d_seq, 0, ((size_t)kSeqMetaHead + max_batch) * sizeof(int), st) == cudaSuccess &&
-         cudaMemsetAsync(c->d_err, 0, sizeof(int), st) == cudaSuccess;
+         cudaMemsetAsync(c->d_err, 0, sizeof(int), st) == cudaSuccess &&
+         cudaMemsetAsync(c->norm_count, 0, gemm_norm_count_ints((int)rows) * sizeof(unsigned), st) == cudaSuccess;
     for (int l = 0; ok && l < L; ++l) {
         bf16* dst = c->wqkv + (size_t)l * c->qkv_n * d;
         ok = cudaMemcpyAsync(dst, w->q_proj[l], (size_t)c->q_width * d * 2, cudaMemcpyDeviceToDevice, st) ==
@@ -579,6 +611,7 @@ int qwen3_init(const qwen3_config* g, const qwen3_weights* w, int max_batch, int
          encode_tmap_bf16_2d(&c->tA_hn, c->hn, d, arows, (uint64_t)d * 2, kGemmBK, kGemmBM) &&
          encode_tmap_bf16_2d(&c->tB_head, c->head, d, V, (uint64_t)d * 2, kGemmBK, kGemmBoxN) &&
          encode_tmap_out(&c->tC_x, c->x, false, d, rows, d) && encode_tmap_out(&c->tC_h, c->h, false, F, arows, F) &&
+         encode_tmap_out(&c->tC_xn, c->xn, false, d, arows, d) &&
          encode_skinny_x_map(&c->tX_xn, c->xn, arows, d) && encode_skinny_x_map(&c->tX_attn, c->attn, arows, c->q_width) &&
          encode_skinny_x_map(&c->tX_h, c->h, arows, F) && encode_skinny_x_map(&c->tX_hn, c->hn, arows, d);
     c->tK3.resize(L);
@@ -823,11 +856,12 @@ int qwen3_kernel_times(qwen3_ctx* c, double* total_ms, int64_t* launches, int* n
 const char* qwen3_kernel_class_name(int i) { return (i >= 0 && i < K_NUM_CLASSES) ? kClassNames[i] : nullptr; }
 
 int qwen3_launch_count(const qwen3_ctx* c, int B, int T, int flags, int decode) {
-    (void)T;
     (void)flags;
     if (!c) return -1;
     if (decode && use_skinny_decode(c, B)) return 2 + c->cfg.n_layers * (8 + attn_decode_kernel_count()) + 2;
     const int per_layer = 6 + (decode ? attn_decode_kernel_count() : 1);
+    if (gemm_norm_preferred(B * T, c->cfg.hidden))  // one RMSNorm launch per forward instead of two per layer
+        return 1 + c->cfg.n_layers * (per_layer - 2) + 1 + 3;
     return 1 + c->cfg.n_layers * per_layer + 3;
 }
 
@@ -876,6 +910,31 @@ int qwen3_op_gemm(const void* A, const void* B, int M, int N, int K, int epi, vo
     if (epi == EPI_RESIDUAL && !encode_tmap_out(&m.r, R, false, (uint64_t)N, (uint64_t)M, (uint64_t)ldr))
         return QWEN3_E_CUDA;
     GemmArgs a{M, N, K, epi, 0, C, ldc, static_cast<const bf16*>(R), ldr, err, {}};
+    return gemm_launch(m, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
+}
+
+int qwen3_gemm_norm_supported(int M, int N) { return (M > 0 && N >= 128 && gemm_norm_fusable(M, N)) ? 1 : 0; }
+
+size_t qwen3_gemm_norm_part_floats(int M) { return M > 0 ? gemm_norm_part_floats(M) + gemm_norm_count_ints(M) : 0; }
+
+int qwen3_op_gemm_residual_norm(const void* A, const void* B, int M, int N, int K, void* X, const void* gamma, float eps,
+                                void* Y, float* part, int* err, void* stream) {
+    if (!A || !B || !X || !gamma || !Y || !part || M < 0 || N < 1 || K < 8 || K % 8) return QWEN3_E_ARG;
+    if (!is_aligned(A, 16) || !is_aligned(B, 16) || !is_aligned(X, 16) || !is_aligned(Y, 16) || !is_aligned(gamma, 16))
+        return QWEN3_E_ARG;
+    if (M == 0) return QWEN3_OK;
+    if (!qwen3_gemm_norm_supported(M, N)) return QWEN3_E_ARG;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
+    GemmMaps m;
+    std::memset(&m, 0, sizeof(m));
+    if (!encode_gemm_maps(&m.a, &m.b, A, (uint64_t)M, B, (uint64_t)N, (uint64_t)K) ||
+        !encode_tmap_out(&m.c, X, false, (uint64_t)N, (uint64_t)M, (uint64_t)N) ||
+        !encode_tmap_out(&m.r, X, false, (uint64_t)N, (uint64_t)M, (uint64_t)N) ||
+        !encode_tmap_out(&m.v, Y, false, (uint64_t)N, (uint64_t)M, (uint64_t)N))
+        return QWEN3_E_CUDA;
+    GemmArgs a{M, N, K, EPI_RESIDUAL_NORM, 0, X, N, static_cast<const bf16*>(X), N, err, {},
+               NormArgs{static_cast<const bf16*>(gamma), eps, part,
+                        reinterpret_cast<unsigned*>(part + gemm_norm_part_floats(M))}};
     return gemm_launch(m, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QWEN3_OK : QWEN3_E_CUDA;
 }
 

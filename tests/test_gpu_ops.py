@@ -203,6 +203,47 @@ def test_gemm_residual_in_place(bd, M, N, K):
     assert rel_l2(widen(bits(xd)), widen(ref)) <= 1e-3
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 256, 512), (200, 1024, 2048), (2048, 1024, 1024), (129, 512, 3072),
+                                   (5000, 1024, 512)])
+def test_gemm_residual_norm(bd, M, N, K):
+    """Residual GEMM fused with the next RMSNorm: X against the oracle's residual add, Y against the
+    oracle's RMSNorm of the kernel's own X (each stage pinned on its own). 5000 x 1024 takes 256-wide
+    tiles (4 per row block), the others 128-wide ones (N / 128 per row block)."""
+    assert bd.gemm_norm_supported(M, N)
+    rng = np.random.default_rng(M + 5 * N)
+    a = rand_bf16(rng, (M, K))
+    w = rand_bf16(rng, (N, K), 0.02)
+    x = rand_bf16(rng, (M, N))
+    g = bits(torch.from_numpy(1 + 0.2 * (rng.random(N) - 0.5)).to(torch.bfloat16))
+    xd, y = dev(x), torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    part = torch.zeros(bd.gemm_norm_part_floats(M), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.op_gemm_residual_norm(dev(a), dev(w), xd, dev(g), 1e-6, y, part, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got_x = bits(xd)
+    assert rel_l2(widen(got_x), widen(O.residual_add(x, O.linear(a, w)))) <= 1e-3
+    got_y, ref_y = bits(y), O.rmsnorm(got_x, g, 1e-6)
+    assert rel_l2(widen(got_y), widen(ref_y)) <= 1e-3
+    assert (got_y == ref_y).mean() > 0.99
+    # the meeting counters are left zero for the next call
+    rows_blocks = (M + 127) // 128
+    assert not part.view(torch.int32)[rows_blocks * 8 * 128:].any()
+
+
+def test_gemm_residual_norm_unsupported_shape(bd):
+    """More than 8 column tiles per row block are not supported: refused, nothing launched."""
+    assert not bd.gemm_norm_supported(64, 4096)
+    a, w = torch.zeros(64, 256, dtype=torch.bfloat16, device="cuda"), torch.zeros(4096, 256, dtype=torch.bfloat16,
+                                                                                    device="cuda")
+    x, y = torch.zeros(64, 4096, dtype=torch.bfloat16, device="cuda"), torch.zeros(64, 4096, dtype=torch.bfloat16,
+                                                                                   device="cuda")
+    g, part = torch.ones(4096, dtype=torch.bfloat16, device="cuda"), torch.zeros(4096, dtype=torch.float32,
+                                                                                 device="cuda")
+    with pytest.raises(bd.Qwen3Error):
+        bd.op_gemm_residual_norm(a, w, x, g, 1e-6, y, part)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 256, 64), (16, 4096, 4096), (64, 1024, 2048), (5, 1000, 1024), (33, 3072, 512)])
 def test_gemm_skinny(bd, M, N, K):
     """Decode GEMM: split-K slices (summed on the test side) and the unsplit direct store."""
