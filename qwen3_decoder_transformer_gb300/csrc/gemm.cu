@@ -50,7 +50,8 @@ struct Cfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;  // epilogue staging: 2 boxes of [128 rows][128 B]
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-    static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+    static constexpr int GAMMA_OFF = BAR_OFF + 256;  // EPI_RESIDUAL_NORM: the CTA's BN gamma values
+    static constexpr int SMEM_BYTES = GAMMA_OFF + 512 + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 };
 
@@ -238,8 +239,9 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
 template <int BN>
 __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmR,
                                                        const CUtensorMap* tmY, uint8_t* stg, EpiSync& es, uint32_t tacc,
-                                                       int r, int m0, int n0, int rank, int csize, uint64_t* acc_empty,
-                                                       uint64_t* acc_full, uint32_t aph, volatile int* abort_flag) {
+                                                       int r, int m0, int n0, int rank, int csize, const uint8_t* gam,
+                                                       uint64_t* acc_empty, uint64_t* acc_full, uint32_t aph,
+                                                       volatile int* abort_flag) {
     constexpr int PASSES = BN / 128;
     float ss = 0.f;
 #pragma unroll 1
@@ -283,26 +285,21 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         stg_store(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
     }
     tmem_st_wait();
-    // this tile's partial sums of squares, then meet the row block's other column tiles
+    // this tile's partial sums of squares, then meet the row block's other column tiles (the
+    // releasing increment publishes every epilogue thread's sum, ordered before it by the barrier)
     const size_t rb = (size_t)(m0 / BM);
+    unsigned* arrive = a.norm.count + 2 * rb;
     a.norm.part[(rb * csize + rank) * BM + r] = ss;
     named_barrier(1, 128);
     bool met = true;
     if (threadIdx.x == EPI_LEADER) {
-        unsigned* arrive = a.norm.count + 2 * rb;
-        __threadfence();  // the partial sums are visible before the arrival
-        atomicAdd(arrive, 1u);
+        red_add_release_gpu(arrive, 1u);
         const uint64_t t0 = globaltimer();
         for (uint32_t i = 1; ld_acquire_gpu(arrive) < (unsigned)csize; ++i) {
             if ((i & 63u) == 0 && (*abort_flag || globaltimer() - t0 > kWaitTimeoutNs)) {
                 met = false;
                 break;
             }
-        }
-        // the last CTA to leave resets the counters for the next launch
-        if (met && atomicAdd(arrive + 1, 1u) == (unsigned)csize - 1) {
-            arrive[0] = 0;
-            arrive[1] = 0;
         }
     }
     if (!epi_agree(met, es.fail)) return false;
@@ -316,10 +313,10 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         tmem_ld_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
         tmem_ld_wait();
         stg_acquire();
-        const uint4* gp = reinterpret_cast<const uint4*>(a.norm.gamma + n0 + p * 128);
+        const uint4* gp = reinterpret_cast<const uint4*>(gam + p * 256);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-            const uint4 gv = __ldg(gp + u);
+            const uint4 gv = gp[u];
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
             uint32_t o[4];
 #pragma unroll
@@ -333,6 +330,12 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
     }
     tc_fence_before();
     mbar_arrive(acc_empty);
+    // the last CTA of the row block to get here resets its counters for the next launch (every CTA
+    // has passed the meeting once it has counted itself out)
+    if (threadIdx.x == EPI_LEADER && atomicAdd(arrive + 1, 1u) == (unsigned)csize - 1) {
+        arrive[0] = 0;
+        arrive[1] = 0;
+    }
     return true;
 }
 
@@ -591,6 +594,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // tile row = TMEM lane
         EpiSync es{res_bar, 0, epi_fail};
+        if constexpr (RN) {  // this CTA's column tile is fixed: stage its gamma values once
+            const int et = threadIdx.x - 64;
+            if (et < BN / 8)
+                reinterpret_cast<uint4*>(smem + C::GAMMA_OFF)[et] =
+                    __ldg(reinterpret_cast<const uint4*>(args.norm.gamma + rank * BN) + et);
+            named_barrier(1, 128);
+        }
         int local = 0;
         for (int t = first; t < limit; t += step, ++local) {
             const int acc = local & 1;
@@ -609,7 +619,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             } else if constexpr (RN) {
                 if (!epilogue_residual_norm<BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0, rank, n_tiles,
-                                                &acc_empty[acc], &acc_full[acc], aph, abort_flag)) {
+                                                smem + C::GAMMA_OFF, &acc_empty[acc], &acc_full[acc], aph,
+                                                abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -972,8 +983,9 @@ bool gemm_norm_fusable(int M, int N) {
 }
 
 bool gemm_norm_preferred(int M, int N) {
-    // The row blocks' meeting adds a few microseconds to a tile's epilogue; with at least two tiles per
-    // SM it hides behind the next tile's main loop and the fusion saves the separate RMSNorm pass.
+    // The row block's meeting adds about 3.7 us to a tile's epilogue (0.6B o_proj at 2048 rows: 14.8 us
+    // fused against 11.1 + 4.2 for GEMM and RMSNorm apart, yet the whole step is slower fused); with at
+    // least two tiles per SM it hides behind the next tile's main loop (32768 rows: 112 against 118 us).
     if (!gemm_norm_fusable(M, N)) return false;
     const long long tiles = (long long)((M + BM - 1) / BM) * (N / gemm_tile_n(M, N, EPI_RESIDUAL_NORM));
     return tiles >= 2LL * device_sm_count();
