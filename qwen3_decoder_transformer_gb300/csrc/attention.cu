@@ -801,7 +801,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
 // Keys per decode CTA: long chunks amortise each CTA's fixed work over long caches, shorter ones keep
 // more CTAs busy on short caches; a rolling buffer uses the shortest so that its ring (a multiple of
 // 256) never wraps inside a chunk.
-constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256, DEC_THREADS = 128, DEC_UNROLL = 4;
+constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256, DEC_THREADS = 128;
 
 __device__ __forceinline__ float2 bf16x2_f2(uint32_t v) { return make_float2(bf16_lo(v), bf16_hi(v)); }
 
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
                              const __nv_bfloat16* __restrict__ vc, int Hq, int Hkv, int cap,
                              const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
                              float* __restrict__ work) {
-    constexpr int UNR = CH == DEC_CHUNK_SHORT ? 8 : DEC_UNROLL;  // key rows in flight per lane and pass
+    constexpr int UNR = 8;  // key rows in flight per lane and pass
     constexpr int LPK = 8;                      // lanes per key row
     constexpr int EPL = DH / LPK;               // elements per lane: 16 (dh 128) or 8 (dh 64)
     constexpr int WPL = EPL / 2;                // bf16x2 words per lane
@@ -913,6 +913,14 @@ __global__ void __launch_bounds__(DEC_THREADS)
             }
         }
     }
+    // the first value rows do not depend on the scores: their loads overlap the exponentials below
+    uint4 vv0[UNR][VPL];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+        const int s = s0 + u * KPS + warp * KPW + sub;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) vv0[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
     // chunk max and exponentials, one warp per head
     const int cnt = s1 - s0;
@@ -941,14 +949,7 @@ __global__ void __launch_bounds__(DEC_THREADS)
     for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int e = 0; e < WPL; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    for (int base = s0; base < s1; base += KPS * UNR) {
-        uint4 vv[UNR][VPL];
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int s = base + u * KPS + warp * KPW + sub;
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) vv[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
-        }
+    auto accumulate = [&](const uint4 (&vv)[UNR][VPL], int base) {
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
             const int s = base + u * KPS + warp * KPW + sub;
@@ -965,6 +966,17 @@ __global__ void __launch_bounds__(DEC_THREADS)
                 }
             }
         }
+    };
+    accumulate(vv0, s0);
+    for (int base = s0 + KPS * UNR; base < s1; base += KPS * UNR) {
+        uint4 vv[UNR][VPL];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int s = base + u * KPS + warp * KPW + sub;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) vv[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
+        }
+        accumulate(vv, base);
     }
     // reduce over the KPW key slots of the warp, then over warps
 #pragma unroll

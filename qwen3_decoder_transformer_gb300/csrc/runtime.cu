@@ -339,6 +339,11 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         return all_rows ? rmsnorm_launch(c->x, c->final_norm, rows, d, 1, 0, g.rms_eps, c->hn, st)
                         : rmsnorm_launch(c->x, c->final_norm, rows, d, T, T - 1, g.rms_eps, c->hn, st);
     }));
+    if (rows <= kSkinnyRowsBox) {  // a few rows: stream the vocabulary matrix through the weight-streaming GEMM
+        TRY(skinny(c, K_GEMM_LMHEAD, c->tB_head, c->tX_hn, rows, g.vocab, d, logits, 1, st));
+        TRY(timed(c, K_LENGTH, 1, st, [&] { return add_len_launch(c->d_len, T, st); }));
+        return QWEN3_OK;
+    }
     CUtensorMap t_logits;
     if (!encode_tmap_out(&t_logits, logits, true, g.vocab, rows, g.vocab)) return QWEN3_E_CUDA;
     TRY(gemm(c, K_GEMM_LMHEAD, c->tA_hn, c->tB_head, &t_logits, nullptr, rows, g.vocab, d, EPI_F32, logits, g.vocab,
