@@ -127,3 +127,61 @@ def test_tiny_chunked_prefill_long_context(bd, tiny):
     k, v = m.kv_view(cfg["n_layers"] - 1)
     assert rel_l2(widen(bits(k[0, :, T0:T0 + T1])), widen(kc[-1, 0, :, T0:T0 + T1])) <= 1e-2
     m.close()
+
+
+def test_tiny_graph_replay_matches_eager(bd, tiny):
+    """Repeated forward calls replay a captured CUDA graph: the replay equals the eager pass bit for bit,
+    reads the current contents of the id buffer, follows the cache length, and stays correct after the
+    graph cache has dropped entries (more distinct calls than it keeps)."""
+    cfg, w, _ = tiny
+    V = cfg["vocab"]
+    T, cap = 32, 256
+    m = bd.Model(cfg, w, max_batch=1, capacity=cap, max_tokens=T)
+    ids = synth.make_ids(V, 1, T, 3).cuda()
+    logits = torch.empty(1, V, dtype=torch.float32, device="cuda")
+
+    def run(eager, fn):
+        m.set_timing(eager)  # timing runs the pass eagerly
+        m.set_length(0, 0)
+        fn()
+        torch.cuda.synchronize()
+        m.set_timing(False)
+        return logits.clone()
+
+    pre = lambda: m.prefill(ids, logits)
+    ref = run(True, pre)
+    assert torch.equal(run(False, pre), ref)  # capture + launch
+    assert torch.equal(run(False, pre), ref)  # replay
+    ids.copy_(synth.make_ids(V, 1, T, 4).cuda())  # same buffer, new contents
+    ref2 = run(True, pre)
+    assert not torch.equal(ref2, ref)
+    assert torch.equal(run(False, pre), ref2)
+
+    # decode steps after the prefill: graph replays against the eager steps
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def steps(eager, n):
+        out = []
+        m.set_timing(eager)
+        m.set_length(0, 0)
+        m.prefill(ids, logits)
+        for k in range(n):
+            tok.fill_(k + 1)
+            m.decode_step(tok, logits)
+            out.append(logits.clone())
+        torch.cuda.synchronize()
+        m.set_timing(False)
+        return out
+
+    assert all(torch.equal(a, b) for a, b in zip(steps(False, 4), steps(True, 4)))
+
+    # more distinct prefill calls than the graph cache keeps, then the first one again
+    outs = {}
+    for t in range(4, 4 + 20):
+        part = ids[:, :t].contiguous()
+        outs[t] = run(False, lambda: m.prefill(part, logits))
+    for t in (4, 23):
+        part = ids[:, :t].contiguous()
+        assert torch.equal(run(True, lambda: m.prefill(part, logits)), outs[t])
+    assert m.get_error() == 0
+    m.close()
