@@ -13,13 +13,14 @@
 //                 accumulator row of a tile holds whole head vectors of one token, so the RMS over
 //                 head_dim, the rotate-half pairs (i, i + dh/2) and the stores stay in one thread
 //
-// Design (sm_103a): a persistent kernel, one CTA per SM, 6 warps.
+// Design (sm_103a): a persistent kernel, one CTA per SM, 10 warps (6 for the fused residual + RMSNorm).
 //   warp 0      TMA producer: 128x64 A and 256x64 B boxes (128-byte swizzle) into a 4-stage ring.
 //   warp 1      TMEM owner and MMA issuer: one thread issues tcgen05.mma 128x256x16 (4 per stage)
 //               into one of two 256-column fp32 accumulators, and commits stage releases and
 //               accumulator-ready signals to mbarriers.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM lanes 32*(w%4)..),
-//               fused epilogue math, 16-byte global stores; then release the accumulator.
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM lanes 32*(w%4)..; the
+//               two warps of a lane quarter take half of the columns each), fused epilogue math,
+//               staged TMA stores; then release the accumulator.
 // Two accumulators let tile i's epilogue overlap tile i+1's main loop. Tiles are walked M-fastest
 // so concurrently running CTAs share weight (B) tiles through L2. Every mbarrier wait is bounded:
 // on a timeout the kernel sets ERR_TIMEOUT, tells the other roles to stop, frees TMEM and returns.
@@ -34,9 +35,19 @@ namespace {
 
 constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;  // skinny GEMM; the tile GEMM's count depends on its epilogue (EpiShape)
 constexpr int STG_BYTES = 32768;
 constexpr int EPI_LEADER = 64;  // thread 0 of warp 2 issues the epilogue's TMA loads and stores
+// Epilogue warps per CTA: eight (two per TMEM lane quarter, each taking half of the columns) so the
+// epilogue of a tile takes half as long; four for the fused residual + RMSNorm epilogue, whose
+// row-block meeting is written for one thread per row. Eight epilogue warps (10 in all) cap a thread
+// at 168 registers.
+template <int EPI>
+struct EpiShape {
+    static constexpr int WARPS = EPI == EPI_RESIDUAL_NORM ? 4 : 8;
+    static constexpr int NT = 32 * WARPS;  // epilogue threads
+    static constexpr int THREADS = 64 + NT;
+};
 // Per tile width BN (256, or 128 when 256-wide tiles cannot fill the SMs): stage size, ring depth,
 // TMEM columns (two accumulators) and the instruction descriptor.
 // A stage holds KSUB consecutive 64-wide K boxes of A and B: two for 128-wide tiles, so each
@@ -50,8 +61,9 @@ struct Cfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;  // epilogue staging: 2 boxes of [128 rows][128 B]
     static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-    static constexpr int GAMMA_OFF = BAR_OFF + 256;  // EPI_RESIDUAL_NORM: the CTA's BN gamma values
-    static constexpr int SMEM_BYTES = GAMMA_OFF + 512 + 1024;
+    // 1 KB of epilogue scratch: EPI_RESIDUAL_NORM's BN gamma values, EPI_QKV_ROPE's per-row partial sums
+    static constexpr int GAMMA_OFF = BAR_OFF + 256;
+    static constexpr int SMEM_BYTES = GAMMA_OFF + 1024 + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 };
 
@@ -86,23 +98,26 @@ struct EpiSync {
     volatile int* fail;  // set by any epilogue warp whose wait gave up
 };
 
-// Make a warp's wait outcome uniform over the four epilogue warps: every thread reaches the barrier
-// (the waits before it are bounded), so all four warps take the same branch afterwards.
+// Make a warp's wait outcome uniform over the NT epilogue threads: every thread reaches the barrier
+// (the waits before it are bounded), so all epilogue warps take the same branch afterwards.
+template <int NT>
 __device__ __forceinline__ bool epi_agree(bool ok, volatile int* fail) {
     if (!__all_sync(0xffffffffu, ok) && (threadIdx.x & 31) == 0) *fail = 1;
-    named_barrier(1, 128);
+    named_barrier(1, NT);
     return *fail == 0;
 }
 
 // Staging-buffer hand-off between passes: the previous TMA store must have read it.
+template <int NT>
 __device__ __forceinline__ void stg_acquire() {
     if (threadIdx.x == EPI_LEADER) bulk_wait_read();
-    named_barrier(1, 128);
+    named_barrier(1, NT);
 }
 // Publish the staging buffer (generic-proxy writes) to the TMA store and issue it.
+template <int NT>
 __device__ __forceinline__ void stg_store(uint8_t* stg, const CUtensorMap* tmC, int x0, int x1, int y) {
     fence_proxy_async_smem();
-    named_barrier(1, 128);
+    named_barrier(1, NT);
     if (threadIdx.x == EPI_LEADER) {
         tma_store_2d(tmC, stg, x0, y);
         tma_store_2d(tmC, stg + 16384, x1, y);
@@ -117,21 +132,23 @@ __device__ __forceinline__ void tmem_ld_128(uint32_t taddr, uint32_t (&r)[128]) 
     tmem_ld_wait();
 }
 
-// Epilogue of one tile for the staged epilogues (BF16, RESIDUAL, SWIGLU, F32). The accumulator is
-// released (acc_empty) as soon as its last columns are in registers; outputs go through the staging
-// buffer and TMA stores, so each warp writes whole swizzled rows to shared memory and the copy to
-// global memory is one coalesced bulk operation per box. Returns false if a wait gave up.
+// Epilogue of one tile for the staged epilogues (BF16, RESIDUAL, SWIGLU, F32), eight warps: warp half
+// `hf` (0 or 1) of each TMEM lane quarter takes the second 64-column box (bf16; 32 columns fp32) of
+// every 128-column pass. The accumulator is released (acc_empty) as soon as a thread's last columns
+// are in registers; outputs go through the staging buffer and TMA stores, so each warp writes whole
+// swizzled rows of its box to shared memory and the copy to global memory is one coalesced bulk
+// operation per box. Returns false if a wait gave up.
 template <int EPI, int BN>
 __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmR,
-                                                uint8_t* stg, EpiSync& es, uint32_t tacc, int r, int m0, int n0,
-                                                uint64_t* acc_empty, uint64_t* acc_full, uint32_t aph,
+                                                uint8_t* stg, EpiSync& es, uint32_t tacc, int r, int hf, int m0,
+                                                int n0, uint64_t* acc_empty, uint64_t* acc_full, uint32_t aph,
                                                 volatile int* abort_flag) {
-    bool ok = true;
+    constexpr int NT = EpiShape<EPI>::NT;
     // passes of 128 bf16 (or 64 fp32) output columns, each filling the 32 KB staging buffer
     constexpr int PASSES = EPI == EPI_SWIGLU ? 1 : (EPI == EPI_F32 ? BN / 64 : BN / 128);
 #pragma unroll 1
     for (int p = 0; p < PASSES; ++p) {
-        stg_acquire();
+        stg_acquire<NT>();
         if constexpr (EPI == EPI_RESIDUAL) {
             if (threadIdx.x == EPI_LEADER) {
                 mbar_expect_tx(es.res_bar, STG_BYTES);
@@ -142,25 +159,24 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
         if (p == 0) {
             // the accumulator of this tile
             const bool w = mbar_wait(acc_full, aph, abort_flag);
-            if (!epi_agree(w, es.fail)) return false;
+            if (!epi_agree<NT>(w, es.fail)) return false;
             tc_fence_after();
         }
         if constexpr (EPI == EPI_SWIGLU) {
-            // gate columns [0, BN/2), up columns [BN/2, BN): 64 outputs per half
+            // gate columns [0, BN/2), up columns [BN/2, BN): this half's 64 outputs are gate columns
+            // [64 hf, 64 hf + 64) times the matching up columns (BN = 256)
 #pragma unroll 1
-            for (int hf = 0; hf < BN / 128; ++hf) {
-                uint32_t g[64], u[64];
-                tmem_ld_32x32b_x32(tacc + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-                tmem_ld_32x32b_x32(tacc + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
-                tmem_ld_32x32b_x32(tacc + BN / 2 + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-                tmem_ld_32x32b_x32(tacc + BN / 2 + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+            for (int sub = 0; sub < 2; ++sub) {  // 32 outputs at a time (registers of a 10-warp CTA)
+                uint32_t g[32], u[32];
+                tmem_ld_32x32b_x32(tacc + hf * 64 + sub * 32, g);
+                tmem_ld_32x32b_x32(tacc + BN / 2 + hf * 64 + sub * 32, u);
                 tmem_ld_wait();
-                if (hf == BN / 128 - 1) {
+                if (sub == 1) {
                     tc_fence_before();
                     mbar_arrive(acc_empty);
                 }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < 4; ++q) {
                     uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -176,26 +192,28 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
                         const float2 pv = mul2(make_float2(bf16_lo(sb), bf16_hi(sb)), make_float2(bf16_lo(ub), bf16_hi(ub)));
                         wv[e] = pack_bf16(pv.x, pv.y);
                     }
-                    *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + sub * 4 + q)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
-            stg_store(stg, tmC, n0 / 2, n0 / 2 + 64, m0);
+            stg_store<NT>(stg, tmC, n0 / 2, n0 / 2 + 64, m0);
         } else if constexpr (EPI == EPI_F32) {
-            uint32_t v[64];
-            tmem_ld_32x32b_x32(tacc + p * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld_32x32b_x32(tacc + p * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tacc + p * 64 + hf * 32, v);
             tmem_ld_wait();
             if (p == PASSES - 1) {
                 tc_fence_before();
                 mbar_arrive(acc_empty);
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            stg_store(stg, tmC, n0 + p * 64, n0 + p * 64 + 32, m0);
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + u)) =
+                    make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            stg_store<NT>(stg, tmC, n0 + p * 64, n0 + p * 64 + 32, m0);
         } else {
-            uint32_t v[128];
-            tmem_ld_128(tacc + p * 128, v);
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(tacc + p * 128 + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(tacc + p * 128 + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
             if (p == PASSES - 1) {
                 tc_fence_before();
                 mbar_arrive(acc_empty);
@@ -203,11 +221,11 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
             if constexpr (EPI == EPI_RESIDUAL) {
                 const bool w = mbar_wait(es.res_bar, es.res_phase & 1, abort_flag);
                 ++es.res_phase;
-                if (!epi_agree(w, es.fail)) return false;
+                if (!epi_agree<NT>(w, es.fail)) return false;
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, u));
+            for (int u = 0; u < 8; ++u) {
+                uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + u));
                 uint32_t wv[4];
                 if constexpr (EPI == EPI_RESIDUAL) {
                     const uint4 q = *cp;
@@ -223,10 +241,10 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
                 }
                 *cp = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
-            stg_store(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
+            stg_store<NT>(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
         }
     }
-    return ok;
+    return true;
 }
 
 // Residual epilogue followed by the next RMSNorm ("A modern architecture: Qwen3", section RMSNorm and
@@ -246,7 +264,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
     float ss = 0.f;
 #pragma unroll 1
     for (int p = 0; p < PASSES; ++p) {
-        stg_acquire();
+        stg_acquire<128>();
         if (threadIdx.x == EPI_LEADER) {
             mbar_expect_tx(es.res_bar, STG_BYTES);
             tma_load_2d(stg, tmR, es.res_bar, n0 + p * 128, m0);
@@ -254,7 +272,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         }
         if (p == 0) {
             const bool w = mbar_wait(acc_full, aph, abort_flag);
-            if (!epi_agree(w, es.fail)) return false;
+            if (!epi_agree<128>(w, es.fail)) return false;
             tc_fence_after();
         }
         uint32_t v[128];
@@ -262,7 +280,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         {
             const bool w = mbar_wait(es.res_bar, es.res_phase & 1, abort_flag);
             ++es.res_phase;
-            if (!epi_agree(w, es.fail)) return false;
+            if (!epi_agree<128>(w, es.fail)) return false;
         }
         uint32_t xw[64];
 #pragma unroll
@@ -282,7 +300,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         }
         tmem_st_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
         tmem_st_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
-        stg_store(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
+        stg_store<128>(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
     }
     tmem_st_wait();
     // this tile's partial sums of squares, then meet the row block's other column tiles (the
@@ -302,7 +320,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
             }
         }
     }
-    if (!epi_agree(met, es.fail)) return false;
+    if (!epi_agree<128>(met, es.fail)) return false;
     float tot = 0.f;
     for (int q = 0; q < csize; ++q) tot += __ldcg(a.norm.part + (rb * csize + q) * BM + r);
     const float rn = __frsqrt_rn(tot / (float)(csize * BN) + a.norm.eps);
@@ -312,7 +330,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         tmem_ld_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
         tmem_ld_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
         tmem_ld_wait();
-        stg_acquire();
+        stg_acquire<128>();
         const uint4* gp = reinterpret_cast<const uint4*>(gam + p * 256);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -326,7 +344,7 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
             }
             *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        stg_store(stg, tmY, n0 + p * 128, n0 + p * 128 + 64, m0);
+        stg_store<128>(stg, tmY, n0 + p * 128, n0 + p * 128 + 64, m0);
     }
     tc_fence_before();
     mbar_arrive(acc_empty);
@@ -342,14 +360,20 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
 // Fused QKV epilogue for one tile: per head of the tile, each thread (one token row) rounds its
 // projection to bf16, then V heads are copied and Q/K heads get RMSNorm over head_dim (fp32 reduce,
 // bf16 cast, then gamma) and RoPE (bf16(bf16(a c) + bf16(-b s)), bf16(bf16(b c) + bf16(a s)) for the
-// pair (i, i + dh/2)). When the tile's 128 rows are consecutive tokens of one sequence (prefill with
-// T % 128 == 0), each head's [128 x dh] block is written through the staging buffer with one 3-D TMA
-// store into Q [B*Hq][T][dh] or the cache [B*Hkv][cap][dh]; otherwise (decode) rows are stored directly.
+// pair (i, i + dh/2)). The two warp halves of a TMEM lane quarter split each head's rotation pairs:
+// half hf takes i in [hf dh/4, (hf + 1) dh/4) and the partners i + dh/2, and the halves add their
+// partial sums of squares through shared memory (64-thread barriers per lane quarter). When the
+// tile's 128 rows are consecutive tokens of one sequence (prefill with T % 128 == 0), each head's
+// [128 x dh] block is written through the staging buffer with one 3-D TMA store into Q [B*Hq][T][dh] or
+// the cache [B*Hkv][cap][dh]; otherwise (decode) rows are stored directly.
 template <int DH, int BN>
 __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                                   const CUtensorMap* tmV, uint8_t* stg, EpiSync& es, uint32_t tacc,
-                                                  int r, int m0, int n0, uint64_t* acc_empty, uint64_t* acc_full,
-                                                  uint32_t aph, volatile int* abort_flag) {
+                                                  int r, int hf, int m0, int n0, uint64_t* acc_empty,
+                                                  uint64_t* acc_full, uint32_t aph, volatile int* xss_raw,
+                                                  volatile int* abort_flag) {
+    constexpr int NT = EpiShape<EPI_QKV_ROPE>::NT;
+    volatile float(*xss)[128] = reinterpret_cast<volatile float(*)[128]>(xss_raw);  // [half][row] partial sums
     const QkvRopeArgs& q = a.qkv;
     const int row = m0 + r;
     const bool row_ok = row < a.M;
@@ -357,12 +381,12 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
     // whole 128-row blocks go out by TMA, unless a rolling buffer could wrap inside the block
     const bool staged = (q.T % BM) == 0 && (!q.rolling || len0 % BM == 0);
     const int b = row_ok ? row / q.T : 0, t = row_ok ? row % q.T : 0;
-    constexpr int HALF = DH / 2;
+    constexpr int HALF = DH / 2, QC = DH / 4;  // QC: columns per side of this half
     constexpr int NHEAD = BN / DH;
     {
         const bool w = mbar_wait(acc_full, aph, abort_flag);
         if (staged) {
-            if (!epi_agree(w, es.fail)) return false;
+            if (!epi_agree<NT>(w, es.fail)) return false;
         } else if (!__all_sync(0xffffffffu, w)) {
             return false;
         }
@@ -371,37 +395,53 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
     const int slot = len0 + t;
     const int pos = q.meta ? slot_position(slot, q.meta[0], q.meta[kSeqMetaHead + b]) : slot;
     const int phys = q.rolling ? slot % q.cap : slot;
+    const int pair_bar = 2 + (r >> 5);  // the two warps of this lane quarter
 #pragma unroll 1
     for (int lh = 0; lh < NHEAD; ++lh) {
         const int hg = n0 / DH + lh;
-        uint32_t x[DH];
-#pragma unroll
-        for (int c = 0; c < DH / 32; ++c)
-            tmem_ld_32x32b_x32(tacc + lh * DH + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+        uint32_t x1[QC], x2[QC];  // columns [hf QC, hf QC + QC) and [HALF + hf QC, ...) of the head
+        const uint32_t c1 = tacc + lh * DH + hf * QC, c2 = c1 + HALF;
+        if constexpr (QC == 32) {
+            tmem_ld_32x32b_x32(c1, *reinterpret_cast<uint32_t(*)[32]>(&x1[0]));
+            tmem_ld_32x32b_x32(c2, *reinterpret_cast<uint32_t(*)[32]>(&x2[0]));
+        } else {
+            tmem_ld_32x32b_x16(c1, x1);
+            tmem_ld_32x32b_x16(c2, x2);
+        }
         tmem_ld_wait();
         if (lh == NHEAD - 1) {
             tc_fence_before();
             mbar_arrive(acc_empty);
         }
         const int kind = hg < q.Hq ? 0 : (hg < q.Hq + q.Hkv ? 1 : 2);  // q, k, v
-        uint32_t o[DH / 2];  // packed bf16 outputs of this row
+        uint32_t o1[QC / 2], o2[QC / 2];  // packed bf16 outputs of the two sides
         if (kind == 2) {
 #pragma unroll
-            for (int j = 0; j < DH / 2; ++j) o[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+            for (int j = 0; j < QC / 2; ++j) {
+                o1[j] = pack_bf16(__uint_as_float(x1[2 * j]), __uint_as_float(x1[2 * j + 1]));
+                o2[j] = pack_bf16(__uint_as_float(x2[2 * j]), __uint_as_float(x2[2 * j + 1]));
+            }
         } else {
             float ss = 0.f;
 #pragma unroll
-            for (int j = 0; j < DH; ++j) {
-                const float xv = rbf(__uint_as_float(x[j]));
-                x[j] = __float_as_uint(xv);
-                ss = fmaf(xv, xv, ss);
+            for (int j = 0; j < QC; ++j) {
+                const float xa = rbf(__uint_as_float(x1[j])), xb = rbf(__uint_as_float(x2[j]));
+                x1[j] = __float_as_uint(xa);
+                x2[j] = __float_as_uint(xb);
+                ss = fmaf(xa, xa, ss);
+                ss = fmaf(xb, xb, ss);
             }
-            const float rn = __frsqrt_rn(ss / (float)DH + q.eps);
+            xss[hf][r] = ss;
+            named_barrier(pair_bar, 64);
+            const float tot = xss[0][r] + xss[1][r];  // same order in both halves
+            named_barrier(pair_bar, 64);             // both have read before the next head's write
+            const float rn = __frsqrt_rn(tot / (float)DH + q.eps);
             const __nv_bfloat16* gam = kind == 0 ? q.q_gamma : q.k_gamma;
             const __nv_bfloat16* cs = q.table + (size_t)(row_ok ? pos : 0) * DH;
             // bf16x2 arithmetic: each packed multiply / add rounds once to bf16, as the definition does
 #pragma unroll
-            for (int v = 0; v < HALF / 8; ++v) {
+            for (int vv = 0; vv < QC / 8; ++vv) {
+                const int v = hf * (QC / 8) + vv;  // 8-element group of the first half of the head
                 const uint4 g0 = __ldg(reinterpret_cast<const uint4*>(gam) + v);
                 const uint4 g1 = __ldg(reinterpret_cast<const uint4*>(gam + HALF) + v);
                 const uint4 cc = __ldg(reinterpret_cast<const uint4*>(cs) + v);
@@ -410,25 +450,32 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
                 const uint32_t C[4] = {cc.x, cc.y, cc.z, cc.w}, S[4] = {sn.x, sn.y, sn.z, sn.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = 8 * v + 2 * e;
+                    const int j = 8 * vv + 2 * e;
                     // normalised, cast, then times gamma: a = first-half pair, bb = second-half pair
-                    const uint32_t na = pack_bf16(__uint_as_float(x[j]) * rn, __uint_as_float(x[j + 1]) * rn);
-                    const uint32_t nb = pack_bf16(__uint_as_float(x[j + HALF]) * rn, __uint_as_float(x[j + HALF + 1]) * rn);
+                    const uint32_t na = pack_bf16(__uint_as_float(x1[j]) * rn, __uint_as_float(x1[j + 1]) * rn);
+                    const uint32_t nb = pack_bf16(__uint_as_float(x2[j]) * rn, __uint_as_float(x2[j + 1]) * rn);
                     const __nv_bfloat162 av = __hmul2_rn(as_bf2(G0[e]), as_bf2(na));
                     const __nv_bfloat162 bv = __hmul2_rn(as_bf2(G1[e]), as_bf2(nb));
                     const __nv_bfloat162 co = as_bf2(C[e]), si = as_bf2(S[e]);
-                    o[4 * v + e] = as_u32(__hsub2(__hmul2_rn(av, co), __hmul2_rn(bv, si)));
-                    o[HALF / 2 + 4 * v + e] = as_u32(__hadd2(__hmul2_rn(bv, co), __hmul2_rn(av, si)));
+                    o1[4 * vv + e] = as_u32(__hsub2(__hmul2_rn(av, co), __hmul2_rn(bv, si)));
+                    o2[4 * vv + e] = as_u32(__hadd2(__hmul2_rn(bv, co), __hmul2_rn(av, si)));
                 }
             }
         }
+        // 16-byte chunks of the head row: this half's first-side chunks are hf QC/8 .. and its
+        // second-side chunks HALF/8 + hf QC/8 ..
+        const int u1 = hf * (QC / 8), u2 = HALF / 8 + hf * (QC / 8);
         if (staged) {
-            stg_acquire();
+            stg_acquire<NT>();
 #pragma unroll
-            for (int u = 0; u < DH / 8; ++u)
-                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            for (int vv = 0; vv < QC / 8; ++vv) {
+                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u1 + vv)) =
+                    make_uint4(o1[4 * vv], o1[4 * vv + 1], o1[4 * vv + 2], o1[4 * vv + 3]);
+                *reinterpret_cast<uint4*>(stg_chunk(stg, r, u2 + vv)) =
+                    make_uint4(o2[4 * vv], o2[4 * vv + 1], o2[4 * vv + 2], o2[4 * vv + 3]);
+            }
             fence_proxy_async_smem();
-            named_barrier(1, 128);
+            named_barrier(1, NT);
             if (threadIdx.x == EPI_LEADER) {
                 const int bt = m0 / q.T, t0 = m0 % q.T;
                 const CUtensorMap* map = kind == 0 ? tmQ : (kind == 1 ? tmK : tmV);
@@ -443,15 +490,17 @@ __device__ __forceinline__ bool epilogue_qkv_rope(const GemmArgs& a, const CUten
                                : kind == 1 ? q.k_cache + (((size_t)b * q.Hkv + (hg - q.Hq)) * q.cap + phys) * DH
                                            : q.v_cache + (((size_t)b * q.Hkv + (hg - q.Hq - q.Hkv)) * q.cap + phys) * DH;
 #pragma unroll
-            for (int u = 0; u < DH / 8; ++u)
-                reinterpret_cast<uint4*>(dst)[u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            for (int vv = 0; vv < QC / 8; ++vv) {
+                reinterpret_cast<uint4*>(dst)[u1 + vv] = make_uint4(o1[4 * vv], o1[4 * vv + 1], o1[4 * vv + 2], o1[4 * vv + 3]);
+                reinterpret_cast<uint4*>(dst)[u2 + vv] = make_uint4(o2[4 * vv], o2[4 * vv + 1], o2[4 * vv + 2], o2[4 * vv + 3]);
+            }
         }
     }
     return true;
 }
 
 template <int EPI, int BN>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(EpiShape<EPI>::THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                         const __grid_constant__ CUtensorMap tmV, const GemmArgs args) {
@@ -492,7 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], EpiShape<EPI>::NT);
         }
         mbar_init(res_bar, 1);
         *abort_flag = 0;
@@ -591,8 +640,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 2) {
         // ---------------- epilogue
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // tile row = TMEM lane
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;  // hf: which half of the columns (8 warps)
+        const int r = quarter * 32 + lane;                     // tile row = TMEM lane
         EpiSync es{res_bar, 0, epi_fail};
         if constexpr (RN) {  // this CTA's column tile is fixed: stage its gamma values once
             const int et = threadIdx.x - 64;
@@ -608,11 +657,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile tl = tile_at(t);
             const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
             if constexpr (EPI == EPI_QKV_ROPE) {
+                volatile int* xss = reinterpret_cast<volatile int*>(smem + C::GAMMA_OFF);
                 const bool w = args.qkv.dh == 128
-                                   ? epilogue_qkv_rope<128, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0,
-                                                                &acc_empty[acc], &acc_full[acc], aph, abort_flag)
-                                   : epilogue_qkv_rope<64, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0,
-                                                               &acc_empty[acc], &acc_full[acc], aph, abort_flag);
+                                   ? epilogue_qkv_rope<128, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, hf, tl.m0,
+                                                                tl.n0, &acc_empty[acc], &acc_full[acc], aph, xss,
+                                                                abort_flag)
+                                   : epilogue_qkv_rope<64, BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, hf, tl.m0,
+                                                               tl.n0, &acc_empty[acc], &acc_full[acc], aph, xss,
+                                                               abort_flag);
                 if (!w) {
                     ok = false;
                     break;
@@ -625,7 +677,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
             } else {
-                if (!epilogue_staged<EPI, BN>(args, &tmC, &tmR, stg, es, tacc, r, tl.m0, tl.n0, &acc_empty[acc],
+                if (!epilogue_staged<EPI, BN>(args, &tmC, &tmR, stg, es, tacc, r, hf, tl.m0, tl.n0, &acc_empty[acc],
                                               &acc_full[acc], aph, abort_flag)) {
                     ok = false;
                     break;
@@ -845,7 +897,7 @@ cudaError_t launch_norm(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(tiles, device_sm_count() / csize * csize));
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(EpiShape<EPI_RESIDUAL_NORM>::THREADS);
     cfg.dynamicSmemBytes = Cfg<BN>::SMEM_BYTES;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -862,7 +914,8 @@ template <int EPI, int BN>
 cudaError_t launch_epi(const GemmMaps& m, const GemmArgs& a, cudaStream_t st) {
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int grid = std::min(tiles, device_sm_count());
-    return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(THREADS), Cfg<BN>::SMEM_BYTES, st, m.a, m.b, m.c,
+    return launch_pdl(gemm_tcgen05_kernel<EPI, BN>, dim3(grid), dim3(EpiShape<EPI>::THREADS), Cfg<BN>::SMEM_BYTES, st,
+                      m.a, m.b, m.c,
                       m.r, m.v, a);
 }
 
