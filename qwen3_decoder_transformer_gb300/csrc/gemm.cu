@@ -13,7 +13,7 @@
 //                 accumulator row of a tile holds whole head vectors of one token, so the RMS over
 //                 head_dim, the rotate-half pairs (i, i + dh/2) and the stores stay in one thread
 //
-// Design (sm_103a): a persistent kernel, one CTA per SM, 10 warps (6 for the fused residual + RMSNorm).
+// Design (sm_103a): a persistent kernel, one CTA per SM, 10 warps.
 //   warp 0      TMA producer: 128x64 A and 256x64 B boxes (128-byte swizzle) into a 4-stage ring.
 //   warp 1      TMEM owner and MMA issuer: one thread issues tcgen05.mma 128x256x16 (4 per stage)
 //               into one of two 256-column fp32 accumulators, and commits stage releases and
@@ -39,12 +39,10 @@ constexpr int THREADS = 192;  // skinny GEMM; the tile GEMM's count depends on i
 constexpr int STG_BYTES = 32768;
 constexpr int EPI_LEADER = 64;  // thread 0 of warp 2 issues the epilogue's TMA loads and stores
 // Epilogue warps per CTA: eight (two per TMEM lane quarter, each taking half of the columns) so the
-// epilogue of a tile takes half as long; four for the fused residual + RMSNorm epilogue, whose
-// row-block meeting is written for one thread per row. Eight epilogue warps (10 in all) cap a thread
-// at 168 registers.
+// epilogue of a tile takes half as long. Ten warps in all cap a thread at 168 registers.
 template <int EPI>
 struct EpiShape {
-    static constexpr int WARPS = EPI == EPI_RESIDUAL_NORM ? 4 : 8;
+    static constexpr int WARPS = 8;
     static constexpr int NT = 32 * WARPS;  // epilogue threads
     static constexpr int THREADS = 64 + NT;
 };
@@ -257,14 +255,15 @@ __device__ __forceinline__ bool epilogue_staged(const GemmArgs& a, const CUtenso
 template <int BN>
 __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmR,
                                                        const CUtensorMap* tmY, uint8_t* stg, EpiSync& es, uint32_t tacc,
-                                                       int r, int m0, int n0, int rank, int csize, const uint8_t* gam,
-                                                       uint64_t* acc_empty, uint64_t* acc_full, uint32_t aph,
-                                                       volatile int* abort_flag) {
+                                                       int r, int hf, int m0, int n0, int rank, int csize,
+                                                       const uint8_t* gam, uint64_t* acc_empty, uint64_t* acc_full,
+                                                       uint32_t aph, volatile int* abort_flag) {
+    constexpr int NT = EpiShape<EPI_RESIDUAL_NORM>::NT;
     constexpr int PASSES = BN / 128;
     float ss = 0.f;
 #pragma unroll 1
     for (int p = 0; p < PASSES; ++p) {
-        stg_acquire<128>();
+        stg_acquire<NT>();
         if (threadIdx.x == EPI_LEADER) {
             mbar_expect_tx(es.res_bar, STG_BYTES);
             tma_load_2d(stg, tmR, es.res_bar, n0 + p * 128, m0);
@@ -272,20 +271,24 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         }
         if (p == 0) {
             const bool w = mbar_wait(acc_full, aph, abort_flag);
-            if (!epi_agree<128>(w, es.fail)) return false;
+            if (!epi_agree<NT>(w, es.fail)) return false;
             tc_fence_after();
         }
-        uint32_t v[128];
-        tmem_ld_128(tacc + p * 128, v);
+        // this half's 64 columns of the pass (staging box hf)
+        const uint32_t ta = tacc + p * 128 + hf * 64;
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
         {
             const bool w = mbar_wait(es.res_bar, es.res_phase & 1, abort_flag);
             ++es.res_phase;
-            if (!epi_agree<128>(w, es.fail)) return false;
+            if (!epi_agree<NT>(w, es.fail)) return false;
         }
-        uint32_t xw[64];
+        uint32_t xw[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, u));
+        for (int u = 0; u < 8; ++u) {
+            uint4* cp = reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + u));
             const uint4 q = *cp;
             const uint32_t rr[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -298,17 +301,17 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
             }
             *cp = make_uint4(xw[4 * u], xw[4 * u + 1], xw[4 * u + 2], xw[4 * u + 3]);
         }
-        tmem_st_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
-        tmem_st_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
-        stg_store<128>(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
+        // X packed over the first 32 of the columns this thread has just read
+        tmem_st_32x32b_x32(ta, xw);
+        stg_store<NT>(stg, tmC, n0 + p * 128, n0 + p * 128 + 64, m0);
     }
     tmem_st_wait();
-    // this tile's partial sums of squares, then meet the row block's other column tiles (the
+    // this half-tile's partial sums of squares, then meet the row block's other column tiles (the
     // releasing increment publishes every epilogue thread's sum, ordered before it by the barrier)
     const size_t rb = (size_t)(m0 / BM);
     unsigned* arrive = a.norm.count + 2 * rb;
-    a.norm.part[(rb * csize + rank) * BM + r] = ss;
-    named_barrier(1, 128);
+    a.norm.part[((rb * csize + rank) * 2 + hf) * BM + r] = ss;
+    named_barrier(1, NT);
     bool met = true;
     if (threadIdx.x == EPI_LEADER) {
         red_add_release_gpu(arrive, 1u);
@@ -320,20 +323,19 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
             }
         }
     }
-    if (!epi_agree<128>(met, es.fail)) return false;
-    float tot = 0.f;
-    for (int q = 0; q < csize; ++q) tot += __ldcg(a.norm.part + (rb * csize + q) * BM + r);
+    if (!epi_agree<NT>(met, es.fail)) return false;
+    float tot = 0.f;  // fixed order: column tile, then half
+    for (int q = 0; q < 2 * csize; ++q) tot += __ldcg(a.norm.part + (rb * csize * 2 + q) * BM + r);
     const float rn = __frsqrt_rn(tot / (float)(csize * BN) + a.norm.eps);
 #pragma unroll 1
     for (int p = 0; p < PASSES; ++p) {
-        uint32_t xw[64];
-        tmem_ld_32x32b_x32(tacc + p * 128, *reinterpret_cast<uint32_t(*)[32]>(&xw[0]));
-        tmem_ld_32x32b_x32(tacc + p * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&xw[32]));
+        uint32_t xw[32];
+        tmem_ld_32x32b_x32(tacc + p * 128 + hf * 64, xw);
         tmem_ld_wait();
-        stg_acquire<128>();
-        const uint4* gp = reinterpret_cast<const uint4*>(gam + p * 256);
+        stg_acquire<NT>();
+        const uint4* gp = reinterpret_cast<const uint4*>(gam + (p * 128 + hf * 64) * 2);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 8; ++u) {
             const uint4 gv = gp[u];
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
             uint32_t o[4];
@@ -342,9 +344,9 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
                 const uint32_t xv = xw[4 * u + e];
                 o[e] = pack_bf16(bf16_lo(gw[e]) * rbf(bf16_lo(xv) * rn), bf16_hi(gw[e]) * rbf(bf16_hi(xv) * rn));
             }
-            *reinterpret_cast<uint4*>(stg_chunk(stg, r, u)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(stg_chunk(stg, r, hf * 8 + u)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        stg_store<128>(stg, tmY, n0 + p * 128, n0 + p * 128 + 64, m0);
+        stg_store<NT>(stg, tmY, n0 + p * 128, n0 + p * 128 + 64, m0);
     }
     tc_fence_before();
     mbar_arrive(acc_empty);
@@ -648,7 +650,7 @@ __global__ void __launch_bounds__(EpiShape<EPI>::THREADS, 1)
             if (et < BN / 8)
                 reinterpret_cast<uint4*>(smem + C::GAMMA_OFF)[et] =
                     __ldg(reinterpret_cast<const uint4*>(args.norm.gamma + rank * BN) + et);
-            named_barrier(1, 128);
+            named_barrier(1, EpiShape<EPI>::NT);
         }
         int local = 0;
         for (int t = first; t < limit; t += step, ++local) {
@@ -670,8 +672,8 @@ __global__ void __launch_bounds__(EpiShape<EPI>::THREADS, 1)
                     break;
                 }
             } else if constexpr (RN) {
-                if (!epilogue_residual_norm<BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, tl.m0, tl.n0, rank, n_tiles,
-                                                smem + C::GAMMA_OFF, &acc_empty[acc], &acc_full[acc], aph,
+                if (!epilogue_residual_norm<BN>(args, &tmC, &tmR, &tmV, stg, es, tacc, r, hf, tl.m0, tl.n0, rank,
+                                                n_tiles, smem + C::GAMMA_OFF, &acc_empty[acc], &acc_full[acc], aph,
                                                 abort_flag)) {
                     ok = false;
                     break;
@@ -1044,7 +1046,7 @@ bool gemm_norm_preferred(int M, int N) {
     return tiles >= 2LL * device_sm_count();
 }
 
-size_t gemm_norm_part_floats(int M) { return (size_t)((M + BM - 1) / BM) * 8 * BM; }
+size_t gemm_norm_part_floats(int M) { return (size_t)((M + BM - 1) / BM) * 8 * 2 * BM; }
 size_t gemm_norm_count_ints(int M) { return (size_t)((M + BM - 1) / BM) * 2; }
 
 bool encode_skinny_x_map(CUtensorMap* map, const void* X, uint64_t rows, uint64_t K) {

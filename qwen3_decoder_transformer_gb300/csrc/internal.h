@@ -72,7 +72,7 @@ cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st);
 // EPI_RESIDUAL_NORM: the residual epilogue followed by the next RMSNorm of the updated rows,
 // Y = bf16(gamma * bf16(X * rsqrt(mean(X^2) + eps))) with X the new residual stream. The N / BN column
 // tiles of a row block (at most 8) run at the same time on different CTAs of one cooperative launch and
-// exchange per-row partial sums of squares through part ([row blocks][8][128] floats), meeting on
+// exchange per-row partial sums of squares through part ([row blocks][8 tiles][2 halves][128] floats), meeting on
 // count ([row blocks][2]: arrivals, departures; zero before the first launch, left zero by each).
 struct NormArgs {
     const __nv_bfloat16* gamma;

@@ -228,7 +228,7 @@ def test_gemm_residual_norm(bd, M, N, K):
     assert (got_y == ref_y).mean() > 0.99
     # the meeting counters are left zero for the next call
     rows_blocks = (M + 127) // 128
-    assert not part.view(torch.int32)[rows_blocks * 8 * 128:].any()
+    assert not part.view(torch.int32)[rows_blocks * 16 * 128:].any()
 
 
 def test_gemm_residual_norm_unsupported_shape(bd):
