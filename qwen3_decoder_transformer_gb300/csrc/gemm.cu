@@ -1038,12 +1038,10 @@ bool gemm_norm_fusable(int M, int N) {
 }
 
 bool gemm_norm_preferred(int M, int N) {
-    // The row block's meeting adds about 3.7 us to a tile's epilogue (0.6B o_proj at 2048 rows: 14.8 us
-    // fused against 11.1 + 4.2 for GEMM and RMSNorm apart, yet the whole step is slower fused); with at
-    // least two tiles per SM it hides behind the next tile's main loop (32768 rows: 112 against 118 us).
-    if (!gemm_norm_fusable(M, N)) return false;
-    const long long tiles = (long long)((M + BM - 1) / BM) * (N / gemm_tile_n(M, N, EPI_RESIDUAL_NORM));
-    return tiles >= 2LL * device_sm_count();
+    // With the eight-warp epilogue the row block's meeting costs less than the separate RMSNorm pass at
+    // every measured size (0.6B: 2048 rows 2.83 -> 2.79 ms per prefill step; 32768 rows 118 -> 112 us
+    // per o_proj and norm).
+    return gemm_norm_fusable(M, N);
 }
 
 size_t gemm_norm_part_floats(int M) { return (size_t)((M + BM - 1) / BM) * 8 * 2 * BM; }
