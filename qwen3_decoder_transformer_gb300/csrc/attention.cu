@@ -7,8 +7,9 @@
 //
 // Decode: one query per (sequence, query head) against the whole cache. A CTA owns a chunk (256 to
 // 1024 keys) of one (sequence, kv head) and serves all g query heads of that group from one read of
-// K and V (16-byte coalesced loads). Partial (max, sum, output) triples go to a workspace; a second
-// kernel merges the chunks by log-sum-exp.
+// K and V, streamed by TMA into shared memory; the scores and the weighted sum run as warp-level
+// tensor-core contractions with the group's heads as the narrow dimension. Partial (max, sum,
+// output) triples go to a workspace; a second kernel merges the chunks by log-sum-exp.
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
@@ -801,31 +802,73 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
 // Keys per decode CTA: long chunks amortise each CTA's fixed work over long caches, shorter ones keep
 // more CTAs busy on short caches; a rolling buffer uses the shortest so that its ring (a multiple of
 // 256) never wraps inside a chunk.
-constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256, DEC_THREADS = 128;
+constexpr int DEC_CHUNK = 1024, DEC_CHUNK_SHORT = 512, DEC_CHUNK_RING = 256;
+// Four compute warps and one TMA warp. The TMA warp streams the chunk's key tiles, then its value
+// tiles (128 cache rows each, 128-byte swizzle) through two or three shared-memory stages; the compute warps
+// run the two small contractions on the tensor cores with warp-level mma (m16n8k16, bf16 in, fp32
+// accumulate): scores S^T = K q^T with the chunk's keys as rows and the group's query heads as the
+// 8 columns, and O^T += V^T P^T with head_dim as rows. That leaves the CUDA cores only the softmax of
+// G x CH scores, so the kernel streams K and V at HBM speed for any group size.
+constexpr int DEC_WARPS = 4, DEC_THREADS = 32 * (DEC_WARPS + 1), DEC_TK = 128;
 
-__device__ __forceinline__ float2 bf16x2_f2(uint32_t v) { return make_float2(bf16_lo(v), bf16_hi(v)); }
+template <int DH, int G, int CH>
+struct DecLayout {
+    static constexpr int NCH = DH / 64;                  // 64-column boxes per cache row
+    static constexpr int STAGE = DEC_TK * DH * 2;        // bytes per stage: 32 KB (dh 128) / 16 KB (dh 64)
+    static constexpr int NS = DH >= 128 ? 2 : 3;         // stages: two CTAs fit an SM
+    // scores / probabilities [G][CH], later reused for the cross-warp sums [warps][G][DH]
+    static constexpr int SBUF = G * CH > DEC_WARPS * G * DH ? G * CH : DEC_WARPS * G * DH;
+    static constexpr int SBUF_OFF = NS * STAGE;
+    static constexpr int BAR_OFF = SBUF_OFF + SBUF * 4;
+    static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 16 + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// D (16x8 fp32) += A (16x16 bf16, row-major) B (16x8 bf16, column-major), one warp
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Shared address of the 16-byte chunk `dc` (8 columns) of row `row` in a stage of NCH boxes of
+// 128 rows x 128 bytes written by TMA with the 128-byte swizzle (box base 1024-byte aligned).
+template <int NCH>
+__device__ __forceinline__ uint32_t swz_addr(uint32_t stage, int row, int dc) {
+    return stage + (uint32_t)((dc >> 3) * DEC_TK * 128 + row * 128 + (((dc & 7) ^ (row & 7)) << 4));
+}
 
 // Workspace layout per (b, q-head, split): [m, l] floats, then DH floats of unnormalised output.
-// A CTA owns CH keys of one (sequence, kv head). Eight lanes share a key row (16 elements,
-// two 16-byte loads each), so a warp covers four keys per step and a score needs three shuffle
-// levels; products run as paired fp32 FMAs on (even, odd) element pairs.
+// A CTA owns CH keys of one (sequence, kv head) and serves all G query heads of that group from one
+// read of K and V.
 template <int DH, int G, int CH>
 __global__ void __launch_bounds__(DEC_THREADS)
-    attn_decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
-                             const __nv_bfloat16* __restrict__ vc, int Hq, int Hkv, int cap,
-                             const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
-                             float* __restrict__ work) {
-    constexpr int UNR = 8;  // key rows in flight per lane and pass
-    constexpr int LPK = 8;                      // lanes per key row
-    constexpr int EPL = DH / LPK;               // elements per lane: 16 (dh 128) or 8 (dh 64)
-    constexpr int WPL = EPL / 2;                // bf16x2 words per lane
-    constexpr int VPL = EPL / 8;                // 16-byte loads per lane and key
-    constexpr int KPW = 32 / LPK;               // keys per warp per step
-    constexpr int KPS = KPW * (DEC_THREADS / 32);  // keys per block step
+    attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                             const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, const int* __restrict__ len0p,
+                             const int* __restrict__ meta, int window, int ring, float* __restrict__ work, int* err) {
+    static_assert(G <= 8, "the query heads of a group are the 8 columns of the mma");
+    using Ly = DecLayout<DH, G, CH>;
+    constexpr int NCH = Ly::NCH;
+    constexpr int MT = DEC_TK / 16 / DEC_WARPS;  // 16-key tiles per warp and stage
     constexpr int REC = DH + 2;
-    // scores / probabilities [G][CH], later reused for the cross-warp sums [warps][G][DH]
-    constexpr int SBUF = G * CH > (DEC_THREADS / 32) * G * DH ? G * CH : (DEC_THREADS / 32) * G * DH;
-    __shared__ float sbuf[SBUF];
+    extern __shared__ uint8_t dsm_raw[];
+    const uint32_t raw_addr = smem_u32(dsm_raw);
+    uint8_t* dsm = dsm_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    float* sbuf = reinterpret_cast<float*>(dsm + Ly::SBUF_OFF);
+    uint64_t* full = reinterpret_cast<uint64_t*>(dsm + Ly::BAR_OFF);
+    uint64_t* empty = full + Ly::NS;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + Ly::NS);
     __shared__ float stat[G][2];
     auto sc = reinterpret_cast<float(*)[CH]>(sbuf);
     auto red = reinterpret_cast<float(*)[G][DH]>(sbuf);
@@ -839,10 +882,10 @@ __global__ void __launch_bounds__(DEC_THREADS)
     const int lo = window > 0 ? max(0, n - window) : 0;
     const int s0 = lo / CH * CH + split * CH, s1 = min(n, s0 + CH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / LPK, li = lane % LPK;
+    const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates: group (row / column) and thread in group
     float* wb = work + (((size_t)b * Hq + (size_t)j * G) * nsplit + split) * REC;
-    // padding slots [ps, pe) of this sequence; slots below psh live in sequence 0; a rolling buffer
-    // stores slot s at s mod ring (ring a multiple of CH, so a chunk stays contiguous)
+    // padding slots [ps, pe) of this sequence; slots below psh (a multiple of 128) live in sequence 0;
+    // a rolling buffer stores slot s at s mod ring (ring a multiple of CH, so a chunk stays contiguous)
     int ps = 0, pe = 0, psh = 0;
     if (meta) {
         ps = meta[0];
@@ -856,75 +899,101 @@ __global__ void __launch_bounds__(DEC_THREADS)
         }
         return;
     }
-    const ptrdiff_t shift = ring ? (ptrdiff_t)(s0 % ring) - s0 : 0;
-    const ptrdiff_t kv_own = (ptrdiff_t)(((size_t)b * Hkv + j) * cap) * DH + shift * DH;
-    const ptrdiff_t kv_shared = (ptrdiff_t)((size_t)j * cap) * DH + shift * DH;
-    const float sl2 = kLog2e / sqrtf((float)DH);
-    // this lane's slice of the G query vectors, pre-scaled into log2 units
-    float2 qv[G][WPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + (size_t)j * G + h) * DH + li * EPL);
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const uint4 x = src[v];
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = bf16x2_f2(w[e]);
-                qv[h][v * 4 + e] = make_float2(f.x * sl2, f.y * sl2);
-            }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Ly::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], DEC_WARPS);
         }
-    }
-    auto row_ptr = [&](const __nv_bfloat16* base, int s) {
-        return reinterpret_cast<const uint4*>(base + (s < psh ? kv_shared : kv_own) + (ptrdiff_t)s * DH + li * EPL);
-    };
-    // pass 1: scores (already in log2 units)
-    for (int base = s0; base < s1; base += KPS * UNR) {
-        uint4 kv[UNR][VPL];
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int s = base + u * KPS + warp * KPW + sub;
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) kv[u][v] = s < s1 ? row_ptr(kc, s)[v] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int s = base + u * KPS + warp * KPW + sub;
-            float d[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) {
-                    const uint32_t w[4] = {kv[u][v].x, kv[u][v].y, kv[u][v].z, kv[u][v].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc = fma2(bf16x2_f2(w[e]), qv[h][v * 4 + e], acc);
-                }
-                float t = acc.x + acc.y;
-#pragma unroll
-                for (int o = LPK / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                d[h] = t;
-            }
-            if (li == 0 && s < s1) {
-                const bool vis = s >= lo && (s < ps || s >= pe);  // outside the window, or padding
-#pragma unroll
-                for (int h = 0; h < G; ++h) sc[h][s - s0] = vis ? d[h] : -INFINITY;
-            }
-        }
-    }
-    // the first value rows do not depend on the scores: their loads overlap the exponentials below
-    uint4 vv0[UNR][VPL];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-        const int s = s0 + u * KPS + warp * KPW + sub;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) vv0[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
     }
     __syncthreads();
+    const int nt = (s1 - s0 + DEC_TK - 1) / DEC_TK;  // stages per pass
+    bool ok = true;
+
+    if (warp == DEC_WARPS) {
+        // ---------------- TMA warp: key tiles 0..nt-1, then value tiles (rows past the cache read as zero)
+        if (lane == 0) {
+            for (int it = 0; it < 2 * nt; ++it) {
+                const int pass = it >= nt, t = it - pass * nt, stg = it % Ly::NS;
+                if (it >= Ly::NS && !mbar_wait(&empty[stg], ((it / Ly::NS) - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int a = s0 + t * DEC_TK;
+                const int y = ring ? a % ring : a;
+                const int z = (a < psh ? 0 : b) * Hkv + j;
+                uint8_t* dst = dsm + stg * Ly::STAGE;
+                mbar_expect_tx(&full[stg], Ly::STAGE);
+                for (int cc = 0; cc < NCH; ++cc)
+                    tma_load_3d(dst + cc * DEC_TK * 128, pass ? &tmV : &tmK, &full[stg], cc * 64, y, z);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                if (err) atomicOr(err, ERR_TIMEOUT);
+            }
+        }
+        return;  // the compute warps wait for every stage it issued before they finish
+    }
+
+    // ---------------- compute warps (named barrier 1 spans these 128 threads only)
+    const float sl2 = kLog2e / sqrtf((float)DH);
+    // B fragments of q^T: column gq = query head gq of the group, rows = head_dim (zero columns past G)
+    uint32_t qf[DH / 16][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q + ((size_t)b * Hq + (size_t)j * G + gq) * DH);
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+            qf[ks][0] = gq < G ? qrow[ks * 8 + tq] : 0u;
+            qf[ks][1] = gq < G ? qrow[ks * 8 + 4 + tq] : 0u;
+        }
+    }
+    auto wait_full = [&](int it) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(&full[it % Ly::NS], (it / Ly::NS) & 1, abort_flag));
+    };
+    auto release = [&](int it) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[it % Ly::NS]);
+    };
+    // pass 1: scores S^T (keys x heads), in log2 units
+    for (int t = 0; t < nt && ok; ++t) {
+        if (!wait_full(t)) {
+            ok = false;
+            break;
+        }
+        const uint32_t stage = smem_u32(dsm + (t % Ly::NS) * Ly::STAGE);
+        const int a = s0 + t * DEC_TK;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int kb = (m * DEC_WARPS + warp) * 16;  // first key of this 16-key tile within the stage
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const int lrow = kb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                uint32_t af[4];
+                ldsm_x4(swz_addr<NCH>(stage, lrow, 2 * ks + (lane >> 4)), af);
+                mma_16816(d, af, qf[ks][0], qf[ks][1]);
+            }
+            // d[0], d[1]: key kb + gq, heads 2tq, 2tq+1; d[2], d[3]: key kb + gq + 8
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int s = a + kb + gq + 8 * r;
+                if (s < s1) {
+                    const bool vis = s >= lo && (s < ps || s >= pe);  // outside the window, or padding
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        if (2 * tq + c < G) sc[2 * tq + c][s - s0] = vis ? d[2 * r + c] * sl2 : -INFINITY;
+                }
+            }
+        }
+        release(t);
+    }
+    named_barrier(1, 32 * DEC_WARPS);
     // chunk max and exponentials, one warp per head
     const int cnt = s1 - s0;
-    for (int h = warp; h < G; h += DEC_THREADS / 32) {
+    for (int h = warp; h < G; h += DEC_WARPS) {
         float mx = -INFINITY;
         for (int i = lane; i < cnt; i += 32) mx = fmaxf(mx, sc[h][i]);
 #pragma unroll
@@ -942,71 +1011,69 @@ __global__ void __launch_bounds__(DEC_THREADS)
             stat[h][1] = sum;
         }
     }
-    __syncthreads();
-    // pass 2: weighted sum of V rows, (even, odd) element pairs per lane
-    float2 acc[G][WPL];
+    named_barrier(1, 32 * DEC_WARPS);
+    // pass 2: O^T (head_dim x heads) += V^T P^T, P rounded to bf16 for the mma
+    float o[DH / 16][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < WPL; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    auto accumulate = [&](const uint4 (&vv)[UNR][VPL], int base) {
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int s = base + u * KPS + warp * KPW + sub;
-            if (s >= s1) continue;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float p = sc[h][s - s0];
-                const float2 pp = make_float2(p, p);
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) {
-                    const uint32_t w[4] = {vv[u][v].x, vv[u][v].y, vv[u][v].z, vv[u][v].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[h][v * 4 + e] = fma2(bf16x2_f2(w[e]), pp, acc[h][v * 4 + e]);
+    for (int mt = 0; mt < DH / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    auto prob = [&](int s) -> float { return (gq < G && s < s1) ? sc[gq][s - s0] : 0.f; };
+    for (int t = 0; t < nt && ok; ++t) {
+        if (!wait_full(nt + t)) {
+            ok = false;
+            break;
+        }
+        uint8_t* stage_p = dsm + ((nt + t) % Ly::NS) * Ly::STAGE;
+        const uint32_t stage = smem_u32(stage_p);
+        const int a = s0 + t * DEC_TK;
+        if (a + DEC_TK > s1) {
+            // value rows past the last key hold stale cache contents: zero this warp's, so that
+            // 0 * NaN cannot reach O
+            for (int m = 0; m < MT; ++m) {
+                const int kb = (m * DEC_WARPS + warp) * 16;
+                for (int e = lane; e < 16 * NCH * 8; e += 32) {
+                    const int row = kb + e / (NCH * 8), dc = e % (NCH * 8);
+                    if (a + row >= s1)
+                        *reinterpret_cast<uint4*>(stage_p + (swz_addr<NCH>(stage, row, dc) - stage)) =
+                            make_uint4(0, 0, 0, 0);
                 }
             }
+            __syncwarp();
         }
-    };
-    accumulate(vv0, s0);
-    for (int base = s0 + KPS * UNR; base < s1; base += KPS * UNR) {
-        uint4 vv[UNR][VPL];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const int s = base + u * KPS + warp * KPW + sub;
+        for (int m = 0; m < MT; ++m) {
+            const int kb = (m * DEC_WARPS + warp) * 16;
+            const int s = a + kb + 2 * tq;
+            const uint32_t b0 = pack_bf16(prob(s), prob(s + 1)), b1 = pack_bf16(prob(s + 8), prob(s + 9));
+            const int vrow = kb + (lane & 7) + ((lane >> 4) & 1) * 8;  // key row of this lane's address
 #pragma unroll
-            for (int v = 0; v < VPL; ++v) vv[u][v] = s < s1 ? row_ptr(vc, s)[v] : make_uint4(0, 0, 0, 0);
-        }
-        accumulate(vv, base);
-    }
-    // reduce over the KPW key slots of the warp, then over warps
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < WPL; ++e) {
-            float x = acc[h][e].x, y = acc[h][e].y;
-#pragma unroll
-            for (int o = LPK; o < 32; o <<= 1) {
-                x += __shfl_xor_sync(0xffffffffu, x, o);
-                y += __shfl_xor_sync(0xffffffffu, y, o);
+            for (int mt = 0; mt < DH / 16; ++mt) {
+                uint32_t af[4];
+                ldsm_x4_trans(swz_addr<NCH>(stage, vrow, 2 * mt + ((lane >> 3) & 1)), af);
+                mma_16816(o[mt], af, b0, b1);
             }
-            acc[h][e] = make_float2(x, y);
         }
-    __syncthreads();  // every warp is done with the probabilities before their space is reused
-    if (sub == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < WPL; ++e) {
-                red[warp][h][li * EPL + 2 * e] = acc[h][e].x;
-                red[warp][h][li * EPL + 2 * e + 1] = acc[h][e].y;
-            }
+        if (a + DEC_TK > s1) fence_proxy_async_smem();  // the zeroing stores precede the next TMA write
+        release(nt + t);
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * DH; i += DEC_THREADS) {
+    if (!ok) {
+        *abort_flag = 1;
+        if (err) atomicOr(err, ERR_TIMEOUT);
+    }
+    named_barrier(1, 32 * DEC_WARPS);  // every warp is done with the probabilities before their space is reused
+    // o[mt]: rows (head_dim) mt*16 + gq (+8), columns (heads) 2tq, 2tq+1
+#pragma unroll
+    for (int mt = 0; mt < DH / 16; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (2 * tq + c < G) red[warp][2 * tq + c][mt * 16 + gq + 8 * r] = o[mt][2 * r + c];
+    named_barrier(1, 32 * DEC_WARPS);
+    for (int i = threadIdx.x; i < G * DH; i += 32 * DEC_WARPS) {
         const int h = i / DH, dd = i % DH;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < DEC_THREADS / 32; ++w) v += red[w][h][dd];
+        for (int w = 0; w < DEC_WARPS; ++w) v += red[w][h][dd];
         float* rec = wb + (size_t)h * nsplit * REC;
         rec[2 + dd] = v;
         if (dd == 0) {
@@ -1086,26 +1153,34 @@ int decode_nsplit(int cap, int window, int ring) {
     return window > 0 ? std::min(all, (window + ch - 1) / ch + 1) : all;
 }
 
+template <int DH, int G, int CH>
+cudaError_t decode_launch_ch(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* q, int Hq,
+                             int Hkv, const int* len0, SeqMap sm, float* work, int* err, cudaStream_t st) {
+    constexpr int smem = DecLayout<DH, G, CH>::SMEM;  // limit raised in attention_prepare
+    return launch_pdl(attn_decode_split_kernel<DH, G, CH>, grid, dim3(DEC_THREADS), smem, st, tk, tv, q, Hq, Hkv, len0,
+                      sm.meta, sm.window, sm.ring, work, err);
+}
+
 template <int DH, int G>
 cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                            int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
+                            int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out, int* err,
                             cudaStream_t st) {
     const int nsplit = decode_nsplit(cap, sm.window, sm.ring);
     if (nsplit > COMB_MAX_SPLITS) return cudaErrorInvalidValue;
     const dim3 grid(nsplit, Hkv, B);
+    CUtensorMap tk, tv;
+    if (!encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) || !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
+        return cudaErrorInvalidValue;
     cudaError_t e;
     switch (decode_chunk(cap, sm.ring)) {
         case DEC_CHUNK_RING:
-            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK_RING>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq,
-                           Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
+            e = decode_launch_ch<DH, G, DEC_CHUNK_RING>(grid, tk, tv, q, Hq, Hkv, len0, sm, work, err, st);
             break;
         case DEC_CHUNK_SHORT:
-            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK_SHORT>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq,
-                           Hkv, cap, len0, sm.meta, sm.window, sm.ring, work);
+            e = decode_launch_ch<DH, G, DEC_CHUNK_SHORT>(grid, tk, tv, q, Hq, Hkv, len0, sm, work, err, st);
             break;
         default:
-            e = launch_pdl(attn_decode_split_kernel<DH, G, DEC_CHUNK>, grid, dim3(DEC_THREADS), 0, st, q, kc, vc, Hq, Hkv,
-                           cap, len0, sm.meta, sm.window, sm.ring, work);
+            e = decode_launch_ch<DH, G, DEC_CHUNK>(grid, tk, tv, q, Hq, Hkv, len0, sm, work, err, st);
     }
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, out);
@@ -1113,13 +1188,13 @@ cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, con
 
 template <int DH>
 cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
-                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
+                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out, int* err,
                              cudaStream_t st) {
     switch (Hq / Hkv) {
-        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
-        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
-        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
-        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -1222,15 +1297,36 @@ size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int rin
 
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
-                               cudaStream_t st) {
+                               int* err, cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
     if (sm.ring && (sm.ring % DEC_CHUNK_RING || sm.ring != cap)) return cudaErrorInvalidValue;
-    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
-    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, st);
+    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
     return cudaErrorInvalidValue;
 }
 
 int attn_decode_kernel_count() { return 2; }
+
+template <int DH, int G, int CH>
+cudaError_t decode_prepare_one() {
+    return cudaFuncSetAttribute(attn_decode_split_kernel<DH, G, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                DecLayout<DH, G, CH>::SMEM);
+}
+template <int DH, int G>
+cudaError_t decode_prepare_g() {
+    cudaError_t e = decode_prepare_one<DH, G, DEC_CHUNK>();
+    if (e == cudaSuccess) e = decode_prepare_one<DH, G, DEC_CHUNK_SHORT>();
+    if (e == cudaSuccess) e = decode_prepare_one<DH, G, DEC_CHUNK_RING>();
+    return e;
+}
+template <int DH>
+cudaError_t decode_prepare_dh() {
+    cudaError_t e = decode_prepare_g<DH, 1>();
+    if (e == cudaSuccess) e = decode_prepare_g<DH, 2>();
+    if (e == cudaSuccess) e = decode_prepare_g<DH, 4>();
+    if (e == cudaSuccess) e = decode_prepare_g<DH, 8>();
+    return e;
+}
 
 cudaError_t attention_prepare() {
     const void* fns[] = {(const void*)attn_prefill_tc_kernel<128, 1>, (const void*)attn_prefill_tc_kernel<128, 2>,
@@ -1242,7 +1338,8 @@ cudaError_t attention_prepare() {
         cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    cudaError_t e = decode_prepare_dh<128>();
+    return e == cudaSuccess ? decode_prepare_dh<64>() : e;
 }
 
 }  // namespace q3

@@ -186,9 +186,10 @@ size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chu
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
 // work: attn_decode_workspace() bytes of chunk records, merged by a second kernel.
+// err (may be null): ERR_TIMEOUT is or-ed in when a copy-ring wait gives up.
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
-                               cudaStream_t st);
+                               int* err, cudaStream_t st);
 int attn_decode_kernel_count();
 // Allocation-free decode attention: size of the library's fixed scratch, and its device address on
 // the current device (looked up on first use per device).

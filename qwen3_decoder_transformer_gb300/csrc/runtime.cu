@@ -235,7 +235,7 @@ int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits
         }));
         TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
             return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                      c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, st);
+                                      c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, st);
         }));
         TRY(skinny(c, K_GEMM_O, c->tB_o[l], c->tX_attn, B, d, c->q_width, nullptr, s_o, st));
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
@@ -298,7 +298,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         if (decode) {
             TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
                 return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                          c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, st);
+                                          c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, st);
             }));
         } else {
             int split = 0, chunks = 1;
@@ -1027,9 +1027,10 @@ int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int
     if (window < 0 || (ring && (ring != cap || ring % 256 || window < 1))) return QWEN3_E_ARG;
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
                               Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<float*>(work),
-                              static_cast<bf16*>(out),
+                              static_cast<bf16*>(out), nullptr,
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
@@ -1043,10 +1044,11 @@ int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void*
     const int grp = Hq / Hkv;
     if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return QWEN3_E_ARG;
     if (attn_decode_workspace(B, Hq, dh, cap, 0, 0) > attn_decode_noalloc_max_bytes()) return QWEN3_E_ARG;
+    if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     float* scratch = nullptr;
     if (attn_decode_noalloc_scratch(&scratch) != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
-                              Hq, Hkv, dh, cap, len0, SeqMap{}, scratch, static_cast<bf16*>(out),
+                              Hq, Hkv, dh, cap, len0, SeqMap{}, scratch, static_cast<bf16*>(out), nullptr,
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
