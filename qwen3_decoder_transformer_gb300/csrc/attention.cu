@@ -453,7 +453,25 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
 // scores load while the softmax warps finish the current item, whose output accumulator is then
 // handed back to the MMA warp (o_free) before the next item's first PV overwrites it. Tiles are
 // counted across items (g), so ring stages, score regions and barrier phases simply continue.
-constexpr int PS_THREADS = 64 + 128;
+// Tensor memory holds three score regions and the output accumulator (4 x 128 columns): the scores
+// run two tiles ahead of P V, so the scores a softmax pass needs are complete when it starts. With
+// two regions the MMA thread could issue S of tile j+2 only after P V of tile j; since a thread that
+// issues tcgen05.mma waits while the pipe is full, it then sat behind that S while P of tile j+1
+// was already waiting, and the softmax warps waited for their next scores: about 2,100 cycles per
+// tile against 1,024 of MMA work (clock64 timeline of one CTA, 0.6B 1x2048).
+constexpr int PS_THREADS = 64 + 128 + 64;  // + a TMA warp for the value tiles and a P V MMA warp
+constexpr int PS_KST = 3, PS_VST = 2;      // key and value ring stages
+template <int DH>
+struct PsLayout {
+    static constexpr int NCH = DH / 64;
+    static constexpr int Q_BYTES = TC_BM * DH * 2;
+    static constexpr int KV_BYTES = TC_BN * DH * 2;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_BYTES;
+    static constexpr int V_OFF = K_OFF + PS_KST * KV_BYTES;
+    static constexpr int BAR_OFF = V_OFF + PS_VST * KV_BYTES;
+    static constexpr int SMEM = BAR_OFF + 256 + 1024;
+};
 
 template <int DH>
 __global__ void __launch_bounds__(PS_THREADS, 1)
@@ -461,27 +479,29 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                                    const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv, int B,
                                    const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
                                    __nv_bfloat16* __restrict__ out, int* err) {
-    using Ly = TcLayout<DH, 1>;
+    using Ly = PsLayout<DH>;
     constexpr int NCH = Ly::NCH;
     constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
     constexpr uint32_t IDESC_O = idesc_bf16(TC_BM, DH, true);
-    constexpr uint32_t TM_O = 2 * TC_BN;
+    constexpr int NR = 3;                  // score regions in tensor memory
+    constexpr uint32_t TM_O = NR * TC_BN;  // then the output accumulator: 512 columns in all
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::BAR_OFF);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 1;
-    uint64_t* k_full = bars + 2;   // [2]
-    uint64_t* v_full = bars + 4;   // [2]
-    uint64_t* k_empty = bars + 6;  // [2]
-    uint64_t* v_empty = bars + 8;  // [2]
-    uint64_t* s_full = bars + 10;  // [2] per score region
-    uint64_t* p_full = bars + 12;  // [2] per score region
-    uint64_t* o_done = bars + 14;
-    uint64_t* o_free = bars + 15;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+    uint64_t* k_full = bars + 2;   // [PS_KST]
+    uint64_t* k_empty = bars + 5;  // [PS_KST]
+    uint64_t* v_full = bars + 8;   // [PS_VST]
+    uint64_t* v_empty = bars + 10; // [PS_VST]
+    uint64_t* s_full = bars + 12;  // [NR] per score region
+    uint64_t* p_full = bars + 15;  // [NR] per score region
+    uint64_t* o_done = bars + 18;
+    uint64_t* o_free = bars + 19;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+    uint64_t* r_free = bars + 22;  // [NR] P V of the region's tile is done: the region can take new scores
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (T + TC_BM - 1) / TC_BM;
@@ -491,13 +511,18 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < PS_KST; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < PS_VST; ++i) {
+            mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < NR; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
+            mbar_init(&r_free[i], 1);
         }
         mbar_init(o_done, 1);
         mbar_init(o_free, 128);
@@ -563,14 +588,32 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 for (int cc = 0; cc < NCH; ++cc)
                     tma_load_3d(smem + Ly::Q_OFF + cc * TC_BM * 128, &tmQ, q_full, cc * 64, it.q0, it.b * Hq + it.h);
                 for (int i = 0; i < it.n_tiles; ++i, ++g) {
-                    const int s = g & 1, j = tile_j(it, i);
-                    const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
+                    const int s = g % PS_KST, j = tile_j(it, i);
+                    const uint32_t free_ph = ((g / PS_KST) & 1) ^ 1;
                     const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
                     const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
                     if (!mbar_wait(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
                     for (int cc = 0; cc < NCH; ++cc)
                         tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmK, &k_full[s], cc * 64, y, z);
+                }
+            }
+        }
+    } else if (warp == 6) {
+        // ---------------- TMA producer for the value tiles, a warp of its own: a key stage is freed by
+        // its scores, a value stage by its P V, two tiles apart, so one in-order producer would hold
+        // back the keys of the scores that run ahead
+        if (lane == 0) {
+            int g = 0;
+            for (int round = 0; ok; ++round) {
+                const Item it = item_of(round);
+                if (it.n_tiles == 0) break;
+                const int jkv = it.h / (Hq / Hkv);
+                for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                    const int s = g & 1, j = tile_j(it, i);
+                    const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
+                    const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
+                    const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
                     if (!mbar_wait(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
                     for (int cc = 0; cc < NCH; ++cc)
@@ -579,38 +622,52 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer (all lanes walk the schedule; lane 0 issues)
-        int g = 0;  // tiles of earlier items
-        for (int round = 0; ok; ++round) {
-            const Item it = item_of(round);
-            const int nt = it.n_tiles;
-            if (nt == 0) break;
-            // scores of local tile i into region (g + i) & 1; the item's last score releases Q
-            auto issue_s = [&](int i) -> bool {
-                const int gi = g + i, s = gi & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (gi >> 1) & 1, abort_flag))) return false;
-                tc_fence_after();
-                if (lane == 0) {
+        // ---------------- score MMAs: S of tile gi (key stage gi % PS_KST) into region gi % NR, once
+        // P V of tile gi - NR (issued by warp 7) has finished reading that region. A thread issuing
+        // tcgen05.mma waits while the pipe is full, so the score and the P V batches come from two
+        // threads: while one waits with its batch, the other's work keeps the pipe fed.
+        if (lane == 0) {
+            int g = 0;  // tiles of earlier items
+            for (int round = 0; ok; ++round) {
+                const Item it = item_of(round);
+                const int nt = it.n_tiles;
+                if (nt == 0) break;
+                if (!mbar_wait(q_full, round & 1, abort_flag)) { ok = false; break; }
+                for (int i = 0; i < nt; ++i) {
+                    const int gi = g + i, s = gi % PS_KST, r = gi % NR;
+                    if (!mbar_wait(&k_full[s], (gi / PS_KST) & 1, abort_flag)) { ok = false; break; }
+                    // region r's next completion would be P V of tile gi itself, not yet possible: the
+                    // parity wait cannot alias
+                    if (gi >= NR && !mbar_wait(&r_free[r], ((gi - NR) / NR) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     const uint32_t sq = smem_u32(smem + Ly::Q_OFF);
                     const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < DH / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
-                        umma_bf16_ss(tmem + s * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off),
+                        umma_bf16_ss(tmem + r * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off),
                                      IDESC_S, kk > 0);
                     }
-                    umma_commit(&s_full[s]);
+                    umma_commit(&s_full[r]);
                     umma_commit(&k_empty[s]);
-                    if (i == nt - 1) umma_commit(q_empty);
+                    if (i == nt - 1) umma_commit(q_empty);  // the item's last score releases Q
                 }
-                __syncwarp();
-                return true;
-            };
-            ok = __all_sync(0xffffffffu, mbar_wait(q_full, round & 1, abort_flag));
-            if (ok) ok = issue_s(0);
-            if (ok && nt > 1) ok = issue_s(1);
+                g += nt;
+            }
+        }
+    } else if (warp == 7) {
+        // ---------------- P V MMAs: O += P V of tile gi, P read from region gi % NR (A operand in
+        // tensor memory), V from value stage gi & 1
+        int g = 0;
+        for (int round = 0; ok; ++round) {
+            const Item it = item_of(round);
+            const int nt = it.n_tiles;
+            if (nt == 0) break;
             for (int i = 0; ok && i < nt; ++i) {
-                const int gi = g + i, s = gi & 1;
+                const int gi = g + i, s = gi & 1, r = gi % NR;
                 const int j = tile_j(it, i);
                 if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
                 uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
@@ -624,24 +681,24 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (i == 0 && !__all_sync(0xffffffffu, mbar_wait(o_free, (round & 1) ^ 1, abort_flag))) {
-                    ok = false;  // the previous item's output is still being read
-                    break;
-                }
-                if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
-                tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t svv = smem_u32(sv);
+                    bool w = i > 0 || mbar_wait(o_free, (round & 1) ^ 1, abort_flag);  // previous item's O read out
+                    w = w && mbar_wait(&p_full[r], (gi / NR) & 1, abort_flag);
+                    if (w) {
+                        tc_fence_after();
+                        const uint32_t svv = smem_u32(sv);
 #pragma unroll
-                    for (int kk = 0; kk < TC_BN / 16; ++kk) {
-                        const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
-                        umma_bf16_ts(tmem + TM_O, tmem + s * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
+                        for (int kk = 0; kk < TC_BN / 16; ++kk) {
+                            const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
+                            umma_bf16_ts(tmem + TM_O, tmem + r * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
+                        }
+                        umma_commit(o_done);
+                        umma_commit(&v_empty[s]);
+                        umma_commit(&r_free[r]);
                     }
-                    umma_commit(o_done);
-                    umma_commit(&v_empty[s]);
+                    ok = w;
                 }
-                __syncwarp();
-                if (i + 2 < nt) ok = issue_s(i + 2);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
             }
             g += nt;
         }
@@ -667,10 +724,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
             const int t = it.q0 + row, pos = len0 + t;
             float m_used = -INFINITY, l = 0.f;
             for (int i = 0; i < nt; ++i) {
-                const int gi = g + i, r = gi & 1;
+                const int gi = g + i, r = gi % NR;
                 const int j = tile_j(it, i);
                 const uint32_t tm_s = tmem + lane_off + r * TC_BN;
-                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[r], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[r], (gi / NR) & 1, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[TC_BN];
 #pragma unroll
@@ -1242,7 +1299,7 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
     const long long items = (long long)((T + TC_BM - 1) / TC_BM) * Hq * B;
     const unsigned grid = (unsigned)std::min<long long>(items, device_sm_count());
-    return launch_pdl(attn_prefill_persistent_kernel<DH>, dim3(grid), dim3(PS_THREADS), TcLayout<DH, 1>::SMEM, st, tq, tk,
+    return launch_pdl(attn_prefill_persistent_kernel<DH>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st, tq, tk,
                       tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
 }
 
@@ -1333,7 +1390,7 @@ cudaError_t attention_prepare() {
                          (const void*)attn_prefill_tc_kernel<64, 1>,  (const void*)attn_prefill_tc_kernel<64, 2>,
                          (const void*)attn_prefill_persistent_kernel<128>, (const void*)attn_prefill_persistent_kernel<64>};
     const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM,
-                        TcLayout<128, 1>::SMEM, TcLayout<64, 1>::SMEM};
+                        PsLayout<128>::SMEM, PsLayout<64>::SMEM};
     for (int i = 0; i < 6; ++i) {
         cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
