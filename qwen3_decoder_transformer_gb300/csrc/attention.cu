@@ -497,7 +497,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
     uint64_t* v_empty = bars + 10; // [PS_VST]
     uint64_t* s_full = bars + 12;  // [NR] per score region
     uint64_t* p_full = bars + 15;  // [NR] per score region
-    uint64_t* o_done = bars + 18;
     uint64_t* o_free = bars + 19;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
@@ -524,7 +523,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
             mbar_init(&p_full[i], 128);
             mbar_init(&r_free[i], 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(o_free, 128);
         *abort_flag = 0;
         fence_mbar_init();
@@ -692,7 +690,6 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                             const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
                             umma_bf16_ts(tmem + TM_O, tmem + r * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
                         }
-                        umma_commit(o_done);
                         umma_commit(&v_empty[s]);
                         umma_commit(&r_free[r]);
                     }
@@ -708,14 +705,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tm_o = tmem + lane_off + TM_O;
         const float sl2 = kLog2e / sqrtf((float)DH);
-        int pv_seen = 0;  // PV completions confirmed so far, across items
-        auto confirm_pv = [&](int upto) -> bool {
-            while (pv_seen < upto) {
-                if (!mbar_wait(o_done, pv_seen & 1, abort_flag)) return false;
-                ++pv_seen;
-            }
-            return true;
-        };
+        // P V of global tile k (and so every earlier one) has completed. The region's next completion
+        // would be P V of tile k + NR, which needs a P this thread has not released yet, so the parity
+        // wait cannot alias; P is therefore released without waiting for the previous P V.
+        auto pv_done = [&](int k) -> bool { return mbar_wait(&r_free[k % NR], (k / NR) & 1, abort_flag); };
         int g = 0;
         for (int round = 0; ok; ++round) {
             const Item it = item_of(round);
@@ -762,7 +755,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 const bool grow = mx > m_used + 8.0f;
                 const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
                 if (i > 0 && __any_sync(0xffffffffu, grow)) {
-                    const bool w = confirm_pv(gi);  // O must hold P V of the previous tile before it is scaled
+                    const bool w = pv_done(gi - 1);  // O must hold P V of the previous tile before it is scaled
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll 1
@@ -804,16 +797,10 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 }
                 tmem_st_wait();
                 l += rs2.x + rs2.y;
-                // observe the previous PV completion before releasing this P (keeps o_done parity waits
-                // unambiguous: never more than one phase ahead of this thread)
-                if (i > 0) {
-                    const bool w = confirm_pv(gi);
-                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-                }
                 tc_fence_before();
                 mbar_arrive(&p_full[r]);
             }
-            if (ok) ok = confirm_pv(g + nt);
+            if (ok) ok = pv_done(g + nt - 1);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             // O / l to the output, then hand the accumulator back to the MMA warp
