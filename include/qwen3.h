@@ -300,7 +300,10 @@ QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache,
  * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.
  * d_seq_meta, window and ring as for qwen3_op_attention_prefill (padding slots are skipped, a window
  * keeps the last `window` slots, a ring wraps; ring > 0 must be a multiple of 256). d_work is caller
- * scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring) bytes. */
+ * scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring) bytes. Caches
+ * [B, Hkv, cap, dh] bf16 with 16-byte aligned bases (they are read through TMA tensor maps; a base the
+ * map rejects returns QWEN3_E_CUDA). Scores and the weighted sum run on the tensor cores with fp32
+ * accumulation; the probabilities are rounded to bf16 for the weighted sum, as in the prefill. */
 QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
 QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                               int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
