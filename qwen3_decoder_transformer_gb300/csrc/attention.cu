@@ -448,22 +448,17 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
 
 // Persistent form of the one-head-per-CTA kernel: grid = min(work items, SMs). Work items are
 // (query tile, sequence, query head) triples, longest causal range first; CTA c takes items
-// c, 2G-1-c, 2G+c, ... (a snake over the sorted list, so every CTA gets a similar total). Warps:
-//   0      TMA: Q of each item, key tiles into a 3-stage ring (a stage is freed by its scores)
-//   6      TMA: value tiles into a 2-stage ring (a stage is freed by its P V)
-//   1      TMEM owner; lane 0 issues the score MMAs of tile g into region g % 3
-//   7      lane 0 issues O += P V of tile g (P from region g % 3, V from shared memory)
-//   2..5   softmax, thread = query row
-// Tensor memory holds three score regions and the output accumulator (4 x 128 columns), so the
-// scores run up to two tiles ahead of P V. A thread that issues tcgen05.mma waits while the pipe is
-// full, so one MMA thread for both kinds of batch kept the pipe in step with its own waits: with two
-// regions and one MMA thread, P of tile j+1 waited behind the scores of tile j+2 and the softmax warps
-// waited for their next scores, about 2,100 cycles per tile against 1,024 of MMA work (clock64
-// timeline of one CTA, 0.6B 1x2048). Completions are tracked per region (r_free), so the softmax
-// releases P without waiting for the previous P V. Tensor memory, barriers and the pipeline stay alive
-// across items; the output accumulator is handed back (o_free) before the next item's first P V
-// overwrites it. Tiles are counted across items (g), so ring stages, score regions and barrier phases
-// simply continue.
+// c, 2G-1-c, 2G+c, ... (a snake over the sorted list, so every CTA gets a similar total). Tensor
+// memory, barriers and the TMA/MMA pipeline stay alive across items: the next item's Q and first
+// scores load while the softmax warps finish the current item, whose output accumulator is then
+// handed back to the MMA warp (o_free) before the next item's first PV overwrites it. Tiles are
+// counted across items (g), so ring stages, score regions and barrier phases simply continue.
+// Tensor memory holds three score regions and the output accumulator (4 x 128 columns): the scores
+// run two tiles ahead of P V, so the scores a softmax pass needs are complete when it starts. With
+// two regions the MMA thread could issue S of tile j+2 only after P V of tile j; since a thread that
+// issues tcgen05.mma waits while the pipe is full, it then sat behind that S while P of tile j+1
+// was already waiting, and the softmax warps waited for their next scores: about 2,100 cycles per
+// tile against 1,024 of MMA work (clock64 timeline of one CTA, 0.6B 1x2048).
 constexpr int PS_THREADS = 64 + 128 + 64;  // + a TMA warp for the value tiles and a P V MMA warp
 constexpr int PS_KST = 3, PS_VST = 2;      // key and value ring stages
 template <int DH>
