@@ -1,9 +1,13 @@
-"""Benchmark: Qwen3-style decoder prefill throughput on one GB300 (per process), through the C ABI.
+"""Benchmark: Qwen3-style decoder prefill throughput and decode-step latency on one GB300 (per process),
+through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+The default workload is the largest single-GPU one: the Qwen3-8B shape, causal prefill of 1 x 32768
+tokens, then decode of 16 sequences at a 32,768-token pre-filled context (77 GB bf16 cache).
 A step is one causal prefill (embedding, all layers, final norm, LM head on each sequence's last row)
-of the workload's batch of synthetic token ids, on random-init bf16 weights of the named shape. With
+of the workload's batch of synthetic token ids, on random-init bf16 weights of the named shape, and its
+greedy token; the `decode` block times greedy decode steps (each step's argmax fed back). With
 N > 1 (torchrun, one process per GPU) every rank runs an independent replica ("replicas only": the
 forward pass has no exchange step); value = all ranks' tokens / the slowest rank's time.
 
@@ -31,7 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s and decode-step ms on 1 GB300; % of bf16-tensor / HBM roofline"
-DEFAULT_WORKLOAD = "0.6b-prefill-1x2048"
+DEFAULT_WORKLOAD = "8b-prefill-1x32768-decode-16@32768"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -182,39 +186,88 @@ def barrier(world: int):
 
 # ----------------------------------------------------------------------------- oracle baseline
 
+def cpu_description() -> dict:
+    """Host cores and CPU model of this machine (for the baseline's record)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k, _, v = ln.partition(":")
+                k = k.strip().lower()
+                if k in ("model name", "cpu model", "hardware") and v.strip():
+                    model = v.strip()
+                    break
+                if k == "cpu part" and model is None:
+                    model = "cpu part " + v.strip()
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine()}
+
+
 class OracleBench:
-    """The oracle (single-threaded C++, as it stands) on the workload's weights and token ids."""
+    """The oracle (single-threaded C++, as it stands) timed on a bounded sample of the workload: one
+    decoder layer (steps a2-a9) of the workload's shape over a prefix of `tokens` rows, extrapolated to
+    the workload's whole prefill step by the ratio of algorithmic FLOPs. A whole step is far beyond a
+    bounded run (the 8B 1x32768 prefill is 7.7e14 FLOPs; the oracle runs a few GFLOP/s)."""
 
     def __init__(self, cfg: dict, seed: int):
         import oracle as O
         from qwen3_decoder_transformer_gb300 import synth
+        self.O = O
         self.cfg = cfg
-        self.model = O.Model(cfg, synth.weights_to_numpy(synth.make_weights(cfg, seed)))
-        self.ids = synth.make_ids(cfg["vocab"], 1, 64, seed).numpy()
+        d = cfg["hidden"]
+        w = {"embed": None, "lm_head": None, "final_norm": synth._gain(d, synth._seed(seed, "final_norm"), "cpu")}
+        for name in synth.LAYER_NAMES:
+            w[name] = [None] * cfg["n_layers"]
+        for name, t in synth.make_layer(cfg, seed, 0).items():
+            w[name][0] = t
+        self.model = O.Model(cfg, synth.weights_to_numpy(w))
+        # layer-0 inputs: rows distributed as embedding rows (bf16 N(0, 0.02)), 1024 at most
+        self.x = synth.to_numpy_bits(synth._normal((1024, d), 0.02, synth._seed(seed, "bench_rows"), "cpu"))
 
     def run(self, tokens: int) -> float:
-        """Seconds for a full forward pass (all layers + LM head on the last row) of a `tokens` prefix."""
-        kc, vc = self.model.new_cache(1, tokens)
+        """Seconds for layer 0 (norm, Q/K/V + q/k-norm + RoPE, causal GQA attention, o_proj + residual,
+        norm, SwiGLU MLP, down + residual) over `tokens` rows at positions 0..tokens-1."""
+        c = self.cfg
+        tokens = min(tokens, self.x.shape[0])
+        x = self.x[:tokens]
+        pos = np.arange(tokens, dtype=np.int32)
+        kc = np.zeros((1, c["n_kv_heads"], tokens, c["head_dim"]), dtype=np.uint16)
+        vc = np.zeros_like(kc)
         t0 = time.perf_counter()
-        self.model.forward(kc, vc, self.ids[:, :tokens], 0)
+        q, k, v = self.model.layer_qkv(0, x, pos)
+        kc[0] = k.transpose(1, 0, 2)
+        vc[0] = v.transpose(1, 0, 2)
+        self.model.layer_out(0, x, q, pos, kc, vc, np.zeros(tokens, dtype=np.int32))
         return time.perf_counter() - t0
 
-    def describe(self, tokens: int) -> str:
-        return (f"oracle forward (single-threaded C++, fp64 accumulation, bf16 emulation) of all "
-                f"{self.cfg['n_layers']} layers + LM head on a {tokens}-token prefix of the workload's ids, "
-                f"batch 1; tokens/s = {tokens} / wall time (its attention work is that of the prefix, "
-                f"not of the full sequence)")
+    @staticmethod
+    def layer_flops(cfg: dict, tokens: int) -> float:
+        d, dh, F = cfg["hidden"], cfg["head_dim"], cfg["intermediate"]
+        hq, hkv = cfg["n_q_heads"], cfg["n_kv_heads"]
+        gemm = 2.0 * tokens * (d * (hq + 2 * hkv) * dh + hq * dh * d + 3 * d * F)
+        return gemm + 4.0 * hq * dh * tokens * (tokens + 1) / 2
 
+    def extrapolate(self, seconds: float, tokens: int, B: int, T: int) -> float:
+        """Workload tokens/s implied by `seconds` for one layer over `tokens` rows."""
+        step_s = seconds * step_flops(self.cfg, B, T) / self.layer_flops(self.cfg, tokens)
+        return B * T / step_s
 
-def flops_per_token(cfg: dict) -> float:
-    d, dh, F = cfg["hidden"], cfg["head_dim"], cfg["intermediate"]
-    per_layer = d * (cfg["n_q_heads"] + 2 * cfg["n_kv_heads"]) * dh + cfg["n_q_heads"] * dh * d + 3 * d * F
-    return 2.0 * cfg["n_layers"] * per_layer
+    def describe(self, tokens: int, B: int, T: int) -> str:
+        ratio = step_flops(self.cfg, B, T) / self.layer_flops(self.cfg, tokens)
+        return (f"extrapolated: oracle (single-threaded C++, fp64 accumulation, bf16 emulation) timed on one "
+                f"decoder layer of the workload's shape over a {tokens}-token prefix, scaled by the FLOP ratio "
+                f"{ratio:.4g} to the {B}x{T} prefill step ({self.cfg['n_layers']} layers, causal attention, "
+                f"LM head on the last rows); tokens/s = {B * T} / extrapolated step time")
 
 
 def sample_tokens(cfg: dict, budget_flops: float) -> int:
-    """Prefix length whose oracle pass costs about `budget_flops` (the oracle runs ~1-2 GFLOP/s)."""
-    return int(max(1, min(64, budget_flops / flops_per_token(cfg))))
+    """Prefix length whose one-layer oracle pass costs about `budget_flops` (the oracle runs a few
+    GFLOP/s on one core)."""
+    per_tok = OracleBench.layer_flops(cfg, 1)
+    return int(max(2, min(1024, budget_flops / per_tok)))
 
 
 # ----------------------------------------------------------------------------- arms
@@ -223,24 +276,25 @@ def run_reference(args, wl):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    from qwen3_decoder_transformer_gb300 import configs
     cfg = wl["model"]
     B, T = wl["prefill"]
     ob = OracleBench(cfg, wl["seed"])
-    # whole run about 2-3 minutes of single-core work: ~2.5e11 FLOPs shared by the timed steps
-    toks = sample_tokens(cfg, 2.5e11 / max(1, args.steps))
+    # whole run about 2-3 minutes of single-core work: ~2e11 FLOPs shared by the timed steps
+    toks = sample_tokens(cfg, 2e11 / max(1, args.steps))
     for _ in range(args.warmup):
-        ob.run(1)
+        ob.run(2)
     times = [ob.run(toks) for _ in range(args.steps)]
-    v = toks * len(times) / sum(times)
-    desc = ob.describe(toks)
+    sec = sum(times) / len(times)
+    v = ob.extrapolate(sec, toks, B, T)
+    desc = ob.describe(toks, B, T)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * B * T / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/bf16-storage",
             "data": "synthetic (random-init weights, uniform token ids)",
             "config": {"workload": args.workload, "batch": B, "seq_len": T,
-                       "sample": f"{toks}-token prefix per step"},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+                       "sample": f"one layer over a {toks}-token prefix per step, {1e3 * sec:.0f} ms each"},
+            "cpu_baseline": dict({"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+                                 **cpu_description()),
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -349,6 +403,15 @@ def run_ours(args, wl):
             "peak_source": f"{peak_src} ({'sustained' if (bound == 'tensor' and long_region) else 'burst'})",
             "algorithmic_per_launch": units, "avg_launch_ms": avg_ms}
     step_tf = step_flops(cfg, B, T)
+    # the tensor-core share of the step: GEMM + attention FLOPs over the time those kernels took
+    tensor_classes = [k for k, v in work.items() if v[0] == "tensor" and k in kt and kt[k][1]]
+    ga_flops = sum(work[k][1] * kt[k][1] for k in tensor_classes)
+    ga_ms = sum(kt[k][0] for k in tensor_classes)
+    ga_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    gemm_attn = {"tflops": ga_flops / (ga_ms / 1e3) / 1e12, "peak": ga_peak,
+                 "frac": ga_flops / (ga_ms / 1e3) / 1e12 / ga_peak, "ms_per_step": ga_ms / args.steps,
+                 "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
+                 "classes": tensor_classes}
     launches = m.launch_count(B, T) + 2  # + the length reset before each step and the greedy kernel
     if rank != 0:
         return
@@ -361,8 +424,11 @@ def run_ours(args, wl):
                              % (sum(t.numel() * 2 for k, t in _flat(w)) / 1e9)},
             "e2e": e2e, "gpu_launches": launches * args.steps,
             "roofline": roof,
-            "step_tflops": step_tf / 1e12, "step_frac_of_peak": step_tf / (elapsed_ms / args.steps / 1e3) / 1e12
-            / peaks["bf16_tflops"],
+            "step_tflops": step_tf / 1e12,
+            "step_frac_of_peak": {"burst": step_tf / (elapsed_ms / args.steps / 1e3) / 1e12 / peaks["bf16_tflops"],
+                                  "sustained": step_tf / (elapsed_ms / args.steps / 1e3) / 1e12
+                                  / peaks["bf16_tflops_sustained"]},
+            "gemm_attention_frac_of_peak": gemm_attn,
             "clocks": clk.summary(), "kernels": per_kernel,
             "kernels_note": "per-kernel times from a second run of the same steps with a CUDA event pair around "
                             "every launch (%.3f ms/step with events vs %.3f without)"
@@ -376,10 +442,11 @@ def run_ours(args, wl):
         line["decode"]["step_hbm_frac"] = line["decode"]["step_hbm_gbs"] / peaks_hbm
     if world == 1 and not args.no_cpu_baseline:
         ob = OracleBench(cfg, wl["seed"])
-        toks = sample_tokens(cfg, 1.5e10)
+        toks = sample_tokens(cfg, 2.5e10)
         dt = ob.run(toks)
-        line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": ob.describe(toks), "seconds": dt}
+        line["cpu_baseline"] = dict({"value": ob.extrapolate(dt, toks, B, T), "unit": "tokens/s", "cores": 1,
+                                     "kind": "oracle", "sample": ob.describe(toks, B, T), "seconds": dt},
+                                    **cpu_description())
     print(json.dumps(line), flush=True)
     m.close()
 

@@ -118,10 +118,13 @@ QWEN3_API int qwen3_init(const qwen3_config* cfg, const qwen3_weights* w, int ma
 QWEN3_API int qwen3_prefill(qwen3_ctx* ctx, const int32_t* d_ids, int B, int T, float* d_logits, int flags,
                   void* stream);
 
-/* One greedy-decode forward step: one token per sequence at position = length, appended to the
- * cache; length += 1. d_ids: [B] int32; d_logits: fp32 [B, V]. The step is replayed from a CUDA
- * graph that the context captures on first use for each (B, d_ids, d_logits); kernels read the
- * length from device memory, so replays advance correctly. Errors as qwen3_prefill. */
+/* One greedy-decode forward step ("A modern architecture: Qwen3", The whole model: the generation loop
+ * feeds the argmax token back with positions = cache.length; "Transformer architectures: modern",
+ * generation): one token per sequence at position = length, appended to the cache; length += 1.
+ * d_ids: [B] int32 (B must equal the batch already in the cache); d_logits: fp32 [B, V]. The step is
+ * replayed from a CUDA graph that the context captures on first use for each (B, d_ids, d_logits,
+ * number of 512- or 1024-slot context chunks holding keys); kernels read the length from device memory,
+ * so replays advance correctly. Errors as qwen3_prefill. */
 QWEN3_API int qwen3_decode_step(qwen3_ctx* ctx, const int32_t* d_ids, int B, float* d_logits, void* stream);
 
 /* End-to-end variant of qwen3_prefill on HOST buffers: copies h_ids to the device, runs the
@@ -166,12 +169,16 @@ QWEN3_API int qwen3_generate(qwen3_ctx* ctx, const int32_t* d_ids, const int32_t
 /* Current cache length (tokens per sequence) and batch held in the cache. */
 QWEN3_API int qwen3_length(const qwen3_ctx* ctx, int* length, int* batch);
 
-/* Set the cache length and batch, e.g. after filling the cache through qwen3_kv_view. Enqueues a
- * device update on `stream`. The cache then holds plain equal-length sequences: any padding layout
- * or shared prefix is cleared. Errors: E_ARG, E_OVERFLOW (length > capacity), E_BATCH. */
+/* Set the cache length and batch ("A modern architecture: Qwen3", The whole model: the preallocated
+ * KVCache and its `length`, which positions continue from), e.g. after filling the cache through
+ * qwen3_kv_view. Enqueues a device update on `stream`. The cache then holds plain equal-length
+ * sequences: any padding layout or shared prefix is cleared. Errors: E_ARG, E_OVERFLOW (length >
+ * capacity), E_BATCH. */
 QWEN3_API int qwen3_set_length(qwen3_ctx* ctx, int length, int batch, void* stream);
 
-/* Device pointers to layer `layer`'s K and V cache, each [max_batch][Hkv][slots][dh] bf16,
+/* The preallocated KV cache ("A modern architecture: Qwen3", The whole model: new_cache allocates
+ * K and V per layer as [batch, kv heads, capacity, head_dim]; keys are cached already rotated, Attention
+ * with grouped KV heads). Device pointers to layer `layer`'s K and V cache, each [max_batch][Hkv][slots][dh] bf16,
  * dims[0..3] = {max_batch, Hkv, slots, dh}; slots = capacity, or the ring size of a rolling buffer.
  * The memory stays owned by the context. */
 QWEN3_API int qwen3_kv_view(qwen3_ctx* ctx, int layer, void** d_k, void** d_v, int64_t dims[4]);
@@ -182,7 +189,10 @@ QWEN3_API int qwen3_kv_view(qwen3_ctx* ctx, int layer, void** d_k, void** d_v, i
 QWEN3_API int qwen3_set_tap(qwen3_ctx* ctx, int layer, void* d_layer_in, void* d_layer_out);
 
 /* Synchronise `stream`, then read and clear the device error flags: returns QWEN3_OK,
- * QWEN3_E_TOKEN or QWEN3_E_TIMEOUT (or E_CUDA if the synchronisation failed). */
+ * QWEN3_E_TOKEN or QWEN3_E_TIMEOUT (or E_CUDA if the synchronisation failed). The pages' forward pass
+ * raises on invalid input ("A modern architecture: Qwen3", The whole model: the context-limit check);
+ * a kernel cannot raise, so a token id outside [0, vocab) zeroes its embedding row and sets a flag that
+ * this call reports. */
 QWEN3_API int qwen3_get_error(qwen3_ctx* ctx, void* stream);
 
 /* Per-kernel timing: while enabled, every kernel launch of a call is bracketed by CUDA events on
@@ -197,7 +207,13 @@ QWEN3_API const char* qwen3_kernel_class_name(int i);
 /* Number of kernel launches a prefill of B x T or a decode step of B makes (for launch accounting). */
 QWEN3_API int qwen3_launch_count(const qwen3_ctx* ctx, int B, int T, int flags, int decode);
 
+/* Name of an error code (the pages' errors: head divisibility and odd rotary dimension, Attention with
+ * grouped KV heads and Rotary position embeddings sections; capacity and context overflow, The whole
+ * model). Returns a static string; never NULL. */
 QWEN3_API const char* qwen3_strerror(int code);
+/* Release a context and everything it owns (the cache the pages' new_cache allocates, scratch, packed
+ * weights, captured graphs). Synchronises the device first. The borrowed weights are not touched.
+ * NULL is ignored. */
 QWEN3_API void qwen3_free(qwen3_ctx* ctx);
 
 /* ------------------------------------------------------------------------------------------------
@@ -296,18 +312,21 @@ QWEN3_API int qwen3_op_attention_prefill(const void* d_q, const void* d_k_cache,
                                int window, int ring, int heads_per_cta, int kv_split, int kv_chunks, void* d_work,
                                void* d_out, int* d_err, void* stream);
 
-/* Decode attention: one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, split over
- * the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out [B, Hq*dh] bf16.
- * d_seq_meta, window and ring as for qwen3_op_attention_prefill (padding slots are skipped, a window
- * keeps the last `window` slots, a ring wraps; ring > 0 must be a multiple of 256). d_work is caller
- * scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring) bytes. Caches
- * [B, Hkv, cap, dh] bf16 with 16-byte aligned bases (they are read through TMA tensor maps; a base the
- * map rejects returns QWEN3_E_CUDA). Scores and the weighted sum run on the tensor cores with fp32
- * accumulation; the probabilities are rounded to bf16 for the weighted sum, as in the prefill. */
+/* Decode attention ("A modern architecture: Qwen3", Attention with grouped KV heads; the decode loop of
+ * The whole model): one query per (b, h) against cache slots 0..n-1, n = *d_len0 + 1, kv head
+ * h / (Hq/Hkv), split over the context in chunks and merged by log-sum-exp. q [B, Hq, dh]; out
+ * [B, Hq*dh] bf16. d_seq_meta, window and ring as for qwen3_op_attention_prefill (padding slots are
+ * skipped, a window keeps the last `window` slots, a ring wraps; ring > 0 must be a multiple of 256).
+ * d_work is caller scratch of qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring) bytes; its
+ * contents on entry do not matter (a call writes every record it reads back and reads only those).
+ * Caches [B, Hkv, cap, dh] bf16 with 16-byte aligned bases (they are read through TMA tensor maps; a
+ * base the map rejects returns QWEN3_E_CUDA). Scores and the weighted sum run on the tensor cores with
+ * fp32 accumulation; the probabilities are rounded to bf16 for the weighted sum, as in the prefill.
+ * d_err (device int, may be NULL) receives bit 2 if a bounded wait gave up; the output is then invalid. */
 QWEN3_API size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
 QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                               int Hq, int Hkv, int dh, int cap, const int* d_len0, const int* d_seq_meta,
-                              int window, int ring, void* d_work, void* d_out, void* stream);
+                              int window, int ring, void* d_work, void* d_out, int* d_err, void* stream);
 
 /* Greedy next token ("A modern architecture: Qwen3", generation): next[b] = the index of the largest
  * of the V fp32 logits in row b (row stride ld floats; the lowest index on ties, a NaN counting as the
@@ -321,19 +340,24 @@ QWEN3_API int qwen3_op_greedy(const float* d_logits, int64_t ld, int B, int V, i
  * code whose device memory belongs to another allocator (for example a framework's caching pool),
  * code that must not trigger the device-wide synchronisation an allocation can cause, and code that
  * may not allocate once it has started. Same arguments and result as qwen3_op_attention_decode,
- * minus the workspace and the sequence layout (plain causal sequences only): the split partials go to a fixed array compiled into this library,
- * QWEN3_DECODE_NOALLOC_MAX_BYTES (16 MiB) large, which every GPU that loads the library holds until
- * the process exits. A call whose workspace (qwen3_attention_decode_workspace) is larger returns
- * QWEN3_E_ARG and launches nothing. The call allocates nothing itself. Its first call on each device
- * looks up the array's device address with that device current; make that first call before any
- * stream capture. All calls on a device share the one array and it keeps the last call's contents:
- * calls that overlap on the GPU (other streams, concurrent graph launches) race and corrupt each
- * other's results, so serialise them. No part of the array has to start at zero: each call writes
- * every partial it reads back. The pages have no counterpart to this entry point. */
+ * minus the workspace and the sequence layout (plain causal sequences only): the split partials go to a
+ * fixed array compiled into this library, QWEN3_DECODE_NOALLOC_MAX_BYTES (16 MiB) large, which every GPU
+ * that loads the library holds until the process exits. A call whose workspace
+ * (qwen3_attention_decode_workspace(B, Hq, dh, cap, 0, 0)) is larger returns QWEN3_E_ARG and launches
+ * nothing. The call allocates nothing itself. Its first call on each device looks up the array's device
+ * address with that device current and keeps it for the life of the process; make that first call
+ * before any stream capture, and do not call it again on a device after that device was reset
+ * (cudaDeviceReset), since the kept address then no longer names the array. All calls on a device share
+ * the one array and it keeps the last call's contents: calls that overlap on the GPU (other streams,
+ * concurrent graph launches) race and corrupt each other's results, so serialise them. The array needs
+ * no clearing: a call reads back only the partials it wrote itself (the merge skips the records of
+ * chunks past the current length and the output floats of records with no visible key), so what a
+ * previous call left there, even NaN or infinity, cannot reach the output.
+ * d_err as for qwen3_op_attention_decode. The pages have no counterpart to this entry point. */
 #define QWEN3_DECODE_NOALLOC_MAX_BYTES (16u << 20)
 QWEN3_API int qwen3_op_attention_decode_noalloc(const void* d_q, const void* d_k_cache, const void* d_v_cache, int B,
                                                 int Hq, int Hkv, int dh, int cap, const int* d_len0, void* d_out,
-                                                void* stream);
+                                                int* d_err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -97,7 +97,8 @@ def lib() -> ctypes.CDLL:
     L.qwen3_attention_prefill_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_attention_decode_workspace.restype = sz
     L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i, i, i]
-    L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, i, i, _vp, _vp, _vp]
+    L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, i, i, _vp, _vp, _vp, _vp]
+    L.qwen3_op_attention_decode_noalloc.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp, _vp]
     L.qwen3_op_greedy.argtypes = [_vp, ctypes.c_int64, i, i, i, _vp, _vp, _vp]
     L.qwen3_prefill_padded.argtypes = [_vp, _vp, _i32p, i, i, _vp, i, _vp]
     L.qwen3_share_prefix.argtypes = [_vp, i, _vp]
@@ -330,11 +331,12 @@ def attention_decode_workspace(B, Hq, dh, cap, window=0, ring=0) -> int:
     return lib().qwen3_attention_decode_workspace(B, Hq, dh, cap, window, ring)
 
 
-def op_attention_decode(q, k_cache, v_cache, len0, work, out, seq_meta=None, window=0, ring=0, stream=None):
+def op_attention_decode(q, k_cache, v_cache, len0, work, out, seq_meta=None, window=0, ring=0, err=None,
+                        stream=None):
     B, Hq, dh = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
     check(lib().qwen3_op_attention_decode(_p(q), _p(k_cache), _p(v_cache), B, Hq, Hkv, dh, cap, _p(len0),
-                                          _p(seq_meta), window, ring, _p(work), _p(out), _stream(stream)))
+                                          _p(seq_meta), window, ring, _p(work), _p(out), _p(err), _stream(stream)))
 
 
 def op_greedy(logits, next_ids, stop_id=-1, done=None, stream=None):

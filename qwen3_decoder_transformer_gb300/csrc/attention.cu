@@ -936,7 +936,8 @@ __global__ void __launch_bounds__(DEC_THREADS)
         psh = meta[1];
         pe = ps + meta[kSeqMetaHead + b];
     }
-    if (s0 >= n || (s0 >= ps && s1 <= pe)) {  // nothing to read, or only padding
+    if (s0 >= n) return;  // past the length: the merge does not read this chunk's records
+    if (s0 >= ps && s1 <= pe) {  // only padding: a record of weight 0 (its output floats are not read)
         if (threadIdx.x < G) {
             wb[(size_t)threadIdx.x * nsplit * REC + 0] = -INFINITY;
             wb[(size_t)threadIdx.x * nsplit * REC + 1] = 0.f;
@@ -1128,12 +1129,17 @@ __global__ void __launch_bounds__(DEC_THREADS)
 }
 
 // Merge the chunks of one (b, q-head) by log-sum-exp: O = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// Only chunks that can hold keys of this call are read (chunks [lo / CH, (n - 1) / CH] of the
+// current length n, at most nsplit): the split kernel writes nothing for the others, so their records
+// may hold anything, including a previous call's partials. A record with m = -inf (a chunk of padding
+// only) has weight 0 and its output floats are never read: the split kernel writes only m and l there.
 // The chunk weights are computed once into shared memory; each thread then sums its output element
 // over the chunks with four independent chains (four record loads in flight).
 constexpr int COMB_MAX_SPLITS = 1024;
 template <int DH>
 __global__ void __launch_bounds__(DH)
-    attn_decode_combine_kernel(const float* __restrict__ work, int Hq, int nsplit, __nv_bfloat16* __restrict__ out) {
+    attn_decode_combine_kernel(const float* __restrict__ work, int Hq, int nsplit, const int* __restrict__ len0p,
+                               int window, int ch, __nv_bfloat16* __restrict__ out) {
     constexpr int REC = DH + 2;
     __shared__ float wgt[COMB_MAX_SPLITS];
     __shared__ float red[DH / 32];
@@ -1142,8 +1148,11 @@ __global__ void __launch_bounds__(DH)
     pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const float* wb = work + ((size_t)b * Hq + h) * nsplit * REC;
+    const int n = *len0p + 1;
+    const int lo = window > 0 ? max(0, n - window) : 0;
+    const int used = min(nsplit, (n - 1) / ch - lo / ch + 1);
     float M = -INFINITY;
-    for (int c = d; c < nsplit; c += DH) {
+    for (int c = d; c < used; c += DH) {
         const float mi = wb[(size_t)c * REC];
         wgt[c] = mi;
         M = fmaxf(M, mi);
@@ -1156,11 +1165,11 @@ __global__ void __launch_bounds__(DH)
 #pragma unroll
     for (int w = 1; w < DH / 32; ++w) M = fmaxf(M, red[w]);
     float L = 0.f;
-    for (int c = d; c < nsplit; c += DH) {
+    for (int c = d; c < used; c += DH) {
         const float mi = wgt[c];
         const float f = mi == -INFINITY ? 0.f : exp2f(mi - M);
         wgt[c] = f;
-        L = fmaf(wb[(size_t)c * REC + 1], f, L);
+        if (f != 0.f) L = fmaf(wb[(size_t)c * REC + 1], f, L);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -1175,15 +1184,17 @@ __global__ void __launch_bounds__(DH)
     }
     __syncthreads();
     const float* rd = wb + 2 + d;
+    // a weight of 0 adds nothing; skipping it keeps unwritten output floats (NaN, inf) out of the sum
+    auto term = [&](int c, float a) { return wgt[c] != 0.f ? fmaf(rd[(size_t)c * REC], wgt[c], a) : a; };
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     int c = 0;
-    for (; c + 4 <= nsplit; c += 4) {
-        a0 = fmaf(rd[(size_t)c * REC], wgt[c], a0);
-        a1 = fmaf(rd[(size_t)(c + 1) * REC], wgt[c + 1], a1);
-        a2 = fmaf(rd[(size_t)(c + 2) * REC], wgt[c + 2], a2);
-        a3 = fmaf(rd[(size_t)(c + 3) * REC], wgt[c + 3], a3);
+    for (; c + 4 <= used; c += 4) {
+        a0 = term(c, a0);
+        a1 = term(c + 1, a1);
+        a2 = term(c + 2, a2);
+        a3 = term(c + 3, a3);
     }
-    for (; c < nsplit; ++c) a0 = fmaf(rd[(size_t)c * REC], wgt[c], a0);
+    for (; c < used; ++c) a0 = term(c, a0);
     out[((size_t)b * Hq + h) * DH + d] = __float2bfloat16_rn(((a0 + a1) + (a2 + a3)) * inv_l);
 }
 
@@ -1195,6 +1206,12 @@ int decode_nsplit(int cap, int window, int ring) {
     const int ch = decode_chunk(cap, ring);
     const int all = (cap + ch - 1) / ch;
     return window > 0 ? std::min(all, (window + ch - 1) / ch + 1) : all;
+}
+// Chunks that hold keys when the cache has n keys per sequence (slots [lo, n), chunks aligned to CH).
+int decode_nsplit_for(int n, int cap, int window, int ring) {
+    const int ch = decode_chunk(cap, ring);
+    const int lo = window > 0 ? std::max(0, n - window) : 0;
+    return std::max(1, std::min(decode_nsplit(cap, window, ring), (n - 1) / ch - lo / ch + 1));
 }
 
 template <int DH, int G, int CH>
@@ -1208,8 +1225,8 @@ cudaError_t decode_launch_ch(dim3 grid, const CUtensorMap& tk, const CUtensorMap
 template <int DH, int G>
 cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                             int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out, int* err,
-                            cudaStream_t st) {
-    const int nsplit = decode_nsplit(cap, sm.window, sm.ring);
+                            int n_keys, cudaStream_t st) {
+    const int nsplit = n_keys > 0 ? decode_nsplit_for(n_keys, cap, sm.window, sm.ring) : decode_nsplit(cap, sm.window, sm.ring);
     if (nsplit > COMB_MAX_SPLITS) return cudaErrorInvalidValue;
     const dim3 grid(nsplit, Hkv, B);
     CUtensorMap tk, tv;
@@ -1227,18 +1244,19 @@ cudaError_t decode_launch_t(const __nv_bfloat16* q, const __nv_bfloat16* kc, con
             e = decode_launch_ch<DH, G, DEC_CHUNK>(grid, tk, tv, q, Hq, Hkv, len0, sm, work, err, st);
     }
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, out);
+    return launch_pdl(attn_decode_combine_kernel<DH>, dim3(Hq, B), dim3(DH), 0, st, work, Hq, nsplit, len0, sm.window,
+                      decode_chunk(cap, sm.ring), out);
 }
 
 template <int DH>
 cudaError_t decode_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                              int Hkv, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out, int* err,
-                             cudaStream_t st) {
+                             int n_keys, cudaStream_t st) {
     switch (Hq / Hkv) {
-        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
-        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
-        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
-        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+        case 1: return decode_launch_t<DH, 1>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
+        case 2: return decode_launch_t<DH, 2>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
+        case 4: return decode_launch_t<DH, 4>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
+        case 8: return decode_launch_t<DH, 8>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -1341,12 +1359,16 @@ size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int rin
 
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
-                               int* err, cudaStream_t st) {
+                               int* err, int n_keys, cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
     if (sm.ring && (sm.ring % DEC_CHUNK_RING || sm.ring != cap)) return cudaErrorInvalidValue;
-    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
-    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, st);
+    if (dh == 128) return decode_launch_dh<128>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
+    if (dh == 64) return decode_launch_dh<64>(q, kc, vc, B, Hq, Hkv, cap, len0, sm, work, out, err, n_keys, st);
     return cudaErrorInvalidValue;
+}
+
+int attn_decode_chunks(int n_keys, int cap, int window, int ring) {
+    return n_keys > 0 ? decode_nsplit_for(n_keys, cap, window, ring) : decode_nsplit(cap, window, ring);
 }
 
 int attn_decode_kernel_count() { return 2; }

@@ -185,11 +185,15 @@ int attn_heads_per_cta(int Hq, int Hkv);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);
 size_t attn_decode_workspace(int B, int Hq, int dh, int cap, int window, int ring);
-// work: attn_decode_workspace() bytes of chunk records, merged by a second kernel.
+// work: attn_decode_workspace() bytes of chunk records, merged by a second kernel; only the records of
+// chunks holding keys of this call are written and read, so the workspace needs no clearing.
 // err (may be null): ERR_TIMEOUT is or-ed in when a copy-ring wait gives up.
+// n_keys > 0: the key count *len0 + 1 the launch will see (known on the host), which bounds the grid to
+// the chunks holding keys (attn_decode_chunks of it); 0: the grid covers the whole capacity.
 cudaError_t attn_decode_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int Hq,
                                int Hkv, int dh, int cap, const int* len0, SeqMap sm, float* work, __nv_bfloat16* out,
-                               int* err, cudaStream_t st);
+                               int* err, int n_keys, cudaStream_t st);
+int attn_decode_chunks(int n_keys, int cap, int window, int ring);
 int attn_decode_kernel_count();
 // Allocation-free decode attention: size of the library's fixed scratch, and its device address on
 // the current device (looked up on first use per device).

@@ -49,8 +49,10 @@ struct TimedLaunch {
 };
 
 // A captured forward pass. Everything the host decides for a call is in the key: the shape, the
-// flags, the device buffers baked into the launches, and (prefill) the cache length, which picks the
-// attention split; the cache length itself, the sequence layout and the weights are read on the device.
+// flags, the device buffers baked into the launches, and the cache length's effect on the grids (prefill:
+// the length, which picks the attention split; decode: the number of context chunks holding keys, which
+// sizes the decode-attention grid, so a decode graph is reused until the length crosses a chunk boundary);
+// the cache length itself, the sequence layout and the weights are read on the device.
 struct ForwardGraph {
     int B, T, flags, decode, len;
     const int32_t* ids;
@@ -235,7 +237,7 @@ int enqueue_decode_skinny(qwen3_ctx* c, const int32_t* ids, int B, float* logits
         }));
         TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
             return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                      c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, st);
+                                      c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, c->len + 1, st);
         }));
         TRY(skinny(c, K_GEMM_O, c->tB_o[l], c->tX_attn, B, d, c->q_width, nullptr, s_o, st));
         TRY(timed(c, K_FINALIZE, 1, st, [&] {
@@ -298,7 +300,8 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
         if (decode) {
             TRY(timed(c, K_ATTN_DECODE, attn_decode_kernel_count(), st, [&] {
                 return attn_decode_launch(c->q, layer_k(c, l), layer_v(c, l), B, g.n_q_heads, g.n_kv_heads, dh,
-                                          c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, st);
+                                          c->slots, c->d_len, seq_map(c), c->dec_work, c->attn, c->d_err, c->len + 1,
+                                          st);
             }));
         } else {
             int split = 0, chunks = 1;
@@ -362,7 +365,7 @@ int run_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logits, i
     // the caller's own capture records the launches themselves
     if (c->timing || c->tap_layer >= 0 || cs != cudaStreamCaptureStatusNone)
         return enqueue_forward(c, ids, B, T, logits, flags, decode, st);
-    const int len = decode ? -1 : c->len;
+    const int len = decode ? -attn_decode_chunks(c->len + 1, c->slots, c->window, c->ring) : c->len;
     ForwardGraph* gph = nullptr;
     for (auto& x : c->graphs)
         if (x.B == B && x.T == T && x.flags == flags && x.decode == (int)decode && x.len == len && x.ids == ids &&
@@ -1020,7 +1023,7 @@ size_t qwen3_attention_decode_workspace(int B, int Hq, int dh, int cap, int wind
 
 int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh, int cap,
                               const int* len0, const int* seq_meta, int window, int ring, void* work, void* out,
-                              void* stream) {
+                              int* err, void* stream) {
     if (!q || !kc || !vc || !len0 || !work || !out || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (dh != 64 && dh != 128) || cap < 1)
         return QWEN3_E_ARG;
@@ -1030,14 +1033,13 @@ int qwen3_op_attention_decode(const void* q, const void* kc, const void* vc, int
     if (prepare_kernels() != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
                               Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<float*>(work),
-                              static_cast<bf16*>(out), nullptr,
-                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+                              static_cast<bf16*>(out), err, 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;
 }
 
 int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void* vc, int B, int Hq, int Hkv, int dh,
-                                      int cap, const int* len0, void* out, void* stream) {
+                                      int cap, const int* len0, void* out, int* err, void* stream) {
     if (!q || !kc || !vc || !len0 || !out || B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || (dh != 64 && dh != 128) ||
         cap < 1)
         return QWEN3_E_ARG;
@@ -1048,7 +1050,7 @@ int qwen3_op_attention_decode_noalloc(const void* q, const void* kc, const void*
     float* scratch = nullptr;
     if (attn_decode_noalloc_scratch(&scratch) != cudaSuccess) return QWEN3_E_CUDA;
     return attn_decode_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), B,
-                              Hq, Hkv, dh, cap, len0, SeqMap{}, scratch, static_cast<bf16*>(out), nullptr,
+                              Hq, Hkv, dh, cap, len0, SeqMap{}, scratch, static_cast<bf16*>(out), err, 0,
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

@@ -87,4 +87,4 @@ def test_decode_noalloc_refuses_large_workspace(L):
     assert binding.attention_decode_workspace(64, 32, 128, 32832, 0, 0) > (16 << 20)
     dummy = ctypes.c_void_p(16)  # never dereferenced: the size check comes first
     len0 = ctypes.cast(ctypes.c_void_p(16), ctypes.POINTER(ctypes.c_int))
-    assert L.qwen3_op_attention_decode_noalloc(dummy, dummy, dummy, 64, 32, 8, 128, 32832, len0, dummy, None) == 5
+    assert L.qwen3_op_attention_decode_noalloc(dummy, dummy, dummy, 64, 32, 8, 128, 32832, len0, dummy, None, None) == 5

@@ -185,3 +185,54 @@ def test_tiny_graph_replay_matches_eager(bd, tiny):
         assert torch.equal(run(True, lambda: m.prefill(part, logits)), outs[t])
     assert m.get_error() == 0
     m.close()
+
+
+def test_tiny_decode_roomy_capacity_across_chunks(bd, tiny):
+    """Decode with a capacity far above the length (4096 slots for about 512 tokens): the decode-attention
+    grid covers only the 512-slot context chunks that hold keys, and the captured decode graph is swapped
+    when the length crosses a chunk boundary (slot 511 -> 512 during these steps). Cache slots past the
+    length hold NaN, which must never be read. Teacher-forced against the oracle, and the graph replays
+    equal the eager steps bit for bit."""
+    cfg, w, om = tiny
+    V = cfg["vocab"]
+    T, steps, cap = 508, 8, 4096
+    ids = synth.make_ids(V, 1, T, 12)
+    kc_o, vc_o = om.new_cache(1, cap)
+    ref = om.forward(kc_o, vc_o, ids.numpy(), 0)
+    toks = [int(ref[-1].argmax())]
+    refs = []
+    for s in range(steps):
+        r = om.forward(kc_o, vc_o, np.array([[toks[-1]]], dtype=np.int32), T + s)
+        refs.append(r)
+        toks.append(int(r.argmax()))
+
+    m = bd.Model(cfg, w, max_batch=1, capacity=cap, max_tokens=T)
+    logits = torch.empty(1, V, dtype=torch.float32, device="cuda")
+    ids_dev = torch.empty(1, dtype=torch.int32, device="cuda")
+
+    def run(eager):
+        m.set_timing(eager)
+        m.set_length(0, 0)
+        for layer in range(cfg["n_layers"]):  # stale slots past the length: NaN
+            k, v = m.kv_view(layer)
+            k.view(torch.int16).fill_(0x7FC0)
+            v.view(torch.int16).fill_(0x7FC0)
+        m.prefill(ids.cuda(), logits)
+        out = []
+        for s in range(steps):
+            ids_dev.fill_(toks[s])
+            m.decode_step(ids_dev, logits)
+            out.append(logits.clone())
+        torch.cuda.synchronize()
+        m.set_timing(False)
+        return out
+
+    graph = run(False)
+    eager = run(True)
+    assert m.get_error() == 0
+    for s in range(steps):
+        assert torch.equal(graph[s], eager[s]), s
+        g = graph[s].cpu().numpy()
+        assert np.isfinite(g).all(), s
+        assert rel_l2(g, refs[s]) <= 2e-2, (s, rel_l2(g, refs[s]))
+    m.close()

@@ -19,6 +19,16 @@ def rel_l2(got, ref) -> float:
     return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
 
 
+def max_rel_rows(got, ref, width: int) -> float:
+    """Largest relative L2 error over consecutive groups of `width` values (e.g. one (row, head) output
+    vector of head_dim values each), so that a single wrong row or head cannot hide in an aggregate."""
+    g = np.asarray(got, dtype=np.float64).reshape(-1, width)
+    r = np.asarray(ref, dtype=np.float64).reshape(-1, width)
+    den = np.linalg.norm(r, axis=1)
+    num = np.linalg.norm(g - r, axis=1)
+    return float(np.max(num / np.where(den > 0, den, 1.0)))
+
+
 def dev(u16: np.ndarray) -> torch.Tensor:
     """Host bf16 bit patterns -> CUDA bf16 tensor."""
     return synth.from_numpy_bits(u16, "cuda")
