@@ -571,6 +571,50 @@ def run_op(args, wl):
         y = torch.empty_like(x)
         fn = lambda: binding.op_rmsnorm(x, gm, 1e-6, y)
         work, unit, bound = 2.0 * Mx * d * 2, "GB/s", "hbm"
+    elif args.op == "embed":
+        Mx = args.rows or M
+        E = rnd(V, d)
+        ids = torch.randint(0, V, (Mx,), generator=g, device="cuda", dtype=torch.int64).to(torch.int32)
+        out = torch.empty(Mx, d, dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fn = lambda: binding.op_embed(E, ids, out, err)
+        work, unit, bound = 2.0 * Mx * d * 2, "GB/s", "hbm"
+    elif args.op == "greedy":
+        Bx = args.rows or wl["decode_batch"] or B
+        logits = torch.randn(Bx, V, generator=g, device="cuda")
+        nxt = torch.empty(Bx, dtype=torch.int32, device="cuda")
+        fn = lambda: binding.op_greedy(logits, nxt)
+        work, unit, bound = 4.0 * Bx * V, "GB/s", "hbm"
+    elif args.op == "gemm_o_norm":  # o_proj (or down_proj with --rows) + residual fused with the next RMSNorm
+        Mx = args.rows or M
+        K = hq * dh
+        act, wt, gm = rnd(Mx, K), rnd(d, K), rnd(d)
+        x, y = rnd(Mx, d), torch.empty(Mx, d, dtype=torch.bfloat16, device="cuda")
+        part = torch.zeros(binding.gemm_norm_part_floats(Mx), dtype=torch.float32, device="cuda")
+        fn = lambda: binding.op_gemm_residual_norm(act, wt, x, gm, 1e-6, y, part)
+        work, unit, bound = 2.0 * Mx * d * K, "TFLOP/s", "tensor"
+    elif args.op == "decode_step":  # whole greedy decode steps (graph replay) at the workload's context
+        cfgd = dict(cfg, n_layers=args.layers) if args.layers else cfg
+        Bd = args.rows or wl["decode_batch"] or 1
+        ctx = args.len0 or wl["prefilled_ctx"] or 1024
+        from qwen3_decoder_transformer_gb300 import synth
+        w = synth.make_weights(cfgd, wl["seed"], device="cuda")
+        m = binding.Model(cfgd, w, max_batch=Bd, capacity=ctx + args.steps + args.warmup + 8, max_tokens=max(Bd, 128))
+        Hkv_, dh_ = cfgd["n_kv_heads"], cfgd["head_dim"]
+        for layer in range(cfgd["n_layers"]):
+            k, v = m.kv_view(layer)
+            k[:, :, :ctx].copy_(synth.make_kv_normal((Bd, Hkv_, ctx, dh_), wl["seed"], layer, "k", device="cuda"))
+            v[:, :, :ctx].copy_(synth.make_kv_normal((Bd, Hkv_, ctx, dh_), wl["seed"], layer, "v", device="cuda"))
+        m.set_length(ctx, Bd)
+        ids = synth.make_ids(V, Bd, 1, wl["seed"] + 100, device="cuda").reshape(Bd)
+        logits = torch.empty(Bd, V, dtype=torch.float32, device="cuda")
+
+        def fn():
+            m.decode_step(ids, logits)
+            binding.op_greedy(logits, ids)
+        wbytes = float(sum(t.numel() * 2 for _, t in _flat(w)))
+        kvb = 2.0 * cfgd["n_layers"] * Bd * Hkv_ * dh_ * 2 * ctx
+        work, unit, bound = wbytes + kvb, "GB/s", "hbm"
     else:
         raise SystemExit(f"unknown op {args.op}")
     for _ in range(args.warmup):
@@ -808,7 +852,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=128, help="cap on timed decode steps")
     ap.add_argument("--op", default=None, help="time one kernel alone: attn_prefill, attn_decode, gemm_gateup, "
-                                                "gemm_qkv, gemm_o, gemm_down, qknorm_rope, rmsnorm")
+                                                "gemm_qkv, gemm_o, gemm_down, gemm_o_norm, qknorm_rope, rmsnorm, "
+                                                "embed, greedy; or decode_step (whole decode steps)")
     ap.add_argument("--feature", default=None, choices=["padded", "prefix", "window"],
                     help="time a generation feature on its own workload instead of the step")
     ap.add_argument("--kv-split", type=int, default=0, help="--op attn_prefill: minimum tiles per KV chunk")
@@ -816,7 +861,10 @@ def main():
     ap.add_argument("--heads", type=int, default=0, help="--op attn_prefill: query heads per CTA (0 = automatic)")
     ap.add_argument("--len0", type=int, default=0, help="--op attn_prefill: cached tokens before the chunk")
     ap.add_argument("--rows", type=int, default=0,
-                    help="row count for --op gemm_*/rmsnorm (default B*T), batch for --op attn_decode")
+                    help="row count for --op gemm_*/rmsnorm/embed (default B*T), batch for --op attn_decode, "
+                         "greedy and decode_step")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="--op decode_step: build only this many layers (small device footprint for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

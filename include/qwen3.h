@@ -332,9 +332,13 @@ QWEN3_API int qwen3_op_attention_decode(const void* d_q, const void* d_k_cache, 
  * of the V fp32 logits in row b (row stride ld floats; the lowest index on ties, a NaN counting as the
  * largest, as torch.argmax). With stop_id >= 0 and d_done (int [B], device): a row with done[b] != 0
  * emits stop_id, and done[b] becomes 1 once the row emits stop_id. V % 4 == 0, ld % 4 == 0, logits
- * 16-byte aligned. */
+ * 16-byte aligned. d_work (may be NULL) is scratch of qwen3_greedy_workspace(B) bytes, 16-byte aligned,
+ * zero before its first use (each call leaves it as the next call needs it); with it each row is split
+ * over several CTAs and merged by the last one to finish, without it one CTA reads each row. Calls that
+ * share a d_work must not overlap on the GPU. */
+QWEN3_API size_t qwen3_greedy_workspace(int B);
 QWEN3_API int qwen3_op_greedy(const float* d_logits, int64_t ld, int B, int V, int stop_id, int32_t* d_done,
-                              int32_t* d_next, void* stream);
+                              int32_t* d_next, int32_t* d_work, void* stream);
 
 /* Allocation-free variant of qwen3_op_attention_decode, for callers that cannot call cudaMalloc:
  * code whose device memory belongs to another allocator (for example a framework's caching pool),

@@ -99,7 +99,9 @@ def lib() -> ctypes.CDLL:
     L.qwen3_attention_decode_workspace.argtypes = [i, i, i, i, i, i]
     L.qwen3_op_attention_decode.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, i, i, _vp, _vp, _vp, _vp]
     L.qwen3_op_attention_decode_noalloc.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp, _vp]
-    L.qwen3_op_greedy.argtypes = [_vp, ctypes.c_int64, i, i, i, _vp, _vp, _vp]
+    L.qwen3_op_greedy.argtypes = [_vp, ctypes.c_int64, i, i, i, _vp, _vp, _vp, _vp]
+    L.qwen3_greedy_workspace.restype = sz
+    L.qwen3_greedy_workspace.argtypes = [i]
     L.qwen3_prefill_padded.argtypes = [_vp, _vp, _i32p, i, i, _vp, i, _vp]
     L.qwen3_share_prefix.argtypes = [_vp, i, _vp]
     L.qwen3_generate.argtypes = [_vp, _vp, _i32p, i, i, i, i, _vp, _i32p, _vp]
@@ -339,7 +341,21 @@ def op_attention_decode(q, k_cache, v_cache, len0, work, out, seq_meta=None, win
                                           _p(seq_meta), window, ring, _p(work), _p(out), _p(err), _stream(stream)))
 
 
-def op_greedy(logits, next_ids, stop_id=-1, done=None, stream=None):
+_greedy_work = {}
+
+
+def greedy_workspace(B) -> int:
+    return lib().qwen3_greedy_workspace(B)
+
+
+def op_greedy(logits, next_ids, stop_id=-1, done=None, work="auto", stream=None):
+    """work: "auto" (a zeroed scratch buffer kept per device and size, reused across calls on one stream),
+    None (one CTA per row), or a caller tensor of greedy_workspace(B) bytes, zero before its first use."""
     B, V = logits.shape
-    check(lib().qwen3_op_greedy(_p(logits), logits.stride(0), B, V, stop_id, _p(done), _p(next_ids),
+    if isinstance(work, str):
+        key = (logits.device, greedy_workspace(B))
+        if key not in _greedy_work:
+            _greedy_work[key] = torch.zeros(max(1, key[1] // 4), dtype=torch.int32, device=logits.device)
+        work = _greedy_work[key]
+    check(lib().qwen3_op_greedy(_p(logits), logits.stride(0), B, V, stop_id, _p(done), _p(next_ids), _p(work),
                                 _stream(stream)))

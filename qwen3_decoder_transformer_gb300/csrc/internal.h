@@ -163,9 +163,11 @@ cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, in
                                           const int* meta, int rolling, cudaStream_t st);
 // Length bookkeeping on the device: *len = value, or *len += delta.
 // Greedy next tokens of B rows of logits (row stride ld floats); see greedy_kernel. done/next/out/alive
-// may be null (done null: no stop handling).
+// may be null (done null: no stop handling). work: greedy_workspace_ints(B) ints whose tickets are zero
+// before the first launch (each launch leaves them zero), or null (one CTA per row).
+size_t greedy_workspace_ints(int B);
 cudaError_t greedy_launch(const float* logits, long long ld, int B, int V, int stop_id, int* done, int* next, int* out,
-                          long long out_ld, int out_col, int* alive, cudaStream_t st);
+                          long long out_ld, int out_col, int* alive, int* work, cudaStream_t st);
 cudaError_t copy_prefix_slots_launch(__nv_bfloat16* kc, __nv_bfloat16* vc, size_t layer_elems, int L, int nb, int Hkv,
                                      int cap, int dh, int s0, int s1, cudaStream_t st);
 cudaError_t set_len_launch(int* len, int value, cudaStream_t st);

@@ -372,45 +372,20 @@ __global__ void add_len_kernel(int* len, int delta) {
 }
 
 // Greedy next token ("A modern architecture: Qwen3", generation: argmax of the last row's logits):
-// one CTA per row finds the largest logit, the lowest index on ties, a NaN counting as the largest
-// (torch.argmax's rule). With stop_id >= 0 a finished row emits stop_id, and a row that emits it is
-// finished; `alive` counts the rows still running after this step.
-constexpr int GREEDY_THREADS = 1024, GREEDY_UNROLL = 4;
+// the largest logit, the lowest index on ties, a NaN counting as the largest (torch.argmax's rule).
+// A row is split over P CTAs (grid P x B) so that a decode batch of a few rows still streams its
+// logits with most SMs: each CTA reduces a segment to one candidate, and the last CTA of the row to
+// finish (a ticket per row) picks the best candidate. The comparison is a total order, so the result
+// does not depend on which CTA finishes last. With stop_id >= 0 a finished row emits stop_id, and a
+// row that emits it is finished; `alive` counts the rows still running after this step.
+constexpr int GREEDY_THREADS = 512, GREEDY_UNROLL = 4, GREEDY_MAX_PARTS = 32, GREEDY_TICKETS_PAD = 64;
 __device__ __forceinline__ bool greedy_better(float v, int i, float bv, int bi) {
     const bool nv = v != v, nb = bv != bv;
     if (nv != nb) return nv;
     if (nv) return i < bi;
     return v > bv || (v == bv && i < bi);
 }
-__global__ void __launch_bounds__(GREEDY_THREADS)
-    greedy_kernel(const float* __restrict__ logits, long long ld, int V, int stop_id, int* __restrict__ done,
-                  int* __restrict__ next, int* __restrict__ out, long long out_ld, int out_col, int* __restrict__ alive) {
-    pdl_wait();
-    pdl_trigger();
-    const int b = blockIdx.x;
-    const float* row = logits + (size_t)b * ld;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    // GREEDY_UNROLL independent 16-byte loads in flight per thread
-    for (int base = threadIdx.x * 4; base < V; base += GREEDY_THREADS * 4 * GREEDY_UNROLL) {
-        float4 v[GREEDY_UNROLL];
-#pragma unroll
-        for (int u = 0; u < GREEDY_UNROLL; ++u) {
-            const int i = base + u * GREEDY_THREADS * 4;
-            v[u] = i < V ? *reinterpret_cast<const float4*>(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
-#pragma unroll
-        for (int u = 0; u < GREEDY_UNROLL; ++u) {
-            const int i = base + u * GREEDY_THREADS * 4;
-            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (i + k < V && greedy_better(e[k], i + k, bv, bi)) {
-                    bv = e[k];
-                    bi = i + k;
-                }
-        }
-    }
+__device__ __forceinline__ void greedy_warp_best(float& bv, int& bi) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -420,19 +395,74 @@ __global__ void __launch_bounds__(GREEDY_THREADS)
             bi = oi;
         }
     }
+}
+// work: [GREEDY_TICKETS_PAD rounded up to B] ticket ints (zero on entry, left zero), then [B][P] candidates
+// (value bits, index); unused when P == 1.
+__global__ void __launch_bounds__(GREEDY_THREADS)
+    greedy_kernel(const float* __restrict__ logits, long long ld, int V, int stop_id, int* __restrict__ done,
+                  int* __restrict__ next, int* __restrict__ out, long long out_ld, int out_col, int* __restrict__ alive,
+                  int* __restrict__ work, int tickets) {
+    pdl_wait();
+    pdl_trigger();
+    const int p = blockIdx.x, P = gridDim.x, b = blockIdx.y;
+    const float* row = logits + (size_t)b * ld;
+    const int seg = ((V + P - 1) / P + 3) / 4 * 4;  // a multiple of 4 floats: every float4 load stays aligned
+    const int lo = p * seg, hi = min(V, lo + seg);
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    // GREEDY_UNROLL independent 16-byte loads in flight per thread
+    for (int base = lo + threadIdx.x * 4; base < hi; base += GREEDY_THREADS * 4 * GREEDY_UNROLL) {
+        float4 v[GREEDY_UNROLL];
+#pragma unroll
+        for (int u = 0; u < GREEDY_UNROLL; ++u) {
+            const int i = base + u * GREEDY_THREADS * 4;
+            v[u] = i < hi ? __ldg(reinterpret_cast<const float4*>(row + i)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < GREEDY_UNROLL; ++u) {
+            const int i = base + u * GREEDY_THREADS * 4;
+            const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (i + k < hi && greedy_better(e[k], i + k, bv, bi)) {
+                    bv = e[k];
+                    bi = i + k;
+                }
+        }
+    }
+    greedy_warp_best(bv, bi);
     __shared__ float sv[GREEDY_THREADS / 32];
     __shared__ int si[GREEDY_THREADS / 32];
+    __shared__ int last;
     if ((threadIdx.x & 31) == 0) {
         sv[threadIdx.x >> 5] = bv;
         si[threadIdx.x >> 5] = bi;
     }
     __syncthreads();
+    if (threadIdx.x < 32) {
+        bv = threadIdx.x < GREEDY_THREADS / 32 ? sv[threadIdx.x] : -INFINITY;
+        bi = threadIdx.x < GREEDY_THREADS / 32 ? si[threadIdx.x] : 0x7fffffff;
+        greedy_warp_best(bv, bi);
+    }
+    if (P > 1) {
+        int* tick = work + b;
+        int2* cand = reinterpret_cast<int2*>(work + tickets) + (size_t)b * P;
+        if (threadIdx.x == 0) {
+            cand[p] = make_int2(__float_as_int(bv), bi);
+            __threadfence();
+            last = atomicAdd(tick, 1) == P - 1;
+        }
+        __syncthreads();
+        if (!last) return;
+        if (threadIdx.x >= 32) return;
+        __threadfence();
+        const int2 c = threadIdx.x < P ? __ldcg(cand + threadIdx.x) : make_int2(__float_as_int(-INFINITY), 0x7fffffff);
+        bv = __int_as_float(c.x);
+        bi = c.y;
+        greedy_warp_best(bv, bi);
+        if (threadIdx.x == 0) *tick = 0;  // ready for the next launch
+    }
     if (threadIdx.x == 0) {
-        for (int w = 1; w < GREEDY_THREADS / 32; ++w)
-            if (greedy_better(sv[w], si[w], bv, bi)) {
-                bv = sv[w];
-                bi = si[w];
-            }
         if (bi >= V) bi = 0;  // every logit was -inf: the first index, as argmax returns
         int tok = bi;
         if (stop_id >= 0 && done) {
@@ -578,12 +608,26 @@ cudaError_t qknorm_rope_append_f32_launch(const float* ws, int splits, int B, in
     return cudaErrorInvalidValue;
 }
 
+int greedy_parts(int B, int V) {
+    const int per_cta = GREEDY_THREADS * 4 * GREEDY_UNROLL;  // floats one CTA pass covers
+    const int max_p = (V + per_cta - 1) / per_cta;
+    const int want = (2 * device_sm_count() + B - 1) / std::max(B, 1);
+    return std::max(1, std::min(std::min(max_p, want), GREEDY_MAX_PARTS));
+}
+
+size_t greedy_workspace_ints(int B) {
+    const int tickets = (std::max(B, 1) + GREEDY_TICKETS_PAD - 1) / GREEDY_TICKETS_PAD * GREEDY_TICKETS_PAD;
+    return (size_t)tickets + (size_t)std::max(B, 1) * GREEDY_MAX_PARTS * 2;
+}
+
 cudaError_t greedy_launch(const float* logits, long long ld, int B, int V, int stop_id, int* done, int* next, int* out,
-                          long long out_ld, int out_col, int* alive, cudaStream_t st) {
+                          long long out_ld, int out_col, int* alive, int* work, cudaStream_t st) {
     if (B <= 0) return cudaSuccess;
     if (V < 1 || V % 4 || ld % 4) return cudaErrorInvalidValue;
-    return launch_pdl(greedy_kernel, dim3(B), dim3(GREEDY_THREADS), 0, st, logits, ld, V, stop_id, done, next, out,
-                      out_ld, out_col, alive);
+    const int P = work ? greedy_parts(B, V) : 1;
+    const int tickets = (B + GREEDY_TICKETS_PAD - 1) / GREEDY_TICKETS_PAD * GREEDY_TICKETS_PAD;
+    return launch_pdl(greedy_kernel, dim3(P, B), dim3(GREEDY_THREADS), 0, st, logits, ld, V, stop_id, done, next, out,
+                      out_ld, out_col, alive, work, tickets);
 }
 
 cudaError_t set_seq_launch(int* dst, const int* vals, int n, cudaStream_t st) {

@@ -109,6 +109,7 @@ struct qwen3_ctx {
     // greedy generation state: logits of the last rows, finished flags, next ids, running count
     float* gen_logits = nullptr;
     int *gen_done = nullptr, *gen_next = nullptr, *gen_alive = nullptr;
+    int* gen_work = nullptr;  // greedy kernel: per-row tickets (zero between launches) and candidates
     int* h_alive = nullptr;  // pinned
     int32_t* d_ids_buf = nullptr;
     float* d_logits_buf = nullptr;
@@ -424,7 +425,7 @@ void release(qwen3_ctx* c) {
     void* bufs[] = {c->wqkv, c->wgu,      c->kcache, c->vcache, c->rope,      c->x,           c->xn,
                     c->q,    c->attn,     c->h,      c->hn,     c->dec_work,  c->attn_ws,     c->skinny_ws, c->d_len,
                     c->d_err, c->d_ids_buf, c->d_logits_buf, c->d_seq, c->gen_logits, c->gen_done, c->gen_next,
-                    c->gen_alive, c->fin_part, c->fin_tick, c->norm_part, c->norm_count};
+                    c->gen_alive, c->gen_work, c->fin_part, c->fin_tick, c->norm_part, c->norm_count};
     for (void* p : bufs)
         if (p) cudaFree(p);
     if (c->h_alive) cudaFreeHost(c->h_alive);
@@ -446,6 +447,8 @@ int ensure_generation_buffers(qwen3_ctx* c) {
     const size_t mb = (size_t)c->max_batch;
     if (dmalloc(&c->gen_logits, mb * c->cfg.vocab) != cudaSuccess || dmalloc(&c->gen_done, mb) != cudaSuccess ||
         dmalloc(&c->gen_next, mb) != cudaSuccess || dmalloc(&c->gen_alive, 1) != cudaSuccess ||
+        dmalloc(&c->gen_work, greedy_workspace_ints((int)mb)) != cudaSuccess ||
+        cudaMemset(c->gen_work, 0, greedy_workspace_ints((int)mb) * sizeof(int)) != cudaSuccess ||
         cudaMallocHost(reinterpret_cast<void**>(&c->h_alive), sizeof(int)) != cudaSuccess) {
         cudaGetLastError();
         return QWEN3_E_CUDA;
@@ -730,7 +733,7 @@ int qwen3_generate(qwen3_ctx* c, const int32_t* d_ids, const int32_t* h_real, in
     for (;;) {
         if (cudaMemsetAsync(c->gen_alive, 0, sizeof(int), st) != cudaSuccess) return QWEN3_E_CUDA;
         if (greedy_launch(c->gen_logits, V, B, V, stop_id, stop_id >= 0 ? c->gen_done : nullptr, c->gen_next, d_out,
-                          max_new, steps, c->gen_alive, st) != cudaSuccess)
+                          max_new, steps, c->gen_alive, c->gen_work, st) != cudaSuccess)
             return QWEN3_E_CUDA;
         ++steps;
         if (steps == max_new) break;
@@ -746,11 +749,13 @@ int qwen3_generate(qwen3_ctx* c, const int32_t* d_ids, const int32_t* h_real, in
     return QWEN3_OK;
 }
 
+size_t qwen3_greedy_workspace(int B) { return B < 1 ? 0 : greedy_workspace_ints(B) * sizeof(int); }
+
 int qwen3_op_greedy(const float* logits, int64_t ld, int B, int V, int stop_id, int32_t* done, int32_t* next,
-                    void* stream) {
+                    int32_t* work, void* stream) {
     if (!logits || !next || B < 0 || V < 4 || V % 4 || ld < V || ld % 4 || !is_aligned(logits, 16)) return QWEN3_E_ARG;
-    if (stop_id >= V) return QWEN3_E_ARG;
-    return greedy_launch(logits, ld, B, V, stop_id, stop_id >= 0 ? done : nullptr, next, nullptr, 0, 0, nullptr,
+    if (stop_id >= V || (work && !is_aligned(work, 16))) return QWEN3_E_ARG;
+    return greedy_launch(logits, ld, B, V, stop_id, stop_id >= 0 ? done : nullptr, next, nullptr, 0, 0, nullptr, work,
                          static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

@@ -8,6 +8,9 @@ row by row from the GPU's own layer input (tapped through qwen3_set_tap) and the
          GPU's layer output rows must match (<= 1e-2);
   a10-11 the oracle applies the final norm + LM head to the GPU's final hidden rows; logits <= 2e-2
          and top-1 agreement.
+Layer 0's K/V cache is also checked slot by slot over whole 128-slot tiles (every slot at the 0.6B
+1x2048 shape; the first and the last tile at the larger shapes), and at the 0.6B 1x2048 shape the logits
+of 128 consecutive rows (QWEN3_ALL_ROWS) must agree on the top-1 token for >= 99% of the rows.
 Decode uses a cache pre-filled with bf16 N(0, 1) K/V at the workload's context length.
 """
 import numpy as np
@@ -16,7 +19,7 @@ import torch
 
 import oracle as O
 from qwen3_decoder_transformer_gb300 import WORKLOADS, build as Bld, synth
-from tests.util import bits, rel_l2, top1_agreement, widen
+from tests.util import bits, max_rel_rows, rel_l2, top1_agreement, widen
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +62,29 @@ def _check_layer(m, w, cfg, layer, xin, xout, rows, pos, kvset, B):
     return om
 
 
+def _check_kv_rows(m, w, cfg, layer, xin, rows, pos, kvset, chunk=256):
+    """K and V cache slots of `rows` against the oracle's projection + q/k-norm + RoPE of the same tapped
+    inputs: relative L2 <= 1e-3 over all of them and <= 1e-2 for every single (slot, head) vector."""
+    om = _host_layer(w, cfg, layer)
+    k_gpu, v_gpu = m.kv_view(layer)
+    dh = cfg["head_dim"]
+    sets = sorted(set(kvset.tolist()))
+    kc, vc = bits(k_gpu[sets]), bits(v_gpu[sets])  # the sequences involved, copied to the host once
+    local = np.array([sets.index(x) for x in kvset.tolist()], dtype=np.int64)
+    kg_all, vg_all, kr_all, vr_all = [], [], [], []
+    for a in range(0, len(rows), chunk):
+        r, p_, s_ = rows[a:a + chunk], pos[a:a + chunk], local[a:a + chunk]
+        _, k, v = om.layer_qkv(layer, xin[r], p_)
+        kg_all.append(kc[s_, :, p_])
+        vg_all.append(vc[s_, :, p_])
+        kr_all.append(k)
+        vr_all.append(v)
+    kg, vg = widen(np.concatenate(kg_all)), widen(np.concatenate(vg_all))
+    kr, vr = widen(np.concatenate(kr_all)), widen(np.concatenate(vr_all))
+    assert rel_l2(kg, kr) <= 1e-3 and rel_l2(vg, vr) <= 1e-3, (layer, rel_l2(kg, kr), rel_l2(vg, vr))
+    assert max_rel_rows(kg, kr, dh) <= 1e-2 and max_rel_rows(vg, vr, dh) <= 1e-2
+
+
 def _tapped_prefill(bd, m, ids, layer, rows_total, d):
     xin = torch.empty(rows_total, d, dtype=torch.bfloat16, device="cuda")
     xout = torch.empty_like(xin)
@@ -77,7 +103,7 @@ def _sample_rows(n_rows, count, seed):
     return np.unique(np.concatenate([[0, n_rows - 1], extra])).astype(np.int64)
 
 
-def _run_prefill_check(bd, name, sample):
+def _run_prefill_check(bd, name, sample, all_rows_top1=False):
     wl = WORKLOADS[name]
     cfg, seed = wl["model"], wl["seed"]
     B, T = wl["prefill"]
@@ -91,12 +117,34 @@ def _run_prefill_check(bd, name, sample):
     for layer in sorted({0, L // 2, L - 1}):
         xin, xout, logits = _tapped_prefill(bd, m, ids, layer, B * T, d)
         om = _check_layer(m, w, cfg, layer, xin, xout, rows, pos, kvset, B)
+        if layer == 0:
+            # whole tiles of layer 0's cache: every slot when the oracle can afford it, else the first
+            # and the last 128-slot tile
+            tiles = np.arange(B * T) if B * T <= 2048 else np.concatenate([np.arange(128), np.arange(B * T - 128, B * T)])
+            _check_kv_rows(m, w, cfg, 0, xin, tiles, (tiles % T).astype(np.int32), (tiles // T).astype(np.int32))
     # final norm + LM head on each sequence's last row, from the GPU's final hidden state
     last = np.arange(B) * T + T - 1
     ref = om.head(xout[last])
     assert rel_l2(logits, ref) <= 2e-2
     raw, filt, _ = top1_agreement(logits, ref)
     assert filt >= 0.99
+    if all_rows_top1:
+        # logits of every row (QWEN3_ALL_ROWS); the oracle's final norm + LM head on the GPU's final
+        # hidden state of the last 128 rows: raw top-1 agreement over those 128 rows
+        m.set_length(0, 0)
+        hid_in = torch.empty(B * T, d, dtype=torch.bfloat16, device="cuda")
+        hid_out = torch.empty_like(hid_in)
+        m.set_tap(L - 1, hid_in, hid_out)
+        all_logits = torch.empty(B * T, V, dtype=torch.float32, device="cuda")
+        m.prefill(ids, all_logits, all_rows=True)
+        assert m.get_error() == 0
+        m.set_tap(-1)
+        chunk = np.arange(B * T - 128, B * T)
+        got = all_logits[torch.from_numpy(chunk).cuda()].cpu().numpy()
+        ref = om.head(bits(hid_out)[chunk])
+        assert rel_l2(got, ref) <= 2e-2
+        raw, filt, n_clear = top1_agreement(got, ref)
+        assert raw >= 0.99 and filt >= 0.99, (raw, filt, n_clear)
     m.close()
     return w, cfg
 
@@ -147,7 +195,7 @@ def _run_decode_check(bd, name, sample_b, steps=2):
 
 
 def test_qwen3_0p6b_prefill_1x2048(bd):
-    _run_prefill_check(bd, "0.6b-prefill-1x2048", 30)
+    _run_prefill_check(bd, "0.6b-prefill-1x2048", 30, all_rows_top1=True)
 
 
 def test_qwen3_0p6b_prefill_8x4096(bd):

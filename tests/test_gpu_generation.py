@@ -75,6 +75,33 @@ def test_greedy_kernel(bd):
     assert nxt.cpu().numpy().tolist() == np.argmax(lg, axis=1).tolist()
 
 
+@pytest.mark.parametrize("B", [1, 3, 16, 64])
+def test_greedy_kernel_split_rows(bd, B):
+    """Vocabulary-sized rows (151,936 logits) are split over several CTAs per row and merged by the last
+    one: ties, NaN and maxima placed across segment boundaries, with the workspace (split rows) and without
+    it (one CTA per row), twice in a row (the tickets must be left at zero)."""
+    rng = np.random.default_rng(50 + B)
+    V = 151936
+    lg = rng.standard_normal((B, V)).astype(np.float32)
+    lg[0, [70000, 9000, 150000]] = 7.0                # tie across segments: lowest index
+    if B > 1:
+        lg[1, [120001, 80000]] = np.nan               # NaN wins, first NaN
+        lg[1, 5] = 1e30
+    if B > 2:
+        lg[2, :] = -np.inf                            # nothing finite: index 0
+    if B > 3:
+        lg[3, V - 1] = 99.0                           # the very last element
+        lg[4, 0] = 99.0                               # the very first element
+    t = torch.from_numpy(lg).cuda()
+    ref = np.argmax(lg, axis=1).tolist()
+    work = torch.zeros(max(1, bd.greedy_workspace(B) // 4), dtype=torch.int32, device="cuda")
+    for w in (work, work, None):
+        nxt = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+        bd.op_greedy(t, nxt, work=w)
+        assert nxt.cpu().numpy().tolist() == ref
+    assert not work[:64].any()
+
+
 # ------------------------------------------------------------------------------- left padding
 
 def _run_padded(bd, w, prompts, steps_o, cap, prefix_ids=None):
