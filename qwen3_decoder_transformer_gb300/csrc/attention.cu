@@ -1144,8 +1144,8 @@ __global__ void __launch_bounds__(DH)
     __shared__ float wgt[COMB_MAX_SPLITS];
     __shared__ float red[DH / 32];
     __shared__ float inv_l;
+    pdl_trigger();  // the next kernel only prefetches weights before its own wait
     pdl_wait();
-    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const float* wb = work + ((size_t)b * Hq + h) * nsplit * REC;
     const int n = *len0p + 1;
@@ -1293,10 +1293,10 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         max_chunks = 1;
     }
     if (heads == 0) {
-        // Two heads per CTA share each K/V tile and have the best per-tile throughput on long grids;
-        // below ~16 waves of those CTAs the persistent one-head kernel wins on load balance.
-        const long long ctas2 = (long long)((T + TC_BM - 1) / TC_BM) * (Hq / 2) * B;
-        heads = (Hq / Hkv) % 2 == 0 && (split > 0 || ctas2 >= 16LL * device_sm_count()) ? 2 : 1;
+        // The persistent one-head kernel (scores two tiles ahead, score and P V MMAs from separate warps)
+        // is the fastest at every measured size, the longest included (8B 1x32768: 5.93 ms against 6.60
+        // for two heads per CTA); a split KV range runs in the two-heads kernel when the group allows it.
+        heads = (Hq / Hkv) % 2 == 0 && split > 0 ? 2 : 1;
     }
     if (heads == 2 && (Hq / Hkv) % 2 == 0)
         return prefill_launch_nh<DH, 2>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);

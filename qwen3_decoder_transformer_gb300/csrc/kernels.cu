@@ -63,8 +63,8 @@ template <int CACHE>
 __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int rows,
                                int n, long long in_stride, long long in_offset, float eps,
                                __nv_bfloat16* __restrict__ y) {
+    pdl_trigger();  // the next kernel only prefetches weights before its own wait
     pdl_wait();
-    pdl_trigger();
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(FIN_THREADS)
                                      __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int M, int n,
                                      float eps, __nv_bfloat16* __restrict__ y, float* __restrict__ part,
                                      int* __restrict__ tick) {
+    pdl_trigger();  // the next kernel only prefetches weights before its own wait
     pdl_wait();
-    pdl_trigger();
     __shared__ float red[FIN_THREADS / 32];
     __shared__ int last;
     const int row = blockIdx.x, chunk = blockIdx.y, chunks = gridDim.y;
@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(FIN_ROW_THREADS)
     finalize_residual_rmsnorm_row_kernel(const float* __restrict__ ws, int splits, long long ldw,
                                      __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ g, int M, int n,
                                      float eps, __nv_bfloat16* __restrict__ y) {
+    pdl_trigger();  // the next kernel only prefetches weights before its own wait
     pdl_wait();
-    pdl_trigger();
     __shared__ float red[FIN_ROW_THREADS / 32];
     const int row = blockIdx.x;
     constexpr int MAXG = 2;  // 8-element groups per thread: rows up to 256 * 8 * 2 = 4096 elements
@@ -337,8 +337,8 @@ __global__ void __launch_bounds__(FIN_ROW_THREADS)
 // (128-column blocks: gate block j at columns 256j.., up block at 256j+128..).
 __global__ void finalize_swiglu_kernel(const float* __restrict__ ws, int splits, long long ldw,
                                        __nv_bfloat16* __restrict__ h, int M, int F) {
+    pdl_trigger();  // the next kernel only prefetches weights before its own wait
     pdl_wait();
-    pdl_trigger();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // one thread per 4 outputs
     if (idx >= (long long)M * F / 4) return;
     const int row = (int)(idx / (F / 4)), j = (int)(idx % (F / 4)) * 4;

@@ -320,8 +320,10 @@ def test_decode_attention_layout_op(bd, ps, psh, pads):
         assert max_rel_rows(got[b], ref, dh) <= 3e-2, b
 
 
-def test_prefill_attention_window_ring_op(bd):
-    """Prefill attention over a rolling buffer with a window, against oracle rows gathered by position."""
+@pytest.mark.parametrize("heads", [0, 2])
+def test_prefill_attention_window_ring_op(bd, heads):
+    """Prefill attention over a rolling buffer with a window, against oracle rows gathered by position,
+    with the automatic kernel choice and with two heads per CTA."""
     rng = np.random.default_rng(91)
     B, Hq, Hkv, dh, T, W, R = 2, 8, 4, 64, 128, 100, 256
     len0 = 300  # positions 300..427 read keys back to 201, rows p mod 256
@@ -332,7 +334,8 @@ def test_prefill_attention_window_ring_op(bd):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
     bd.op_attention_prefill(synth.from_numpy_bits(q, "cuda"), synth.from_numpy_bits(kc, "cuda"),
-                            synth.from_numpy_bits(vc, "cuda"), len_t, out, err=err, window=W, ring=R)
+                            synth.from_numpy_bits(vc, "cuda"), len_t, out, err=err, window=W, ring=R,
+                            heads_per_cta=heads)
     assert int(err.item()) == 0
     got = widen(bits(out)).reshape(B, T, Hq, dh)
     for b in range(B):
@@ -342,3 +345,35 @@ def test_prefill_attention_window_ring_op(bd):
             ref = O.attention_gqa_row_f64(q[b, :, t], np.ascontiguousarray(kc[b][:, keys]),
                                           np.ascontiguousarray(vc[b][:, keys]), W)
             assert rel_l2(got[b, t], ref) <= 1e-2, (b, t)
+
+
+@pytest.mark.parametrize("heads", [1, 2])
+def test_prefill_attention_padding_op(bd, heads):
+    """Prefill attention with left padding at the start of the block (a padded prompt batch), one and two
+    heads per CTA, against masked oracle rows: a real token sees the real slots up to its own, a padding
+    slot sees only itself. Row 2's padding covers the first 128-slot tile whole (skipped by the kernels)."""
+    rng = np.random.default_rng(92)
+    B, Hq, Hkv, dh, T = 3, 8, 2, 128, 300
+    pads = [0, 37, 200]
+    q = _rand(rng, (B, Hq, T, dh))
+    kc = _rand(rng, (B, Hkv, T, dh))
+    vc = _rand(rng, (B, Hkv, T, dh))
+    meta = torch.tensor([0, 0] + pads, dtype=torch.int32, device="cuda")
+    out = torch.empty(B * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    len_t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.op_attention_prefill(synth.from_numpy_bits(q, "cuda"), synth.from_numpy_bits(kc, "cuda"),
+                            synth.from_numpy_bits(vc, "cuda"), len_t, out, err=err, seq_meta=meta,
+                            heads_per_cta=heads)
+    assert int(err.item()) == 0
+    got = widen(bits(out)).reshape(B, T, Hq, dh)
+    for b in range(B):
+        for t in (0, 5, 36, 37, 127, 128, 199, 200, 201, 255, 256, 299):
+            mask = np.zeros(T, bool)
+            mask[:t + 1] = True
+            mask[:pads[b]] = False
+            mask[t] = True
+            ref = O.attention_masked_gqa_row_f64(q[b, :, t], kc[b], vc[b], mask)
+            assert np.isfinite(got[b, t]).all(), (b, t)
+            assert rel_l2(got[b, t], ref) <= 1e-2, (b, t)
+            assert max_rel_rows(got[b, t], ref, dh) <= 3e-2, (b, t)

@@ -295,6 +295,15 @@ def test_attention_prefill_one_head_per_cta(bd, Bq, T, Hq, Hkv, dh, len0):
         _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 1, 3, heads=1)
 
 
+@pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0", [(1, 64, 8, 4, 64, 0), (2, 130, 8, 2, 64, 0), (1, 700, 8, 2, 128, 0),
+                                                  (2, 77, 16, 8, 128, 70), (3, 257, 8, 2, 128, 511),
+                                                  (1, 1100, 4, 2, 128, 1000)])
+def test_attention_prefill_two_heads_per_cta(bd, Bq, T, Hq, Hkv, dh, len0):
+    """The two-heads-per-CTA kernel without a KV split (the long-prompt kernel; the automatic choice takes it
+    only at 16 or more waves of CTAs, so the heads are forced here)."""
+    _attention_prefill_case(bd, Bq, T, Hq, Hkv, dh, len0, 0, 1, heads=2)
+
+
 @pytest.mark.parametrize("Bq,T,Hq,Hkv,dh,len0,split,chunks", [(1, 700, 8, 2, 128, 0, 1, 4), (1, 1024, 16, 8, 128, 0, 2, 4),
                                                                (2, 257, 8, 8, 128, 511, 1, 3), (1, 384, 4, 1, 64, 129, 1, 2),
                                                                (1, 300, 8, 4, 64, 70, 1, 8)])
