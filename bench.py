@@ -201,6 +201,15 @@ def cpu_description() -> dict:
                     model = "cpu part " + v.strip()
     except OSError:
         pass
+    if model is None or model.startswith("cpu part"):
+        try:  # lscpu names Arm cores that /proc/cpuinfo lists only by part number
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for ln in out.splitlines():
+                if ln.lower().startswith("model name:"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
     import platform
     return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine(),
             "machine": platform.machine()}
