@@ -473,7 +473,7 @@ struct PsLayout {
     static constexpr int SMEM = BAR_OFF + 256 + 1024;
 };
 
-template <int DH>
+template <int DH, bool SPEC>
 __global__ void __launch_bounds__(PS_THREADS, 1)
     attn_prefill_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                                    const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv, int B,
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 const Item it = item_of(round);
                 if (it.n_tiles == 0) break;
                 const int jkv = it.h / (Hq / Hkv);
-                if (!mbar_wait(q_empty, (round & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_suspend(q_empty, (round & 1) ^ 1, abort_flag)) { ok = false; break; }
                 mbar_expect_tx(q_full, Ly::Q_BYTES);
                 for (int cc = 0; cc < NCH; ++cc)
                     tma_load_3d(smem + Ly::Q_OFF + cc * TC_BM * 128, &tmQ, q_full, cc * 64, it.q0, it.b * Hq + it.h);
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     const uint32_t free_ph = ((g / PS_KST) & 1) ^ 1;
                     const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
                     const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
-                    if (!mbar_wait(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_suspend(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
                     for (int cc = 0; cc < NCH; ++cc)
                         tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmK, &k_full[s], cc * 64, y, z);
@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
                     const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
                     const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
-                    if (!mbar_wait(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_suspend(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
                     mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
                     for (int cc = 0; cc < NCH; ++cc)
                         tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmV, &v_full[s], cc * 64, y, z);
@@ -630,13 +630,13 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 const Item it = item_of(round);
                 const int nt = it.n_tiles;
                 if (nt == 0) break;
-                if (!mbar_wait(q_full, round & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait_suspend(q_full, round & 1, abort_flag)) { ok = false; break; }
                 for (int i = 0; i < nt; ++i) {
                     const int gi = g + i, s = gi % PS_KST, r = gi % NR;
-                    if (!mbar_wait(&k_full[s], (gi / PS_KST) & 1, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_suspend(&k_full[s], (gi / PS_KST) & 1, abort_flag)) { ok = false; break; }
                     // region r's next completion would be P V of tile gi itself, not yet possible: the
                     // parity wait cannot alias
-                    if (gi >= NR && !mbar_wait(&r_free[r], ((gi - NR) / NR) & 1, abort_flag)) {
+                    if (gi >= NR && !mbar_wait_suspend(&r_free[r], ((gi - NR) / NR) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
             for (int i = 0; ok && i < nt; ++i) {
                 const int gi = g + i, s = gi & 1, r = gi % NR;
                 const int j = tile_j(it, i);
-                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait_suspend(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
                 uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
                 const int r0 = it.n_valid - j * TC_BN;  // first stale key row of this tile
                 if (r0 < TC_BN) {
@@ -680,8 +680,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    bool w = i > 0 || mbar_wait(o_free, (round & 1) ^ 1, abort_flag);  // previous item's O read out
-                    w = w && mbar_wait(&p_full[r], (gi / NR) & 1, abort_flag);
+                    bool w = i > 0 || mbar_wait_suspend(o_free, (round & 1) ^ 1, abort_flag);  // previous item's O read out
+                    w = w && mbar_wait_suspend(&p_full[r], (gi / NR) & 1, abort_flag);
                     if (w) {
                         tc_fence_after();
                         const uint32_t svv = smem_u32(sv);
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
         // P V of global tile k (and so every earlier one) has completed. The region's next completion
         // would be P V of tile k + NR, which needs a P this thread has not released yet, so the parity
         // wait cannot alias; P is therefore released without waiting for the previous P V.
-        auto pv_done = [&](int k) -> bool { return mbar_wait(&r_free[k % NR], (k / NR) & 1, abort_flag); };
+        auto pv_done = [&](int k) -> bool { return mbar_wait_suspend(&r_free[k % NR], (k / NR) & 1, abort_flag); };
         int g = 0;
         for (int round = 0; ok; ++round) {
             const Item it = item_of(round);
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                 const int gi = g + i, r = gi % NR;
                 const int j = tile_j(it, i);
                 const uint32_t tm_s = tmem + lane_off + r * TC_BN;
-                if (!__all_sync(0xffffffffu, mbar_wait(&s_full[r], (gi / NR) & 1, abort_flag))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait_suspend(&s_full[r], (gi / NR) & 1, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[TC_BN];
 #pragma unroll
@@ -748,9 +748,51 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < TC_BN; ++e) sr[e] = e <= lim ? sr[e] : __float_as_uint(-INFINITY);
                 }
-                float mx = -INFINITY;  // three-input maxima: two scores per instruction
+                // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this tile's region (a row
+                // with no visible key yet keeps m = -inf and gets P = 0); rs2 = their row sum
+                auto exps = [&](float mref, float2& rs2) {
+                    const float nm = mref == -INFINITY ? 0.f : -mref;
+                    const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+                    rs2 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < TC_BN; e += 2) mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 x = fma2(make_float2(__uint_as_float(sr[half * 64 + 2 * e]),
+                                                              __uint_as_float(sr[half * 64 + 2 * e + 1])),
+                                                  sl2x2, nmx2);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            rs2 = add2(rs2, pp);
+                            pk[e] = pack_bf16(pp.x, pp.y);
+                        }
+                        tmem_st_32x32b_x32(tm_s + half * 32, pk);
+                    }
+                };
+                // SPEC: the exponentials start with the running maximum while the tile maximum is reduced
+                // beside them (lazy rescaling keeps m_used in most tiles); a warp recomputes them when one
+                // of its rows grew. The decision is warp-uniform: exps() issues tcgen05.st, which every
+                // lane of the warp must execute.
+                float2 rs2;
+                const bool spec = SPEC && __all_sync(0xffffffffu, m_used != -INFINITY);
+                if (spec) exps(m_used, rs2);
+                // three-input maxima, two scores per instruction; beside the speculative exponentials the
+                // reduction runs as four independent chains so that it finishes with them
+                float mx = -INFINITY;
+                if constexpr (SPEC) {
+                    float m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < TC_BN; e += 8) {
+                        mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                        m1 = fmax3(m1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+                        m2 = fmax3(m2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+                        m3 = fmax3(m3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+                    }
+                    mx = fmaxf(fmaxf(mx, m1), fmaxf(m2, m3));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < TC_BN; e += 2) mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                }
                 mx *= sl2;
                 const bool grow = mx > m_used + 8.0f;
                 const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
@@ -778,22 +820,9 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
                     l *= alpha;
                     m_used = mx;
                 }
-                const float nm = m_used == -INFINITY ? 0.f : -m_used;
-                const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
-                float2 rs2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[half * 64 + 2 * e]),
-                                                          __uint_as_float(sr[half * 64 + 2 * e + 1])),
-                                              sl2x2, nmx2);
-                        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        rs2 = add2(rs2, pp);
-                        pk[e] = pack_bf16(pp.x, pp.y);
-                    }
-                    tmem_st_32x32b_x32(tm_s + half * 32, pk);
+                if (!spec || __any_sync(0xffffffffu, grow)) {
+                    if (spec) tmem_st_wait();  // the speculative P is overwritten
+                    exps(m_used, rs2);
                 }
                 tmem_st_wait();
                 l += rs2.x + rs2.y;
@@ -1280,10 +1309,15 @@ cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, cons
                       sm.meta, sm.window, sm.ring, out, err, split, max_chunks, parts, tickets);
 }
 
+// Key range from which the persistent kernel computes its exponentials speculatively (measured: 8B
+// 1x32768 5.99 -> 5.65 ms, 8B 1x8192 0.403 -> 0.389 ms, 0.6B 8x4096 0.462 -> 0.455 ms; 0.6B 1x2048,
+// 21 us either way, keeps the plain order).
+constexpr int kSpecMinKeys = 4096;
+
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                               int Hq, int Hkv, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out, int* err,
-                              int split, int max_chunks, float* ws, int heads, cudaStream_t st) {
+                              int split, int max_chunks, float* ws, int heads, int kv_hint, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
     if (!encode_tmap_bf16_3d(&tq, q, DH, T, (uint64_t)B * Hq) || !encode_tmap_bf16_3d(&tk, kc, DH, cap, (uint64_t)B * Hkv) ||
         !encode_tmap_bf16_3d(&tv, vc, DH, cap, (uint64_t)B * Hkv))
@@ -1304,8 +1338,11 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
     const long long items = (long long)((T + TC_BM - 1) / TC_BM) * Hq * B;
     const unsigned grid = (unsigned)std::min<long long>(items, device_sm_count());
-    return launch_pdl(attn_prefill_persistent_kernel<DH>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st, tq, tk,
-                      tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
+    if (kv_hint >= kSpecMinKeys)
+        return launch_pdl(attn_prefill_persistent_kernel<DH, true>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st,
+                          tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
+    return launch_pdl(attn_prefill_persistent_kernel<DH, false>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st,
+                      tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
 }
 
 }  // namespace
@@ -1315,15 +1352,17 @@ int attn_heads_per_cta(int Hq, int Hkv) { return (Hq / Hkv) % 2 == 0 ? 2 : 1; }
 
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
-                                int* err, int split, int max_chunks, float* ws, int heads, cudaStream_t st) {
+                                int* err, int split, int max_chunks, float* ws, int heads, int kv_hint,
+                                cudaStream_t st) {
     if (B <= 0 || T <= 0) return cudaSuccess;
     if (sm.ring && (sm.ring % 256 || sm.ring != cap)) return cudaErrorInvalidValue;
     if (heads < 0 || heads > 2) return cudaErrorInvalidValue;
     if (dh == 128)
         return prefill_launch_dh<128>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, heads,
-                                      st);
+                                      kv_hint, st);
     if (dh == 64)
-        return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, heads, st);
+        return prefill_launch_dh<64>(q, kc, vc, B, T, Hq, Hkv, cap, len0, sm, out, err, split, max_chunks, ws, heads,
+                                     kv_hint, st);
     return cudaErrorInvalidValue;
 }
 
@@ -1397,10 +1436,13 @@ cudaError_t decode_prepare_dh() {
 cudaError_t attention_prepare() {
     const void* fns[] = {(const void*)attn_prefill_tc_kernel<128, 1>, (const void*)attn_prefill_tc_kernel<128, 2>,
                          (const void*)attn_prefill_tc_kernel<64, 1>,  (const void*)attn_prefill_tc_kernel<64, 2>,
-                         (const void*)attn_prefill_persistent_kernel<128>, (const void*)attn_prefill_persistent_kernel<64>};
+                         (const void*)attn_prefill_persistent_kernel<128, false>,
+                         (const void*)attn_prefill_persistent_kernel<64, false>,
+                         (const void*)attn_prefill_persistent_kernel<128, true>,
+                         (const void*)attn_prefill_persistent_kernel<64, true>};
     const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM,
-                        PsLayout<128>::SMEM, PsLayout<64>::SMEM};
-    for (int i = 0; i < 6; ++i) {
+                        PsLayout<128>::SMEM, PsLayout<64>::SMEM, PsLayout<128>::SMEM, PsLayout<64>::SMEM};
+    for (int i = 0; i < 8; ++i) {
         cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
     }

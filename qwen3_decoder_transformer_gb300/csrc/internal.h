@@ -180,9 +180,10 @@ cudaError_t add_len_launch(int* len, int delta, cudaStream_t st);
 // cap: physical slots per (sequence, kv head); sm: sequence layout (SeqMap{} for plain sequences).
 cudaError_t attn_prefill_launch(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                                 int Hq, int Hkv, int dh, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out,
-                                int* err, int split, int max_chunks, float* ws, int heads, cudaStream_t st);
+                                int* err, int split, int max_chunks, float* ws, int heads, int kv_hint, cudaStream_t st);
 // heads: query heads per CTA (1 or 2; 0 = chosen from the grid size). One head without a KV split runs
-// the persistent kernel.
+// the persistent kernel. kv_hint: the key count the longest query row will see (len0 + T when the host
+// knows len0, else T); it only picks between two equivalent forms of the persistent kernel.
 int attn_heads_per_cta(int Hq, int Hkv);
 size_t attn_prefill_workspace(int B, int T, int Hq, int Hkv, int dh, int max_chunks);
 void attn_prefill_split_plan(int B, int T, int Hq, int Hkv, int kv_len, int* split, int* max_chunks);

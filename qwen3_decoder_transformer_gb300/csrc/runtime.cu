@@ -314,7 +314,7 @@ int enqueue_forward(qwen3_ctx* c, const int32_t* ids, int B, int T, float* logit
             TRY(timed(c, K_ATTN_PREFILL, 1, st, [&] {
                 return attn_prefill_launch(c->q, layer_k(c, l), layer_v(c, l), B, T, g.n_q_heads, g.n_kv_heads, dh,
                                            c->slots, c->d_len, seq_map(c), c->attn, c->d_err, split, chunks,
-                                           c->attn_ws, 0, st);
+                                           c->attn_ws, 0, c->len + T, st);
             }));
         }
         if (fuse) {
@@ -1015,7 +1015,7 @@ int qwen3_op_attention_prefill(const void* q, const void* kc, const void* vc, in
     return attn_prefill_launch(static_cast<const bf16*>(q), static_cast<const bf16*>(kc), static_cast<const bf16*>(vc),
                                B, T, Hq, Hkv, dh, cap, len0, SeqMap{seq_meta, window, ring}, static_cast<bf16*>(out),
                                err, kv_split,
-                               kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work), heads_per_cta,
+                               kv_chunks < 1 ? 1 : kv_chunks, static_cast<float*>(work), heads_per_cta, T,
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QWEN3_OK
                : QWEN3_E_CUDA;

@@ -372,3 +372,34 @@ def test_attention_decode(bd, Bq, Hq, Hkv, dh, n, extra):
     assert np.isfinite(got).all()
     assert rel_l2(got, ref) <= 1e-2
     assert max_rel_rows(got, ref, dh) <= 3e-2
+
+
+@pytest.mark.parametrize("T,window", [(16384 + 77, 0), (16500, 1000)])
+def test_attention_prefill_long_keys(bd, T, window):
+    """Key ranges of 4096 and more take the speculative form of the persistent kernel (the exponentials
+    start with the running maximum and are recomputed for a warp when one of its rows grew). With a sliding
+    window, rows of one warp reach their first visible key at different tiles. Sampled rows against the
+    oracle's brute-force row, per-row bounds included; slots past the prompt hold NaN."""
+    rng = np.random.default_rng(T + window)
+    Bq, Hq, Hkv, dh = 1, 4, 2, 128
+    cap = T + 3
+    q = rand_bf16(rng, (Bq, Hq, T, dh))
+    kc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    vc = rand_bf16(rng, (Bq, Hkv, cap, dh))
+    kc[:, :, T:] = 0x7FC0
+    vc[:, :, T:] = 0x7FC0
+    out = torch.empty(Bq * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
+    len_t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = _err()
+    bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err, window=window)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = widen(bits(out)).reshape(T, Hq * dh)
+    rows = sorted({0, 1, 127, 128, 999, 1000, 1001, 5000, 8191, 12345, 16383, T - 2, T - 1})
+    for t in rows:
+        lo = max(0, t + 1 - window) if window else 0
+        ref = O.attention_gqa_row_f64(np.ascontiguousarray(q[0, :, t]), np.ascontiguousarray(kc[0][:, lo:t + 1]),
+                                      np.ascontiguousarray(vc[0][:, lo:t + 1]), t + 1 - lo).ravel()
+        assert np.isfinite(got[t]).all(), t
+        assert rel_l2(got[t], ref) <= 1e-2, t
+        assert max_rel_rows(got[t], ref, dh) <= 3e-2, t
