@@ -459,9 +459,30 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
 // issues tcgen05.mma waits while the pipe is full, it then sat behind that S while P of tile j+1
 // was already waiting, and the softmax warps waited for their next scores: about 2,100 cycles per
 // tile against 1,024 of MMA work (clock64 timeline of one CTA, 0.6B 1x2048).
-constexpr int PS_THREADS = 64 + 128 + 64;  // + a TMA warp for the value tiles and a P V MMA warp
-constexpr int PS_KST = 3, PS_VST = 2;      // key and value ring stages
-template <int DH>
+// ALT = false: one softmax warpgroup (warps 2-5); warp 0 streams the keys, warp 1 issues the score
+// MMAs, warp 6 streams the values, warp 7 issues the P V MMAs.
+// ALT = true, for long key ranges: two softmax warpgroups take alternate key tiles (warpgroup 1 the
+// even global tile numbers, warpgroup 2 the odd ones), each thread a whole query row. With one
+// warpgroup the softmax pass sets the period: about 1,400 cycles per tile of mostly dependent work on
+// one warp per sub-partition, against 1,024 cycles of MMA work and 512 of exponentials. The two
+// warpgroups keep each row's scale in step through shared memory: a tile's scale becomes final after
+// the previous tile's (mbarrier fin, one per row quarter and tile parity); its exponentials start
+// speculatively with the scale known so far and are recomputed in the rare tile where it moved.
+// Each warpgroup sums its own tiles' probabilities at its own scale; the two sums meet at the end of
+// the item, where each warpgroup writes half of the output columns. Warpgroup 0 holds the producers
+// (warp 0 keys, 1 score MMAs, 2 values, 3 P V MMAs) and gives registers to the softmax warpgroups
+// (setmaxnreg). The first two tiles of an item run without speculation and the second waits for the
+// first, which costs more than the alternation saves on items of about 30 tiles or fewer (measured:
+// 8B 1x32768 5.69 -> 5.36 ms, 8B 1x8192 equal, 0.6B 8x4096 0.46 -> 0.51 ms).
+template <bool ALT>
+constexpr int ps_threads() { return ALT ? 128 + 256 : 64 + 128 + 64; }
+constexpr int PS_KST = 3, PS_VST = 2;  // key and value ring stages
+constexpr uint32_t PS_REG_PRODUCER = 56, PS_REG_SOFTMAX = 224;
+// the split must fit the registers of the launch (168 per thread at 384 threads and one block per
+// SM) and each sub-partition's register file (one producer warp and two softmax warps)
+static_assert(4 * PS_REG_PRODUCER + 8 * PS_REG_SOFTMAX <= 12 * 168, "register split exceeds the launch");
+static_assert(PS_REG_PRODUCER + 2 * PS_REG_SOFTMAX <= 512, "register split exceeds a sub-partition");
+template <int DH, bool ALT>
 struct PsLayout {
     static constexpr int NCH = DH / 64;
     static constexpr int Q_BYTES = TC_BM * DH * 2;
@@ -470,16 +491,20 @@ struct PsLayout {
     static constexpr int K_OFF = Q_BYTES;
     static constexpr int V_OFF = K_OFF + PS_KST * KV_BYTES;
     static constexpr int BAR_OFF = V_OFF + PS_VST * KV_BYTES;
-    static constexpr int SMEM = BAR_OFF + 256 + 1024;
+    // ALT: 37 barriers, then the row scales [2][128] and row sums [2][2][128] (floats). The other form
+    // keeps the smaller size: the extra 3 KB move the shared-memory carve-out up a step, which cost it
+    // 5-8% (0.6B 8x4096, 8B 1x8192).
+    static constexpr int XCH_OFF = BAR_OFF + (ALT ? 512 : 256);
+    static constexpr int SMEM = XCH_OFF + (ALT ? 6 * TC_BM * 4 : 0) + 1024;
 };
 
-template <int DH, bool SPEC>
-__global__ void __launch_bounds__(PS_THREADS, 1)
+template <int DH, bool SPEC, bool ALT>
+__global__ void __launch_bounds__(ps_threads<ALT>(), 1)
     attn_prefill_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                                    const __grid_constant__ CUtensorMap tmV, int T, int Hq, int Hkv, int B,
                                    const int* __restrict__ len0p, const int* __restrict__ meta, int window, int ring,
                                    __nv_bfloat16* __restrict__ out, int* err) {
-    using Ly = PsLayout<DH>;
+    using Ly = PsLayout<DH, ALT>;
     constexpr int NCH = Ly::NCH;
     constexpr uint32_t IDESC_S = idesc_bf16(TC_BM, TC_BN);
     constexpr uint32_t IDESC_O = idesc_bf16(TC_BM, DH, true);
@@ -501,6 +526,8 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
     uint64_t* r_free = bars + 22;  // [NR] P V of the region's tile is done: the region can take new scores
+    uint64_t* fin = bars + 25;     // ALT [4 row quarters][2 tile parities]: the tile's row scales are final
+    uint64_t* l_meet = bars + 33;  // ALT [4 row quarters]: both warpgroups published the item's row sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (T + TC_BM - 1) / TC_BM;
@@ -520,10 +547,14 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
         }
         for (int i = 0; i < NR; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
+            mbar_init(&p_full[i], 128);  // the softmax warpgroup that owns the tile
             mbar_init(&r_free[i], 1);
         }
-        mbar_init(o_free, 128);
+        mbar_init(o_free, ALT ? 256 : 128);
+        if (ALT) {
+            for (int i = 0; i < 8; ++i) mbar_init(&fin[i], 32);
+            for (int i = 0; i < 4; ++i) mbar_init(&l_meet[i], 64);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -573,130 +604,323 @@ __global__ void __launch_bounds__(PS_THREADS, 1)
     };
     auto tile_j = [](const Item& it, int i) { return it.j_lo + i < it.ja ? it.j_lo + i : it.j_lo + i + (it.jb - it.ja); };
 
-    if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0) {
-            int g = 0;
-            for (int round = 0; ok; ++round) {
-                const Item it = item_of(round);
-                if (it.n_tiles == 0) break;
-                const int jkv = it.h / (Hq / Hkv);
-                if (!mbar_wait_suspend(q_empty, (round & 1) ^ 1, abort_flag)) { ok = false; break; }
-                mbar_expect_tx(q_full, Ly::Q_BYTES);
-                for (int cc = 0; cc < NCH; ++cc)
-                    tma_load_3d(smem + Ly::Q_OFF + cc * TC_BM * 128, &tmQ, q_full, cc * 64, it.q0, it.b * Hq + it.h);
-                for (int i = 0; i < it.n_tiles; ++i, ++g) {
-                    const int s = g % PS_KST, j = tile_j(it, i);
-                    const uint32_t free_ph = ((g / PS_KST) & 1) ^ 1;
-                    const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
-                    const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
-                    if (!mbar_wait_suspend(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
-                    mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
+    constexpr int W_VTMA = ALT ? 2 : 6, W_PV = ALT ? 3 : 7;
+    const bool producer = ALT ? warp < 4 : (warp < 2 || warp >= 6);
+    // with ALT the register split dominates each role's code, so that ptxas allocates it under the
+    // new limit
+    if (producer) {
+        if constexpr (ALT) setmaxnreg_dec<PS_REG_PRODUCER>();
+        if (warp == 0) {
+            // ---------------- TMA producer
+            if (lane == 0) {
+                int g = 0;
+                for (int round = 0; ok; ++round) {
+                    const Item it = item_of(round);
+                    if (it.n_tiles == 0) break;
+                    const int jkv = it.h / (Hq / Hkv);
+                    if (!mbar_wait_suspend(q_empty, (round & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(q_full, Ly::Q_BYTES);
                     for (int cc = 0; cc < NCH; ++cc)
-                        tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmK, &k_full[s], cc * 64, y, z);
+                        tma_load_3d(smem + Ly::Q_OFF + cc * TC_BM * 128, &tmQ, q_full, cc * 64, it.q0, it.b * Hq + it.h);
+                    for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                        const int s = g % PS_KST, j = tile_j(it, i);
+                        const uint32_t free_ph = ((g / PS_KST) & 1) ^ 1;
+                        const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
+                        const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
+                        if (!mbar_wait_suspend(&k_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                        mbar_expect_tx(&k_full[s], Ly::KV_BYTES);
+                        for (int cc = 0; cc < NCH; ++cc)
+                            tma_load_3d(smem + Ly::K_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmK, &k_full[s], cc * 64, y, z);
+                    }
                 }
             }
-        }
-    } else if (warp == 6) {
-        // ---------------- TMA producer for the value tiles, a warp of its own: a key stage is freed by
-        // its scores, a value stage by its P V, two tiles apart, so one in-order producer would hold
-        // back the keys of the scores that run ahead
-        if (lane == 0) {
-            int g = 0;
-            for (int round = 0; ok; ++round) {
-                const Item it = item_of(round);
-                if (it.n_tiles == 0) break;
-                const int jkv = it.h / (Hq / Hkv);
-                for (int i = 0; i < it.n_tiles; ++i, ++g) {
-                    const int s = g & 1, j = tile_j(it, i);
-                    const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
-                    const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
-                    const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
-                    if (!mbar_wait_suspend(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
-                    mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
-                    for (int cc = 0; cc < NCH; ++cc)
-                        tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmV, &v_full[s], cc * 64, y, z);
+        } else if (warp == W_VTMA) {
+            // ---------------- TMA producer for the value tiles, a warp of its own: a key stage is freed by
+            // its scores, a value stage by its P V, two tiles apart, so one in-order producer would hold
+            // back the keys of the scores that run ahead
+            if (lane == 0) {
+                int g = 0;
+                for (int round = 0; ok; ++round) {
+                    const Item it = item_of(round);
+                    if (it.n_tiles == 0) break;
+                    const int jkv = it.h / (Hq / Hkv);
+                    for (int i = 0; i < it.n_tiles; ++i, ++g) {
+                        const int s = g & 1, j = tile_j(it, i);
+                        const uint32_t free_ph = ((g >> 1) & 1) ^ 1;
+                        const int y = ring ? (j * TC_BN) % ring : j * TC_BN;
+                        const int z = (j * TC_BN < psh ? 0 : it.b) * Hkv + jkv;
+                        if (!mbar_wait_suspend(&v_empty[s], free_ph, abort_flag)) { ok = false; break; }
+                        mbar_expect_tx(&v_full[s], Ly::KV_BYTES);
+                        for (int cc = 0; cc < NCH; ++cc)
+                            tma_load_3d(smem + Ly::V_OFF + s * Ly::KV_BYTES + cc * TC_BN * 128, &tmV, &v_full[s], cc * 64, y, z);
+                    }
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ---------------- score MMAs: S of tile gi (key stage gi % PS_KST) into region gi % NR, once
-        // P V of tile gi - NR (issued by warp 7) has finished reading that region. A thread issuing
-        // tcgen05.mma waits while the pipe is full, so the score and the P V batches come from two
-        // threads: while one waits with its batch, the other's work keeps the pipe fed.
-        if (lane == 0) {
-            int g = 0;  // tiles of earlier items
+        } else if (warp == 1) {
+            // ---------------- score MMAs: S of tile gi (key stage gi % PS_KST) into region gi % NR, once
+            // P V of tile gi - NR (issued by the P V warp) has finished reading that region. A thread issuing
+            // tcgen05.mma waits while the pipe is full, so the score and the P V batches come from two
+            // threads: while one waits with its batch, the other's work keeps the pipe fed.
+            if (lane == 0) {
+                int g = 0;  // tiles of earlier items
+                for (int round = 0; ok; ++round) {
+                    const Item it = item_of(round);
+                    const int nt = it.n_tiles;
+                    if (nt == 0) break;
+                    if (!mbar_wait_suspend(q_full, round & 1, abort_flag)) { ok = false; break; }
+                    for (int i = 0; i < nt; ++i) {
+                        const int gi = g + i, s = gi % PS_KST, r = gi % NR;
+                        if (!mbar_wait_suspend(&k_full[s], (gi / PS_KST) & 1, abort_flag)) { ok = false; break; }
+                        // region r's next completion would be P V of tile gi itself, not yet possible: the
+                        // parity wait cannot alias
+                        if (gi >= NR && !mbar_wait_suspend(&r_free[r], ((gi - NR) / NR) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sq = smem_u32(smem + Ly::Q_OFF);
+                        const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < DH / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
+                            umma_bf16_ss(tmem + r * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off),
+                                         IDESC_S, kk > 0);
+                        }
+                        umma_commit(&s_full[r]);
+                        umma_commit(&k_empty[s]);
+                        if (i == nt - 1) umma_commit(q_empty);  // the item's last score releases Q
+                    }
+                    g += nt;
+                }
+            }
+        } else if (warp == W_PV) {
+            // ---------------- P V MMAs: O += P V of tile gi, P read from region gi % NR (A operand in
+            // tensor memory), V from value stage gi & 1
+            int g = 0;
             for (int round = 0; ok; ++round) {
                 const Item it = item_of(round);
                 const int nt = it.n_tiles;
                 if (nt == 0) break;
-                if (!mbar_wait_suspend(q_full, round & 1, abort_flag)) { ok = false; break; }
-                for (int i = 0; i < nt; ++i) {
-                    const int gi = g + i, s = gi % PS_KST, r = gi % NR;
-                    if (!mbar_wait_suspend(&k_full[s], (gi / PS_KST) & 1, abort_flag)) { ok = false; break; }
-                    // region r's next completion would be P V of tile gi itself, not yet possible: the
-                    // parity wait cannot alias
-                    if (gi >= NR && !mbar_wait_suspend(&r_free[r], ((gi - NR) / NR) & 1, abort_flag)) {
-                        ok = false;
-                        break;
+                for (int i = 0; ok && i < nt; ++i) {
+                    const int gi = g + i, s = gi & 1, r = gi % NR;
+                    const int j = tile_j(it, i);
+                    if (!__all_sync(0xffffffffu, mbar_wait_suspend(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
+                    uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
+                    const int r0 = it.n_valid - j * TC_BN;  // first stale key row of this tile
+                    if (r0 < TC_BN) {
+                        for (int e = lane; e < (TC_BN - r0) * 8 * NCH; e += 32) {
+                            const int cc = e / ((TC_BN - r0) * 8), rem = e % ((TC_BN - r0) * 8);
+                            reinterpret_cast<uint4*>(sv + cc * TC_BN * 128 + (r0 + rem / 8) * 128)[rem % 8] =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
                     }
-                    tc_fence_after();
-                    const uint32_t sq = smem_u32(smem + Ly::Q_OFF);
-                    const uint32_t sk = smem_u32(smem + Ly::K_OFF + s * Ly::KV_BYTES);
+                    __syncwarp();
+                    if (lane == 0) {
+                        bool w = i > 0 || mbar_wait_suspend(o_free, (round & 1) ^ 1, abort_flag);  // previous item's O read out
+                        w = w && mbar_wait_suspend(&p_full[r], (gi / NR) & 1, abort_flag);
+                        if (w) {
+                            tc_fence_after();
+                            const uint32_t svv = smem_u32(sv);
 #pragma unroll
-                    for (int kk = 0; kk < DH / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * TC_BM * 128 + (kk & 3) * 32;
-                        umma_bf16_ss(tmem + r * TC_BN, sdesc_kmajor_sw128(sq + off), sdesc_kmajor_sw128(sk + off),
-                                     IDESC_S, kk > 0);
+                            for (int kk = 0; kk < TC_BN / 16; ++kk) {
+                                const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
+                                umma_bf16_ts(tmem + TM_O, tmem + r * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
+                            }
+                            umma_commit(&v_empty[s]);
+                            umma_commit(&r_free[r]);
+                        }
+                        ok = w;
                     }
-                    umma_commit(&s_full[r]);
-                    umma_commit(&k_empty[s]);
-                    if (i == nt - 1) umma_commit(q_empty);  // the item's last score releases Q
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
                 }
                 g += nt;
             }
         }
-    } else if (warp == 7) {
-        // ---------------- P V MMAs: O += P V of tile gi, P read from region gi % NR (A operand in
-        // tensor memory), V from value stage gi & 1
+    } else if constexpr (ALT) {
+        setmaxnreg_inc<PS_REG_SOFTMAX>();
+        // ---------------- softmax warpgroups: thread <-> query row (TMEM lane); warpgroup wg takes the
+        // tiles whose global number has parity wg
+        const int wg = (warp >> 2) - 1;
+        const int quarter = warp & 3, row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tm_o = tmem + lane_off + TM_O;
+        const float sl2 = kLog2e / sqrtf((float)DH);
+        volatile float* m_sh = reinterpret_cast<volatile float*>(smem + Ly::XCH_OFF);  // [item parity][row]
+        volatile float* l_sh = m_sh + 2 * TC_BM;  // [item parity][warpgroup][row]
+        // P V of global tile k (and so every earlier one) has completed. The region's next completion
+        // would be P V of tile k + NR, which needs a P of this warpgroup that is not released yet
+        // (k + NR has the parity of the caller's tile k + 1), so the parity wait cannot alias.
+        auto pv_done = [&](int k) -> bool { return mbar_wait_suspend(&r_free[k % NR], (k / NR) & 1, abort_flag); };
+        // The row scales of global tile k are final. Barrier fin[quarter][k & 1] completes one phase
+        // per tile of that parity; its next phase needs tile k + 2, which waits for the caller's tile
+        // k + 1 to be final, so the parity wait cannot alias.
+        auto fin_wait = [&](int k) -> bool {
+            return mbar_wait_suspend(&fin[quarter * 2 + (k & 1)], (k >> 1) & 1, abort_flag);
+        };
         int g = 0;
         for (int round = 0; ok; ++round) {
             const Item it = item_of(round);
             const int nt = it.n_tiles;
             if (nt == 0) break;
-            for (int i = 0; ok && i < nt; ++i) {
-                const int gi = g + i, s = gi & 1, r = gi % NR;
+            const int t = it.q0 + row, pos = len0 + t;
+            volatile float* m_row = m_sh + (round & 1) * TC_BM + row;
+            float m_l = -INFINITY, l = 0.f;  // this warpgroup's share of the row sum, at scale m_l
+            for (int i = ((g & 1) == wg) ? 0 : 1; i < nt; i += 2) {
+                const int gi = g + i, r = gi % NR;
                 const int j = tile_j(it, i);
-                if (!__all_sync(0xffffffffu, mbar_wait_suspend(&v_full[s], (gi >> 1) & 1, abort_flag))) { ok = false; break; }
-                uint8_t* sv = smem + Ly::V_OFF + s * Ly::KV_BYTES;
-                const int r0 = it.n_valid - j * TC_BN;  // first stale key row of this tile
-                if (r0 < TC_BN) {
-                    for (int e = lane; e < (TC_BN - r0) * 8 * NCH; e += 32) {
-                        const int cc = e / ((TC_BN - r0) * 8), rem = e % ((TC_BN - r0) * 8);
-                        reinterpret_cast<uint4*>(sv + cc * TC_BN * 128 + (r0 + rem / 8) * 128)[rem % 8] =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    bool w = i > 0 || mbar_wait_suspend(o_free, (round & 1) ^ 1, abort_flag);  // previous item's O read out
-                    w = w && mbar_wait_suspend(&p_full[r], (gi / NR) & 1, abort_flag);
-                    if (w) {
-                        tc_fence_after();
-                        const uint32_t svv = smem_u32(sv);
+                const uint32_t tm_s = tmem + lane_off + r * TC_BN;
+                if (!__all_sync(0xffffffffu, mbar_wait_suspend(&s_full[r], (gi / NR) & 1, abort_flag))) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[TC_BN];
 #pragma unroll
-                        for (int kk = 0; kk < TC_BN / 16; ++kk) {
-                            const uint64_t bd = sdesc_mnmajor_sw128(svv + kk * 16 * 128, TC_BN * 128);
-                            umma_bf16_ts(tmem + TM_O, tmem + r * TC_BN + kk * 8, bd, IDESC_O, (i | kk) != 0);
-                        }
-                        umma_commit(&v_empty[s]);
-                        umma_commit(&r_free[r]);
+                for (int cc = 0; cc < TC_BN / 32; ++cc)
+                    tmem_ld_32x32b_x32(tm_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+                tmem_ld_wait();
+                const int k0 = j * TC_BN;
+                const bool diag = k0 + TC_BN - 1 > len0 + it.q0;
+                const bool pads = k0 < it.pe && k0 + TC_BN > it.ps;
+                const bool old = window > 0 && k0 < len0 + it.q_end - window;
+                if (pads || old) {
+                    // visible: (i <= lim, not padding, inside the window) or the query itself; branch-free
+                    const int lim = pos - k0;
+                    const int lo = window > 0 ? lim - window + 1 : -TC_BN;
+                    const int a1 = max(lo, 0), n1 = max(0, min(lim, it.ps - k0 - 1) - a1 + 1);
+                    const int a2 = max(lo, it.pe - k0), n2 = max(0, lim - a2 + 1);
+#pragma unroll
+                    for (int e = 0; e < TC_BN; ++e) {
+                        const bool vis =
+                            ((unsigned)(e - a1) < (unsigned)n1) | ((unsigned)(e - a2) < (unsigned)n2) | (e == lim);
+                        sr[e] = vis ? sr[e] : __float_as_uint(-INFINITY);
                     }
-                    ok = w;
+                } else if (diag) {
+                    const int lim = pos - k0;
+#pragma unroll
+                    for (int e = 0; e < TC_BN; ++e) sr[e] = e <= lim ? sr[e] : __float_as_uint(-INFINITY);
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                // P = 2^(s * sl2 - m) as packed bf16 into the first 64 columns of this tile's region (a row
+                // with no visible key yet keeps m = -inf and gets P = 0); rs2 = their row sum
+                auto exps = [&](float mref, float2& rs2) {
+                    const float nm = mref == -INFINITY ? 0.f : -mref;
+                    const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+                    rs2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 x = fma2(make_float2(__uint_as_float(sr[half * 64 + 2 * e]),
+                                                              __uint_as_float(sr[half * 64 + 2 * e + 1])),
+                                                  sl2x2, nmx2);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            rs2 = add2(rs2, pp);
+                            pk[e] = pack_bf16(pp.x, pp.y);
+                        }
+                        tmem_st_32x32b_x32(tm_s + half * 32, pk);
+                    }
+                };
+                // SPEC: the exponentials start with the scale published after this warpgroup's previous
+                // tile of the item (or later) while the tile maximum is reduced beside them; they are
+                // recomputed when the final scale differs. Decisions are warp-uniform (tcgen05.st is
+                // warp-wide).
+                const float m_ref = i >= 2 ? *m_row : -INFINITY;
+                float2 rs2;
+                const bool spec = SPEC && __all_sync(0xffffffffu, m_ref != -INFINITY);
+                if (spec) exps(m_ref, rs2);
+                float mx = -INFINITY;
+                if constexpr (SPEC) {
+                    float m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < TC_BN; e += 8) {
+                        mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                        m1 = fmax3(m1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+                        m2 = fmax3(m2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+                        m3 = fmax3(m3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+                    }
+                    mx = fmaxf(fmaxf(mx, m1), fmaxf(m2, m3));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < TC_BN; e += 2) mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                }
+                mx *= sl2;
+                // the scale after the previous tile of the item (final once that tile is)
+                if (i > 0 && !__all_sync(0xffffffffu, fin_wait(gi - 1))) { ok = false; break; }
+                const float m_prev = i > 0 ? *m_row : -INFINITY;
+                // lazy rescale, decided per row but executed by the whole warp
+                const bool grow = mx > m_prev + 8.0f;
+                const float m_new = grow ? mx : m_prev;
+                if (i > 0 && __any_sync(0xffffffffu, grow)) {
+                    // O holds P V of every earlier tile at scale m_prev
+                    const bool w = pv_done(gi - 1);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = grow ? ex2_approx(m_prev - mx) : 1.0f;
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                    for (int cc = 0; cc < DH / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(tm_o + cc * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 r2 = mul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                            o[e] = __float_as_uint(r2.x);
+                            o[e + 1] = __float_as_uint(r2.y);
+                        }
+                        tmem_st_32x32b_x32(tm_o + cc * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                if (!spec || __any_sync(0xffffffffu, m_new != m_ref)) {
+                    if (spec) tmem_st_wait();  // the speculative P is overwritten
+                    exps(m_new, rs2);
+                }
+                // this warpgroup's share of the row sum moves to the new scale (m_new > m_l, so finite)
+                if (m_new != m_l) {
+                    l *= ex2_approx(m_l - m_new);
+                    m_l = m_new;
+                }
+                tmem_st_wait();
+                l += rs2.x + rs2.y;
+                *m_row = m_new;
+                tc_fence_before();
+                mbar_arrive(&p_full[r]);
+                mbar_arrive(&fin[quarter * 2 + (gi & 1)]);  // releases the scale written above
             }
+            if (!ok) break;
+            // the item's last tile is final: the row's final scale, and (once its P V is done) O
+            const int last = g + nt - 1;
+            ok = __all_sync(0xffffffffu, fin_wait(last));
+            if (!ok) break;
+            const float m_fin = *m_row;
+            volatile float* l_row = l_sh + (round & 1) * 2 * TC_BM + row;
+            l_row[wg * TC_BM] = m_l == m_fin ? l : l * ex2_approx(m_l - m_fin);
+            mbar_arrive(&l_meet[quarter]);
+            ok = mbar_wait_suspend(&l_meet[quarter], round & 1, abort_flag) && pv_done(last);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            // O / l to the output, this warpgroup's half of the columns, then hand the accumulator back
+            tc_fence_after();
+            const float inv = 1.f / (l_row[0] + l_row[TC_BM]);
+            __nv_bfloat16* orow = out + (((size_t)it.b * T + t) * Hq + it.h) * DH + wg * (DH / 2);
+#pragma unroll 1
+            for (int cc = 0; cc < DH / 64; ++cc) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tm_o + wg * (DH / 2) + cc * 32, o);
+                tmem_ld_wait();
+                if (t < T) {
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        reinterpret_cast<uint4*>(orow + cc * 32)[v] =
+                            make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(o_free);
             g += nt;
         }
     } else {
@@ -1313,6 +1537,8 @@ cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, cons
 // 1x32768 5.99 -> 5.65 ms, 8B 1x8192 0.403 -> 0.389 ms, 0.6B 8x4096 0.462 -> 0.455 ms; 0.6B 1x2048,
 // 21 us either way, keeps the plain order).
 constexpr int kSpecMinKeys = 4096;
+// Key range from which the persistent kernel alternates tiles between two softmax warpgroups (ALT).
+constexpr int kAltMinKeys = 16384;
 
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
@@ -1338,11 +1564,14 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
     const long long items = (long long)((T + TC_BM - 1) / TC_BM) * Hq * B;
     const unsigned grid = (unsigned)std::min<long long>(items, device_sm_count());
+    if (kv_hint >= kAltMinKeys)
+        return launch_pdl(attn_prefill_persistent_kernel<DH, true, true>, dim3(grid), dim3(ps_threads<true>()),
+                          PsLayout<DH, true>::SMEM, st, tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
     if (kv_hint >= kSpecMinKeys)
-        return launch_pdl(attn_prefill_persistent_kernel<DH, true>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st,
-                          tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
-    return launch_pdl(attn_prefill_persistent_kernel<DH, false>, dim3(grid), dim3(PS_THREADS), PsLayout<DH>::SMEM, st,
-                      tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
+        return launch_pdl(attn_prefill_persistent_kernel<DH, true, false>, dim3(grid), dim3(ps_threads<false>()),
+                          PsLayout<DH, false>::SMEM, st, tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
+    return launch_pdl(attn_prefill_persistent_kernel<DH, false, false>, dim3(grid), dim3(ps_threads<false>()),
+                      PsLayout<DH, false>::SMEM, st, tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
 }
 
 }  // namespace
@@ -1436,13 +1665,16 @@ cudaError_t decode_prepare_dh() {
 cudaError_t attention_prepare() {
     const void* fns[] = {(const void*)attn_prefill_tc_kernel<128, 1>, (const void*)attn_prefill_tc_kernel<128, 2>,
                          (const void*)attn_prefill_tc_kernel<64, 1>,  (const void*)attn_prefill_tc_kernel<64, 2>,
-                         (const void*)attn_prefill_persistent_kernel<128, false>,
-                         (const void*)attn_prefill_persistent_kernel<64, false>,
-                         (const void*)attn_prefill_persistent_kernel<128, true>,
-                         (const void*)attn_prefill_persistent_kernel<64, true>};
+                         (const void*)attn_prefill_persistent_kernel<128, false, false>,
+                         (const void*)attn_prefill_persistent_kernel<64, false, false>,
+                         (const void*)attn_prefill_persistent_kernel<128, true, false>,
+                         (const void*)attn_prefill_persistent_kernel<64, true, false>,
+                         (const void*)attn_prefill_persistent_kernel<128, true, true>,
+                         (const void*)attn_prefill_persistent_kernel<64, true, true>};
     const int smem[] = {TcLayout<128, 1>::SMEM, TcLayout<128, 2>::SMEM, TcLayout<64, 1>::SMEM, TcLayout<64, 2>::SMEM,
-                        PsLayout<128>::SMEM, PsLayout<64>::SMEM, PsLayout<128>::SMEM, PsLayout<64>::SMEM};
-    for (int i = 0; i < 8; ++i) {
+                        PsLayout<128, false>::SMEM, PsLayout<64, false>::SMEM, PsLayout<128, false>::SMEM,
+                        PsLayout<64, false>::SMEM, PsLayout<128, true>::SMEM,  PsLayout<64, true>::SMEM};
+    for (int i = 0; i < 10; ++i) {
         cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
         if (e != cudaSuccess) return e;
     }

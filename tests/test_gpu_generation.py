@@ -347,13 +347,13 @@ def test_prefill_attention_window_ring_op(bd, heads):
             assert rel_l2(got[b, t], ref) <= 1e-2, (b, t)
 
 
-@pytest.mark.parametrize("heads,T", [(1, 300), (2, 300), (1, 4200)])
+@pytest.mark.parametrize("heads,T", [(1, 300), (2, 300), (1, 4200), (1, 16500)])
 def test_prefill_attention_padding_op(bd, heads, T):
     """Prefill attention with left padding at the start of the block (a padded prompt batch), one and two
     heads per CTA, against masked oracle rows: a real token sees the real slots up to its own, a padding
     slot sees only itself. Row 2's padding covers the first 128-slot tile whole (skipped by the kernels).
     At 4200 keys the persistent kernel takes its speculative form, where the rows of one warp reach their
-    first visible key at different tiles."""
+    first visible key at different tiles; at 16500 keys its alternating form (two softmax warpgroups)."""
     rng = np.random.default_rng(92)
     B, Hq, Hkv, dh = 3, 8, 2, 128
     pads = [0, 37, 200]

@@ -374,14 +374,15 @@ def test_attention_decode(bd, Bq, Hq, Hkv, dh, n, extra):
     assert max_rel_rows(got, ref, dh) <= 3e-2
 
 
-@pytest.mark.parametrize("T,window", [(16384 + 77, 0), (16500, 1000)])
-def test_attention_prefill_long_keys(bd, T, window):
-    """Key ranges of 4096 and more take the speculative form of the persistent kernel (the exponentials
-    start with the running maximum and are recomputed for a warp when one of its rows grew). With a sliding
-    window, rows of one warp reach their first visible key at different tiles. Sampled rows against the
-    oracle's brute-force row, per-row bounds included; slots past the prompt hold NaN."""
-    rng = np.random.default_rng(T + window)
-    Bq, Hq, Hkv, dh = 1, 4, 2, 128
+@pytest.mark.parametrize("T,window,dh", [(16384 + 77, 0, 128), (16500, 1000, 128), (16384 + 77, 0, 64)])
+def test_attention_prefill_long_keys(bd, T, window, dh):
+    """Key ranges of 16384 and more take the alternating form of the persistent kernel: two softmax
+    warpgroups take alternate key tiles and hand each row's scale from tile to tile; the exponentials start
+    with the scale known so far and are recomputed when it moved. With a sliding window, rows of one warp
+    reach their first visible key at different tiles. Sampled rows against the oracle's brute-force row,
+    per-row bounds included; slots past the prompt hold NaN."""
+    rng = np.random.default_rng(T + window + dh)
+    Bq, Hq, Hkv = 1, 4, 2
     cap = T + 3
     q = rand_bf16(rng, (Bq, Hq, T, dh))
     kc = rand_bf16(rng, (Bq, Hkv, cap, dh))
