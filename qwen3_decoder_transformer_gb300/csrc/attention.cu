@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
             const bool pads = k0 < pe && k0 + TC_BN > ps;
             const bool old = window > 0 && k0 < len0 + q_end - window;
             if (pads || old) {
-                // key i is visible iff (i <= lim, not padding, inside the window) or it is the query
+                // key e is visible iff (e <= lim, not padding, inside the window) or it is the query
                 // itself: two intervals, before and after the padding, plus the query's own slot.
                 // Branch-free (unsigned range tests): a short-circuit form diverges per element.
                 const int lim = pos - k0;
@@ -277,18 +277,18 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
                 const int a1 = max(lo, 0), n1 = max(0, min(lim, ps - k0 - 1) - a1 + 1);
                 const int a2 = max(lo, pe - k0), n2 = max(0, lim - a2 + 1);
 #pragma unroll
-                for (int i = 0; i < TC_BN; ++i) {
-                    const bool vis = ((unsigned)(i - a1) < (unsigned)n1) | ((unsigned)(i - a2) < (unsigned)n2) | (i == lim);
-                    sr[i] = vis ? sr[i] : __float_as_uint(-INFINITY);
+                for (int e = 0; e < TC_BN; ++e) {
+                    const bool vis = ((unsigned)(e - a1) < (unsigned)n1) | ((unsigned)(e - a2) < (unsigned)n2) | (e == lim);
+                    sr[e] = vis ? sr[e] : __float_as_uint(-INFINITY);
                 }
             } else if (diag) {  // only the causal diagonal: keys past the query's slot
                 const int lim = pos - k0;
 #pragma unroll
-                for (int i = 0; i < TC_BN; ++i) sr[i] = i <= lim ? sr[i] : __float_as_uint(-INFINITY);
+                for (int e = 0; e < TC_BN; ++e) sr[e] = e <= lim ? sr[e] : __float_as_uint(-INFINITY);
             }
             float mx = -INFINITY;  // three-input maxima: two scores per instruction
 #pragma unroll
-            for (int i = 0; i < TC_BN; i += 2) mx = fmax3(mx, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+            for (int e = 0; e < TC_BN; e += 2) mx = fmax3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
             mx *= sl2;
             // lazy rescale, decided per row but executed by the whole warp (tcgen05.ld/st are warp-wide)
             const bool grow = mx > m_used + 8.0f;
@@ -1540,6 +1540,20 @@ constexpr int kSpecMinKeys = 4096;
 // Key range from which the persistent kernel alternates tiles between two softmax warpgroups (ALT).
 constexpr int kAltMinKeys = 16384;
 
+// setmaxnreg.inc waits until the registers it asks for are free, so the ALT form runs only when the
+// compiled kernel was given at least the registers per thread its split hands out (checked once).
+template <int DH>
+bool alt_registers_cover_split() {
+    static const bool ok = [] {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, attn_prefill_persistent_kernel<DH, true, true>) != cudaSuccess) return false;
+        const long long have = (long long)ps_threads<true>() * fa.numRegs;
+        const long long need = 128LL * PS_REG_PRODUCER + 256LL * PS_REG_SOFTMAX;
+        return have >= need;
+    }();
+    return ok;
+}
+
 template <int DH>
 cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int B, int T,
                               int Hq, int Hkv, int cap, const int* len0, SeqMap sm, __nv_bfloat16* out, int* err,
@@ -1564,7 +1578,7 @@ cudaError_t prefill_launch_dh(const __nv_bfloat16* q, const __nv_bfloat16* kc, c
         return prefill_launch_nh<DH, 1>(tq, tk, tv, B, T, Hq, Hkv, len0, sm, out, err, split, max_chunks, ws, st);
     const long long items = (long long)((T + TC_BM - 1) / TC_BM) * Hq * B;
     const unsigned grid = (unsigned)std::min<long long>(items, device_sm_count());
-    if (kv_hint >= kAltMinKeys)
+    if (kv_hint >= kAltMinKeys && alt_registers_cover_split<DH>())
         return launch_pdl(attn_prefill_persistent_kernel<DH, true, true>, dim3(grid), dim3(ps_threads<true>()),
                           PsLayout<DH, true>::SMEM, st, tq, tk, tv, T, Hq, Hkv, B, len0, sm.meta, sm.window, sm.ring, out, err);
     if (kv_hint >= kSpecMinKeys)
