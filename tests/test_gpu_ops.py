@@ -374,23 +374,26 @@ def test_attention_decode(bd, Bq, Hq, Hkv, dh, n, extra):
     assert max_rel_rows(got, ref, dh) <= 3e-2
 
 
-@pytest.mark.parametrize("T,window,dh", [(16384 + 77, 0, 128), (16500, 1000, 128), (16384 + 77, 0, 64)])
-def test_attention_prefill_long_keys(bd, T, window, dh):
+@pytest.mark.parametrize("T,window,dh,len0", [(16384 + 77, 0, 128, 0), (16500, 1000, 128, 0), (16384 + 77, 0, 64, 0),
+                                               (16384 + 77, 0, 128, 300)])
+def test_attention_prefill_long_keys(bd, T, window, dh, len0):
     """Key ranges of 16384 and more take the alternating form of the persistent kernel: two softmax
     warpgroups take alternate key tiles and hand each row's scale from tile to tile; the exponentials start
     with the scale known so far and are recomputed when it moved. With a sliding window, rows of one warp
-    reach their first visible key at different tiles. Sampled rows against the oracle's brute-force row,
-    per-row bounds included; slots past the prompt hold NaN."""
-    rng = np.random.default_rng(T + window + dh)
+    reach their first visible key at different tiles; with len0 cached tokens the block's query t sees
+    slots 0..len0 + t (a chunk after a prefix). Sampled rows against the oracle's brute-force row, per-row
+    bounds included; slots past the block hold NaN."""
+    rng = np.random.default_rng(T + window + dh + len0)
     Bq, Hq, Hkv = 1, 4, 2
-    cap = T + 3
+    n = len0 + T
+    cap = n + 3
     q = rand_bf16(rng, (Bq, Hq, T, dh))
     kc = rand_bf16(rng, (Bq, Hkv, cap, dh))
     vc = rand_bf16(rng, (Bq, Hkv, cap, dh))
-    kc[:, :, T:] = 0x7FC0
-    vc[:, :, T:] = 0x7FC0
+    kc[:, :, n:] = 0x7FC0
+    vc[:, :, n:] = 0x7FC0
     out = torch.empty(Bq * T, Hq * dh, dtype=torch.bfloat16, device="cuda")
-    len_t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    len_t = torch.tensor([len0], dtype=torch.int32, device="cuda")
     err = _err()
     bd.op_attention_prefill(dev(q), dev(kc), dev(vc), len_t, out, err=err, window=window)
     torch.cuda.synchronize()
@@ -398,9 +401,10 @@ def test_attention_prefill_long_keys(bd, T, window, dh):
     got = widen(bits(out)).reshape(T, Hq * dh)
     rows = sorted({0, 1, 127, 128, 999, 1000, 1001, 5000, 8191, 12345, 16383, T - 2, T - 1})
     for t in rows:
-        lo = max(0, t + 1 - window) if window else 0
-        ref = O.attention_gqa_row_f64(np.ascontiguousarray(q[0, :, t]), np.ascontiguousarray(kc[0][:, lo:t + 1]),
-                                      np.ascontiguousarray(vc[0][:, lo:t + 1]), t + 1 - lo).ravel()
+        p = len0 + t  # the query's own slot
+        lo = max(0, p + 1 - window) if window else 0
+        ref = O.attention_gqa_row_f64(np.ascontiguousarray(q[0, :, t]), np.ascontiguousarray(kc[0][:, lo:p + 1]),
+                                      np.ascontiguousarray(vc[0][:, lo:p + 1]), p + 1 - lo).ravel()
         assert np.isfinite(got[t]).all(), t
         assert rel_l2(got[t], ref) <= 1e-2, t
         assert max_rel_rows(got[t], ref, dh) <= 3e-2, t
