@@ -56,32 +56,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait for the phase with the given parity to complete. Gives up (returns false) when another role
-// has raised *abort or after kWaitTimeoutNs; the caller then flags the error and unwinds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) return false;
-        }
-    }
-}
-
-// The same with a suspend-time hint: the waiting thread is parked by the hardware until the phase
-// completes (or about 1 ms passes) instead of polling, which leaves its sub-partition's issue slots to
-// the warps that share it.
+// One test of the phase with the given parity, with a suspend-time hint: the thread is parked by the
+// hardware until the phase completes or about 1 ms passes.
 __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -91,6 +67,9 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
+// Wait for the phase with the given parity to complete, parked rather than polling, which leaves the
+// sub-partition's issue slots to the warps that share it. Gives up (returns false) when another role has
+// raised *abort or after kWaitTimeoutNs; the caller then flags the error and unwinds.
 __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait_suspend(bar, parity)) return true;
     uint64_t t0 = globaltimer();
