@@ -324,8 +324,15 @@ __device__ __forceinline__ bool epilogue_residual_norm(const GemmArgs& a, const 
         }
     }
     if (!epi_agree<NT>(met, es.fail)) return false;
-    float tot = 0.f;  // fixed order: column tile, then half
-    for (int q = 0; q < 2 * csize; ++q) tot += __ldcg(a.norm.part + (rb * csize * 2 + q) * BM + r);
+    // the row block's partial sums (at most 8 column tiles x 2 halves), all loads in flight at once, then
+    // added in a fixed order: column tile, then half
+    float pv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) pv[q] = q < 2 * csize ? __ldcg(a.norm.part + (rb * csize * 2 + q) * BM + r) : 0.f;
+    float tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        if (q < 2 * csize) tot += pv[q];
     const float rn = __frsqrt_rn(tot / (float)(csize * BN) + a.norm.eps);
 #pragma unroll 1
     for (int p = 0; p < PASSES; ++p) {
