@@ -888,16 +888,18 @@ __global__ void __launch_bounds__(ps_threads<ALT>(), 1)
                 mbar_arrive(&fin[quarter * 2 + (gi & 1)]);  // releases the scale written above
             }
             if (!ok) break;
-            // the item's last tile is final: the row's final scale, and (once its P V is done) O
+            // the item's last tile is final: the row's final scale, and once its P V is done, O. Both
+            // waits come before the meeting, which neither warpgroup passes before both arrive, so no
+            // tile of the next item (whose P V would complete the region barrier's next phase) can run
+            // before both waits are over.
             const int last = g + nt - 1;
-            ok = __all_sync(0xffffffffu, fin_wait(last));
+            ok = __all_sync(0xffffffffu, fin_wait(last) && pv_done(last));
             if (!ok) break;
             const float m_fin = *m_row;
             volatile float* l_row = l_sh + (round & 1) * 2 * TC_BM + row;
             l_row[wg * TC_BM] = m_l == m_fin ? l : l * ex2_approx(m_l - m_fin);
             mbar_arrive(&l_meet[quarter]);
-            ok = mbar_wait_suspend(&l_meet[quarter], round & 1, abort_flag) && pv_done(last);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait_suspend(&l_meet[quarter], round & 1, abort_flag));
             if (!ok) break;
             // O / l to the output, this warpgroup's half of the columns, then hand the accumulator back
             tc_fence_after();
