@@ -472,8 +472,9 @@ __global__ void __launch_bounds__(TcLayout<DH, NH>::THREADS, 1)
 // the item, where each warpgroup writes half of the output columns. Warpgroup 0 holds the producers
 // (warp 0 keys, 1 score MMAs, 2 values, 3 P V MMAs) and gives registers to the softmax warpgroups
 // (setmaxnreg). The first two tiles of an item run without speculation and the second waits for the
-// first, which costs more than the alternation saves on items of about 30 tiles or fewer (measured:
-// 8B 1x32768 5.69 -> 5.36 ms, 8B 1x8192 equal, 0.6B 8x4096 0.46 -> 0.51 ms).
+// first, which costs more than the alternation saves on items of about 16 tiles or fewer (measured,
+// shapes timed in both orders: 8B 1x32768 5.65 -> 5.21-5.25 ms, 8B 1x8192 0.391 -> 0.364 ms, 0.6B
+// 8x4096 0.447 -> 0.472 ms, 0.6B 1x2048 20.3 -> 22.0 us).
 template <bool ALT>
 constexpr int ps_threads() { return ALT ? 128 + 256 : 64 + 128 + 64; }
 constexpr int PS_KST = 3, PS_VST = 2;  // key and value ring stages
@@ -1541,7 +1542,7 @@ cudaError_t prefill_launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, cons
 // 21 us either way, keeps the plain order).
 constexpr int kSpecMinKeys = 4096;
 // Key range from which the persistent kernel alternates tiles between two softmax warpgroups (ALT).
-constexpr int kAltMinKeys = 16384;
+constexpr int kAltMinKeys = 8192;
 
 // setmaxnreg.inc waits until the registers it asks for are free, so the ALT form runs only when the
 // compiled kernel was given at least the registers per thread its split hands out (checked once).

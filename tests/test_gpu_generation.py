@@ -353,7 +353,8 @@ def test_prefill_attention_padding_op(bd, heads, T):
     heads per CTA, against masked oracle rows: a real token sees the real slots up to its own, a padding
     slot sees only itself. Row 2's padding covers the first 128-slot tile whole (skipped by the kernels).
     At 4200 keys the persistent kernel takes its speculative form, where the rows of one warp reach their
-    first visible key at different tiles; at 16500 keys its alternating form (two softmax warpgroups)."""
+    first visible key at different tiles; at 16500 keys its alternating form (two softmax warpgroups, used from
+    8192 keys)."""
     rng = np.random.default_rng(92)
     B, Hq, Hkv, dh = 3, 8, 2, 128
     pads = [0, 37, 200]
